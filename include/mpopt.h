@@ -1,0 +1,259 @@
+/*
+ * mpopt.h -- C ABI of the GB300 mixed-precision optimizer step (libmpopt.so).
+ *
+ * One optimizer step over fp32 master weights ("main_param"), fp32 reduced
+ * gradients ("main_grad") and fp32 optimizer state, ending with the bf16 copy
+ * of every master weight written back to the model:
+ *
+ *   - AdamW for every tensor routed to it (opt_adamw_step), as defined in
+ *     "02 · Optimizer：算法与 infra" §2 (Adam, bias correction, eps outside the
+ *     square root) and §3 (decoupled weight decay, AdamW Algorithm 2);
+ *   - Muon for 2-D hidden matrices (opt_muon_step), as defined in the same
+ *     page §1 (momentum and Nesterov as lerp), §5.2 (Newton-Schulz quintic),
+ *     §5.4 (decoupled decay, Eq. 3; update scaled by 0.2*sqrt(max(A, B)),
+ *     Eq. 4), and in "优化器：AdamW、Muon 与分布式优化器", Muon section;
+ *   - both at once with the routing rule of §5.5 / §14.2 (opt_mixed_step):
+ *     a tensor is a Muon tensor when it is 2-D and not an embedding or an
+ *     output (LM head) parameter; every other tensor goes to AdamW;
+ *   - the bf16 writeback of §9.2 ("参数写回": master -> model copy), done in
+ *     the same kernels, round-to-nearest-even.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Every data pointer is a DEVICE pointer owned by the caller (for example
+ *    torch.Tensor.data_ptr()).  The library allocates nothing and keeps no
+ *    state between calls: optimizer state lives in the caller's buffers and
+ *    scratch space in the caller's workspace.
+ *  - Updates are in place.  Tensors are dense, row-major, element-contiguous.
+ *    fp32 pointers must be 4-byte aligned and bf16 pointers 2-byte aligned;
+ *    any other alignment is handled (unaligned heads and tails take a scalar
+ *    path).  Tensors in one call must not overlap.
+ *  - Work is enqueued on `stream` (a cudaStream_t; NULL is the legacy default
+ *    stream) and runs asynchronously.  Argument errors are detected on the host
+ *    before anything is enqueued and return a status; nothing runs then.
+ *    A failed launch returns OPT_ERR_CUDA (the CUDA error text is available
+ *    from opt_last_cuda_error()).
+ *  - Device-side waits in the tensor-core kernels are bounded in time.  A wait
+ *    that runs out records a code in the workspace header; opt_device_status()
+ *    reads it.  Each step clears the header first.
+ *  - Thread safety: calls that share a workspace must be serialised on one
+ *    stream.
+ */
+#ifndef MPOPT_H
+#define MPOPT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MPOPT_API __attribute__((visibility("default")))
+#else
+#define MPOPT_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  OPT_OK = 0,
+  OPT_ERR_INVALID_ARG = 1,   /* null pointer, bad size/shape/hyper-parameter  */
+  OPT_ERR_UNSUPPORTED = 2,   /* a case this library does not implement        */
+  OPT_ERR_MISALIGNED = 3,    /* fp32 pointer not 4-byte / bf16 not 2-byte aligned */
+  OPT_ERR_WORKSPACE = 4,     /* workspace null, too small or not 256-B aligned */
+  OPT_ERR_CUDA = 5,          /* a CUDA runtime/driver call or launch failed    */
+  OPT_ERR_DEVICE_TIMEOUT = 6 /* a bounded device-side wait ran out (device status) */
+} opt_status;
+
+/* Routing of one tensor (opt_tensor.kind). */
+enum {
+  OPT_KIND_AUTO = 0,   /* opt_mixed_step decides: Muon iff ndim == 2 and not
+                          flagged OPT_FLAG_EMBEDDING_OR_OUTPUT                  */
+  OPT_KIND_ADAMW = 1,
+  OPT_KIND_MUON = 2
+};
+
+/* opt_tensor.flags */
+enum { OPT_FLAG_EMBEDDING_OR_OUTPUT = 1 };
+
+/*
+ * AdamW hyper-parameters for one step ("02 · Optimizer：算法与 infra" §2, §3).
+ *   lr            eta, the step size
+ *   beta1, beta2  EMA factors of the first and second raw moments, in [0, 1)
+ *   eps           added OUTSIDE the square root: mhat / (sqrt(vhat) + eps)
+ *   weight_decay  lambda, decoupled: theta <- theta * (1 - lr*lambda) - lr*update
+ *   step          t >= 1, the number of this step (bias corrections 1 - beta^t)
+ * The per-step scalars 1-beta1, 1-beta2, 1-beta1^t, 1-beta2^t and 1-lr*lambda are
+ * formed in double precision from these values and rounded once to float; each
+ * element is then evaluated in fp32 in the order written above, every operation
+ * rounded to nearest (no fused multiply-add).
+ */
+typedef struct {
+  float lr;
+  float beta1;
+  float beta2;
+  float eps;
+  float weight_decay;
+  int32_t reserved;
+  int64_t step;
+} opt_adamw_hp;
+
+/*
+ * Muon hyper-parameters ("02 · Optimizer：算法与 infra" §1, §5.2, §5.4, §14.1).
+ *   lr            eta
+ *   momentum      mu in [0, 1): m <- lerp(m, g, 1 - mu)
+ *   weight_decay  lambda, decoupled, applied to W_{t-1}
+ *   eps           Newton-Schulz normalisation X = G / (||G||_F + eps); 1e-7
+ *   nesterov      nonzero: Newton-Schulz input lerp(g, m, mu); zero: m
+ *   ns_steps      number of quintic iterations, 0..16 (5 on the pages)
+ *   ns_a, ns_b, ns_c  quintic coefficients, (3.4445, -4.7750, 2.0315)
+ *   scale_coeff   update scale factor k in k*sqrt(max(A, B)); 0.2
+ */
+typedef struct {
+  float lr;
+  float momentum;
+  float weight_decay;
+  float eps;
+  int32_t nesterov;
+  int32_t ns_steps;
+  float ns_a;
+  float ns_b;
+  float ns_c;
+  float scale_coeff;
+} opt_muon_hp;
+
+/*
+ * One parameter tensor.
+ *   main_param   fp32 [rows*cols]   master weights, updated in place
+ *   main_grad    fp32 [rows*cols]   this step's gradient, read only
+ *   exp_avg      fp32 [rows*cols]   AdamW first moment m / Muon momentum buffer
+ *   exp_avg_sq   fp32 [rows*cols]   AdamW second moment v; ignored for Muon
+ *   model_param  bf16 [rows*cols]   written with the rounded master; NULL means
+ *                                   the model parameter is itself fp32 (it IS
+ *                                   main_param) and nothing is written back
+ *   rows, cols   the shape; a 1-D tensor of n elements is rows = 1, cols = n,
+ *                ndim = 1.  Muon requires ndim == 2, rows >= 1, cols >= 1.
+ *                rows*cols == 0 is allowed and does nothing.
+ *   ndim         the parameter's dimensionality (used by OPT_KIND_AUTO)
+ *   kind, flags  routing, see above
+ */
+typedef struct {
+  float* main_param;
+  const float* main_grad;
+  float* exp_avg;
+  float* exp_avg_sq;
+  uint16_t* model_param;
+  int64_t rows;
+  int64_t cols;
+  int32_t ndim;
+  int32_t kind;
+  int32_t flags;
+  int32_t reserved;
+} opt_tensor;
+
+/*
+ * Bytes of device workspace that opt_mixed_step (and the other steps) need for
+ * this tensor list: a 256-byte status header and the Newton-Schulz buffers of
+ * the largest group of same-shape Muon matrices (fp32 and bf16 copies of the
+ * iterate, its bf16 transpose twice, the fp32 Gram matrix, the bf16
+ * polynomial).  AdamW needs no workspace: 0 for a list without Muon tensors.
+ * `routing` selects how kinds are interpreted: OPT_KIND_AUTO as in
+ * opt_mixed_step, OPT_KIND_ADAMW treats every tensor as AdamW, OPT_KIND_MUON
+ * every tensor as Muon.  Returns 0 if the list is invalid.
+ * A smaller workspace is accepted by the Muon path as long as one matrix of
+ * each shape fits; matrices are then processed in smaller groups.
+ */
+MPOPT_API size_t opt_workspace_size(const opt_tensor* tensors, int32_t n, int32_t routing);
+
+/*
+ * AdamW step over a list of n tensors (n >= 0): a multi-tensor kernel over
+ * 16K-element chunks whose tensor table travels in the kernel's parameter
+ * space, one launch per 400 tensors.  kind/flags are ignored.  exp_avg_sq
+ * must be non-null.  No workspace is needed (workspace may be NULL).
+ */
+MPOPT_API opt_status opt_adamw_step(const opt_adamw_hp* hp, const opt_tensor* tensors, int32_t n,
+                          void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Muon step for one 2-D matrix t (t->ndim must be 2): momentum, Nesterov,
+ * Newton-Schulz on the wide orientation (transposed when rows > cols),
+ * W <- W (1 - lr*lambda) - lr * scale_coeff * sqrt(max(rows, cols)) * O, and
+ * bf16 writeback.  exp_avg is the momentum buffer; exp_avg_sq is ignored.
+ */
+MPOPT_API opt_status opt_muon_step(const opt_muon_hp* hp, const opt_tensor* t,
+                         void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * The whole mixed step: routes each tensor (kind/flags), runs one AdamW
+ * launch over all AdamW tensors, and Muon over all Muon matrices, batching
+ * matrices of the same (min, max) shape into shared tensor-core launches.
+ * hp_muon may be NULL when no tensor routes to Muon, hp_adamw when none
+ * routes to AdamW.
+ */
+MPOPT_API opt_status opt_mixed_step(const opt_muon_hp* hp_muon, const opt_adamw_hp* hp_adamw,
+                          const opt_tensor* tensors, int32_t n,
+                          void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Newton-Schulz orthogonalisation alone ("02 · Optimizer：算法与 infra" §5.2):
+ * O = NS_steps(G) for one fp32 rows x cols matrix G, same bf16/tf32 tensor-core
+ * path as opt_muon_step.  G and O are device fp32 [rows*cols]; O may alias G.
+ * Workspace: opt_workspace_size of a one-matrix Muon list of that shape.
+ */
+MPOPT_API opt_status opt_newton_schulz(const float* G, float* O, int64_t rows, int64_t cols,
+                             int32_t ns_steps, float a, float b, float c, float eps,
+                             void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Synchronises `stream` and reports whether a kernel of the last step on this
+ * workspace recorded a device-side timeout (OPT_ERR_DEVICE_TIMEOUT) or not
+ * (OPT_OK).  Returns OPT_ERR_CUDA if the synchronisation itself fails.
+ */
+MPOPT_API opt_status opt_device_status(const void* workspace, void* stream);
+
+/*
+ * Optional launch instrumentation (off by default).  After
+ *   opt_profile_launches(events, info, capacity, &count)
+ * every kernel this library launches from the calling thread is bracketed by
+ * cudaEventRecord(events[2*i]) and cudaEventRecord(events[2*i+1]) on the
+ * launch's stream, and info[i] describes it, for i = count, count+1, ...
+ * while count < capacity (count is incremented by the library, also past
+ * capacity, so the caller learns how many launches there were).  `events`
+ * holds 2*capacity cudaEvent_t created by the caller; `info` and `count` are
+ * host memory owned by the caller and must stay valid until
+ * opt_profile_launches(NULL, NULL, 0, NULL) switches it off.
+ */
+typedef struct {
+  int32_t kernel;   /* OPT_KERNEL_* */
+  int32_t count;    /* matrices (Newton-Schulz, Muon stages) or tensors (AdamW) */
+  int64_t a;        /* Newton-Schulz: A = min(rows, cols); AdamW: elements */
+  int64_t b;        /* Newton-Schulz: B = max(rows, cols) */
+} opt_launch_info;
+
+enum {
+  OPT_KERNEL_NS_GRAM = 0,    /* X X^T, bf16 tensor cores     */
+  OPT_KERNEL_NS_POLY = 1,    /* b A + c A A, tf32 tensor cores */
+  OPT_KERNEL_NS_BX = 2,      /* a X + B X, bf16 tensor cores (last one also updates W) */
+  OPT_KERNEL_ADAMW = 3,
+  OPT_KERNEL_MUON_PREP = 4,  /* momentum, Nesterov, operand copies, norm partials */
+  OPT_KERNEL_MUON_NORM = 5,
+  OPT_KERNEL_MUON_APPLY = 6  /* ns_steps == 0 only */
+};
+
+MPOPT_API opt_status opt_profile_launches(void* const* events, opt_launch_info* info, int32_t capacity,
+                                          int32_t* count);
+
+/* Static text for a status code. */
+MPOPT_API const char* opt_strerror(opt_status status);
+
+/* Text of the last CUDA error seen by this thread's calls ("" if none). */
+MPOPT_API const char* opt_last_cuda_error(void);
+
+/* ABI version: (major << 16) | minor. */
+MPOPT_API int32_t opt_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MPOPT_H */

@@ -1,0 +1,319 @@
+"""GB300 mixed-precision optimizer step: Python binding of ``libmpopt.so``.
+
+This module only marshals arguments: it checks dtypes, devices and layouts of
+PyTorch tensors, packs their device pointers into the C structs of
+``include/mpopt.h`` and calls the library on the current CUDA stream.  Every
+step of the optimizer runs in the library's CUDA kernels.  If the library has
+not been built, importing works but every call raises ``MpoptUnavailable``.
+
+Entry points (same names as the C ABI, without the ``opt_`` prefix):
+
+* ``adamw_step``      -- AdamW over a list of tensors
+* ``muon_step``       -- Muon for one 2-D matrix
+* ``mixed_step``      -- both, with the Muon/AdamW routing rule
+* ``newton_schulz``   -- Newton-Schulz orthogonalisation alone
+* ``workspace_size``  -- device scratch bytes a call needs
+* ``device_status``   -- reads the device-side status word of a workspace
+"""
+
+from __future__ import annotations
+
+import ctypes
+import dataclasses
+import os
+from typing import Optional, Sequence
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmpopt.so")
+
+OPT_OK = 0
+STATUS_NAMES = {0: "OPT_OK", 1: "OPT_ERR_INVALID_ARG", 2: "OPT_ERR_UNSUPPORTED", 3: "OPT_ERR_MISALIGNED",
+                4: "OPT_ERR_WORKSPACE", 5: "OPT_ERR_CUDA", 6: "OPT_ERR_DEVICE_TIMEOUT"}
+KIND_AUTO, KIND_ADAMW, KIND_MUON = 0, 1, 2
+FLAG_EMBEDDING_OR_OUTPUT = 1
+NS_COEFFS = (3.4445, -4.7750, 2.0315)
+
+
+class MpoptUnavailable(RuntimeError):
+    """The compiled library is missing or failed to load."""
+
+
+class MpoptError(RuntimeError):
+    def __init__(self, status, where, detail=""):
+        self.status = status
+        super().__init__(f"{where}: {STATUS_NAMES.get(status, status)}"
+                         + (f" ({detail})" if detail else ""))
+
+
+class OptTensor(ctypes.Structure):
+    _fields_ = [("main_param", ctypes.c_void_p), ("main_grad", ctypes.c_void_p),
+                ("exp_avg", ctypes.c_void_p), ("exp_avg_sq", ctypes.c_void_p),
+                ("model_param", ctypes.c_void_p), ("rows", ctypes.c_int64), ("cols", ctypes.c_int64),
+                ("ndim", ctypes.c_int32), ("kind", ctypes.c_int32), ("flags", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
+
+
+class OptAdamwHP(ctypes.Structure):
+    _fields_ = [("lr", ctypes.c_float), ("beta1", ctypes.c_float), ("beta2", ctypes.c_float),
+                ("eps", ctypes.c_float), ("weight_decay", ctypes.c_float), ("reserved", ctypes.c_int32),
+                ("step", ctypes.c_int64)]
+
+
+class OptMuonHP(ctypes.Structure):
+    _fields_ = [("lr", ctypes.c_float), ("momentum", ctypes.c_float), ("weight_decay", ctypes.c_float),
+                ("eps", ctypes.c_float), ("nesterov", ctypes.c_int32), ("ns_steps", ctypes.c_int32),
+                ("ns_a", ctypes.c_float), ("ns_b", ctypes.c_float), ("ns_c", ctypes.c_float),
+                ("scale_coeff", ctypes.c_float)]
+
+
+_lib = None
+
+EXPORTED = ("opt_workspace_size", "opt_adamw_step", "opt_muon_step", "opt_mixed_step",
+            "opt_newton_schulz", "opt_device_status", "opt_profile_launches", "opt_strerror",
+            "opt_last_cuda_error", "opt_abi_version")
+
+KERNEL_NAMES = {0: "ns_gram", 1: "ns_poly", 2: "ns_bx", 3: "adamw", 4: "muon_prep", 5: "muon_norm",
+                6: "muon_apply"}
+
+
+class OptLaunchInfo(ctypes.Structure):
+    _fields_ = [("kernel", ctypes.c_int32), ("count", ctypes.c_int32), ("a", ctypes.c_int64),
+                ("b", ctypes.c_int64)]
+
+
+def lib():
+    """The loaded library (loads it on first use)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise MpoptUnavailable(f"{LIB_PATH} is not built; run mixed_precision_optimizer_gb300.build_lib")
+    try:
+        L = ctypes.CDLL(LIB_PATH)
+    except OSError as e:
+        raise MpoptUnavailable(str(e)) from e
+    vp, sz, i32, i64, f32 = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int32, ctypes.c_int64, ctypes.c_float
+    T = ctypes.POINTER(OptTensor)
+    L.opt_workspace_size.argtypes = [T, i32, i32]
+    L.opt_workspace_size.restype = sz
+    L.opt_adamw_step.argtypes = [ctypes.POINTER(OptAdamwHP), T, i32, vp, sz, vp]
+    L.opt_adamw_step.restype = ctypes.c_int
+    L.opt_muon_step.argtypes = [ctypes.POINTER(OptMuonHP), T, vp, sz, vp]
+    L.opt_muon_step.restype = ctypes.c_int
+    L.opt_mixed_step.argtypes = [ctypes.POINTER(OptMuonHP), ctypes.POINTER(OptAdamwHP), T, i32, vp, sz, vp]
+    L.opt_mixed_step.restype = ctypes.c_int
+    L.opt_newton_schulz.argtypes = [vp, vp, i64, i64, i32, f32, f32, f32, f32, vp, sz, vp]
+    L.opt_newton_schulz.restype = ctypes.c_int
+    L.opt_device_status.argtypes = [vp, vp]
+    L.opt_device_status.restype = ctypes.c_int
+    L.opt_profile_launches.argtypes = [vp, ctypes.POINTER(OptLaunchInfo), i32, ctypes.POINTER(i32)]
+    L.opt_profile_launches.restype = ctypes.c_int
+    L.opt_strerror.argtypes = [ctypes.c_int]
+    L.opt_strerror.restype = ctypes.c_char_p
+    L.opt_last_cuda_error.argtypes = []
+    L.opt_last_cuda_error.restype = ctypes.c_char_p
+    L.opt_abi_version.argtypes = []
+    L.opt_abi_version.restype = i32
+    _lib = L
+    return L
+
+
+def _check(status, where):
+    if status != OPT_OK:
+        detail = lib().opt_last_cuda_error().decode() if status == 5 else ""
+        raise MpoptError(status, where, detail)
+
+
+# --------------------------------------------------------------------------
+# tensor marshalling
+# --------------------------------------------------------------------------
+
+def _ptr(t, dtype, what, numel):
+    import torch
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{what} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{what} must be {dtype}, got {t.dtype}")
+    if t.device.type != "cuda":
+        raise ValueError(f"{what} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{what} must be contiguous")
+    if t.numel() != numel:
+        raise ValueError(f"{what} has {t.numel()} elements, expected {numel}")
+    return t.data_ptr() if numel else None
+
+
+@dataclasses.dataclass
+class Param:
+    """One parameter's buffers.  ``model`` is the bf16 model copy (None: the
+    parameter is fp32-native and ``main_param`` is the model parameter).
+    ``exp_avg_sq`` is only used by AdamW.  ``kind`` forces the route
+    ("adamw" or "muon"); by default 2-D tensors that are not embeddings or
+    output heads go to Muon."""
+    main_param: object
+    main_grad: object
+    exp_avg: object
+    exp_avg_sq: object = None
+    model: object = None
+    embedding_or_output: bool = False
+    kind: Optional[str] = None
+
+    def to_c(self, force=None):
+        import torch
+        p = self.main_param
+        shape = tuple(p.shape)
+        ndim = len(shape)
+        if ndim == 2:
+            rows, cols = shape
+        else:
+            rows, cols = 1, p.numel()
+        n = rows * cols
+        kind = force or self.kind
+        ct = OptTensor()
+        ct.main_param = _ptr(p, torch.float32, "main_param", n)
+        ct.main_grad = _ptr(self.main_grad, torch.float32, "main_grad", n)
+        ct.exp_avg = _ptr(self.exp_avg, torch.float32, "exp_avg", n)
+        ct.exp_avg_sq = _ptr(self.exp_avg_sq, torch.float32, "exp_avg_sq", n)
+        ct.model_param = _ptr(self.model, torch.bfloat16, "model", n)
+        ct.rows, ct.cols, ct.ndim = rows, cols, ndim
+        ct.kind = {None: KIND_AUTO, "adamw": KIND_ADAMW, "muon": KIND_MUON}[kind]
+        ct.flags = FLAG_EMBEDDING_OR_OUTPUT if self.embedding_or_output else 0
+        return ct
+
+
+def _array(params: Sequence[Param], force=None):
+    arr = (OptTensor * max(1, len(params)))()
+    for i, p in enumerate(params):
+        arr[i] = p.to_c(force)
+    return arr
+
+
+def _stream(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def adamw_hp(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01, step=1):
+    return OptAdamwHP(lr, beta1, beta2, eps, weight_decay, 0, int(step))
+
+
+def muon_hp(lr=0.02, momentum=0.95, weight_decay=0.0, eps=1e-7, nesterov=True, ns_steps=5,
+            coeffs=NS_COEFFS, scale_coeff=0.2):
+    a, b, c = coeffs
+    return OptMuonHP(lr, momentum, weight_decay, eps, 1 if nesterov else 0, int(ns_steps), a, b, c, scale_coeff)
+
+
+def workspace_size(params: Sequence[Param], routing="auto") -> int:
+    r = {"auto": KIND_AUTO, "adamw": KIND_ADAMW, "muon": KIND_MUON}[routing]
+    arr = _array(params)
+    return int(lib().opt_workspace_size(arr, len(params), r))
+
+
+def alloc_workspace(nbytes, device=None):
+    """Device scratch from the PyTorch caching allocator (256-byte aligned)."""
+    import torch
+    if nbytes == 0:
+        return None
+    return torch.empty(int(nbytes), dtype=torch.uint8, device=device or "cuda")
+
+
+def _ws(workspace):
+    if workspace is None:
+        return None, 0
+    return ctypes.c_void_p(workspace.data_ptr()), workspace.numel() * workspace.element_size()
+
+
+def adamw_step(params: Sequence[Param], hp: OptAdamwHP, workspace=None, stream=None):
+    arr = _array(params, "adamw")
+    w, nb = _ws(workspace)
+    _check(lib().opt_adamw_step(ctypes.byref(hp), arr, len(params), w, nb, _stream(stream)), "opt_adamw_step")
+
+
+def muon_step(param: Param, hp: OptMuonHP, workspace, stream=None):
+    arr = _array([param], "muon")
+    w, nb = _ws(workspace)
+    _check(lib().opt_muon_step(ctypes.byref(hp), arr, w, nb, _stream(stream)), "opt_muon_step")
+
+
+def mixed_step(params: Sequence[Param], hp_muon: Optional[OptMuonHP], hp_adamw: Optional[OptAdamwHP],
+               workspace, stream=None):
+    arr = _array(params)
+    w, nb = _ws(workspace)
+    _check(lib().opt_mixed_step(ctypes.byref(hp_muon) if hp_muon is not None else None,
+                                ctypes.byref(hp_adamw) if hp_adamw is not None else None,
+                                arr, len(params), w, nb, _stream(stream)), "opt_mixed_step")
+
+
+def newton_schulz(G, out, steps=5, coeffs=NS_COEFFS, eps=1e-7, workspace=None, stream=None):
+    import torch
+    if G.dim() != 2:
+        raise ValueError("G must be 2-D")
+    rows, cols = G.shape
+    gp = _ptr(G, torch.float32, "G", rows * cols)
+    op = _ptr(out, torch.float32, "out", rows * cols)
+    w, nb = _ws(workspace)
+    a, b, c = coeffs
+    _check(lib().opt_newton_schulz(gp, op, rows, cols, int(steps), a, b, c, eps, w, nb, _stream(stream)),
+           "opt_newton_schulz")
+
+
+def newton_schulz_workspace_size(rows, cols):
+    ct = OptTensor()
+    ct.rows, ct.cols, ct.ndim, ct.kind = rows, cols, 2, KIND_MUON
+    ct.main_param = ct.main_grad = ct.exp_avg = 256   # any aligned non-null value: sizing only
+    arr = (OptTensor * 1)(ct)
+    return int(lib().opt_workspace_size(arr, 1, KIND_MUON))
+
+
+def device_status(workspace, stream=None) -> int:
+    if workspace is None:
+        return OPT_OK
+    return int(lib().opt_device_status(ctypes.c_void_p(workspace.data_ptr()), _stream(stream)))
+
+
+class LaunchProfiler:
+    """Records a CUDA event pair around every kernel the library launches
+    from this thread (opt_profile_launches), up to ``capacity`` launches.
+
+        with LaunchProfiler(4096) as prof:
+            ... library calls ...
+        torch.cuda.synchronize()
+        for rec in prof.records(): rec["kernel"], rec["ms"], rec["count"], ...
+    """
+
+    def __init__(self, capacity=4096):
+        import torch
+        self.capacity = int(capacity)
+        self._events = [torch.cuda.Event(enable_timing=True) for _ in range(2 * self.capacity)]
+        for e in self._events:           # materialise the cudaEvent_t handles
+            e.record()
+        self._handles = (ctypes.c_void_p * (2 * self.capacity))(*[e.cuda_event for e in self._events])
+        self._info = (OptLaunchInfo * self.capacity)()
+        self._count = ctypes.c_int32(0)
+
+    def __enter__(self):
+        self._count.value = 0
+        _check(lib().opt_profile_launches(self._handles, self._info, self.capacity, ctypes.byref(self._count)),
+               "opt_profile_launches")
+        return self
+
+    def __exit__(self, *exc):
+        lib().opt_profile_launches(None, None, 0, None)
+        return False
+
+    @property
+    def count(self):
+        return int(self._count.value)
+
+    def records(self):
+        out = []
+        for i in range(min(self.count, self.capacity)):
+            inf = self._info[i]
+            ms = self._events[2 * i].elapsed_time(self._events[2 * i + 1])
+            out.append(dict(kernel=KERNEL_NAMES.get(inf.kernel, str(inf.kernel)), count=int(inf.count),
+                            a=int(inf.a), b=int(inf.b), ms=float(ms)))
+        return out

@@ -1,0 +1,544 @@
+// C ABI of libmpopt.so: argument validation, routing, workspace layout and
+// the launch sequence of one optimizer step.  See include/mpopt.h for the
+// contract of every entry point.
+
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <utility>
+#include <vector>
+
+#include "../../include/mpopt.h"
+#include "internal.h"
+
+namespace mpopt {
+
+int num_sms() {
+  static thread_local int cached_dev = -1, cached = 0;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  if (dev != cached_dev) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 1;
+    cached = n;
+    cached_dev = dev;
+  }
+  return cached;
+}
+
+namespace {
+struct ProfState {
+  cudaEvent_t const* events = nullptr;
+  opt_launch_info* info = nullptr;
+  int32_t capacity = 0;
+  int32_t* count = nullptr;
+  int32_t open = -1;
+};
+thread_local ProfState g_prof;
+}  // namespace
+
+void prof_begin(int kernel, int count, int64_t a, int64_t b, cudaStream_t stream) {
+  if (!g_prof.count) return;
+  const int32_t i = *g_prof.count;
+  g_prof.open = -1;
+  if (i < g_prof.capacity) {
+    g_prof.info[i] = opt_launch_info{kernel, count, a, b};
+    cudaEventRecord(g_prof.events[2 * i], stream);
+    g_prof.open = i;
+  }
+}
+
+void prof_end(cudaStream_t stream) {
+  if (!g_prof.count) return;
+  if (g_prof.open >= 0) cudaEventRecord(g_prof.events[2 * g_prof.open + 1], stream);
+  g_prof.open = -1;
+  ++*g_prof.count;
+}
+
+namespace {
+
+constexpr size_t kHeaderBytes = 256;
+constexpr size_t kAlign = 1024;
+
+thread_local char g_last_cuda_error[256] = "";
+
+opt_status cuda_fail(cudaError_t e, const char* where) {
+  std::snprintf(g_last_cuda_error, sizeof(g_last_cuda_error), "%s: %s (%s)", where, cudaGetErrorName(e),
+                cudaGetErrorString(e));
+  return OPT_ERR_CUDA;
+}
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+int64_t pad_to(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
+
+bool finite(float x) { return std::isfinite(x); }
+
+opt_status check_fp32_ptr(const void* p) {
+  return (reinterpret_cast<uintptr_t>(p) & 3u) ? OPT_ERR_MISALIGNED : OPT_OK;
+}
+
+// Per-tensor checks shared by both kinds.
+opt_status check_tensor(const opt_tensor& t, bool muon) {
+  if (t.rows < 0 || t.cols < 0) return OPT_ERR_INVALID_ARG;
+  if (t.ndim < 0) return OPT_ERR_INVALID_ARG;
+  if (t.rows > 0 && t.cols > (INT64_MAX / t.rows)) return OPT_ERR_INVALID_ARG;
+  const int64_t n = t.rows * t.cols;
+  if (muon) {
+    if (t.ndim != 2) return OPT_ERR_INVALID_ARG;
+    if (t.rows > (int64_t(1) << 30) || t.cols > (int64_t(1) << 30)) return OPT_ERR_UNSUPPORTED;
+  }
+  if (n == 0) return OPT_OK;
+  if (!t.main_param || !t.main_grad || !t.exp_avg) return OPT_ERR_INVALID_ARG;
+  if (!muon && !t.exp_avg_sq) return OPT_ERR_INVALID_ARG;
+  opt_status s;
+  if ((s = check_fp32_ptr(t.main_param)) != OPT_OK) return s;
+  if ((s = check_fp32_ptr(t.main_grad)) != OPT_OK) return s;
+  if ((s = check_fp32_ptr(t.exp_avg)) != OPT_OK) return s;
+  if (!muon && (s = check_fp32_ptr(t.exp_avg_sq)) != OPT_OK) return s;
+  if (t.model_param && (reinterpret_cast<uintptr_t>(t.model_param) & 1u)) return OPT_ERR_MISALIGNED;
+  return OPT_OK;
+}
+
+opt_status check_adamw_hp(const opt_adamw_hp* hp) {
+  if (!hp) return OPT_ERR_INVALID_ARG;
+  if (!finite(hp->lr) || !finite(hp->eps) || !finite(hp->weight_decay)) return OPT_ERR_INVALID_ARG;
+  if (!(hp->beta1 >= 0.f && hp->beta1 < 1.f) || !(hp->beta2 >= 0.f && hp->beta2 < 1.f)) return OPT_ERR_INVALID_ARG;
+  if (hp->step < 1) return OPT_ERR_INVALID_ARG;
+  return OPT_OK;
+}
+
+opt_status check_muon_hp(const opt_muon_hp* hp) {
+  if (!hp) return OPT_ERR_INVALID_ARG;
+  if (!finite(hp->lr) || !finite(hp->weight_decay) || !finite(hp->eps) || !finite(hp->ns_a) ||
+      !finite(hp->ns_b) || !finite(hp->ns_c) || !finite(hp->scale_coeff))
+    return OPT_ERR_INVALID_ARG;
+  if (!(hp->momentum >= 0.f && hp->momentum < 1.f)) return OPT_ERR_INVALID_ARG;
+  if (hp->eps < 0.f) return OPT_ERR_INVALID_ARG;
+  if (hp->ns_steps < 0 || hp->ns_steps > 16) return OPT_ERR_INVALID_ARG;
+  return OPT_OK;
+}
+
+// Routing rule: "02 · Optimizer：算法与 infra" §5.5 / §14.2 -- Muon for 2-D
+// parameters that are not embeddings or output heads, AdamW for the rest.
+bool routes_to_muon(const opt_tensor& t, int32_t routing) {
+  if (routing == OPT_KIND_ADAMW) return false;
+  if (routing == OPT_KIND_MUON) return true;
+  if (t.kind == OPT_KIND_MUON) return true;
+  if (t.kind == OPT_KIND_ADAMW) return false;
+  return t.ndim == 2 && !(t.flags & OPT_FLAG_EMBEDDING_OR_OUTPUT);
+}
+
+// ------------------------------------------------------------ AdamW plan --
+
+// Elements to peel so that p, g, m, v (fp32) and model (bf16) are all 16-byte
+// aligned at the same element index; -1 if no such index exists.
+int32_t vector_head(const opt_tensor& t) {
+  for (int h = 0; h < 8; ++h) {
+    auto al = [h](const void* p, int esz) { return ((reinterpret_cast<uintptr_t>(p) + h * esz) & 15u) == 0; };
+    if (al(t.main_param, 4) && al(t.main_grad, 4) && al(t.exp_avg, 4) && al(t.exp_avg_sq, 4) &&
+        (!t.model_param || al(t.model_param, 2)))
+      return h;
+  }
+  return -1;
+}
+
+AdamwTensorDesc describe(const opt_tensor& t, int64_t chunk_begin, int64_t& chunks) {
+  const int64_t n = t.rows * t.cols;
+  AdamwTensorDesc d{};
+  d.p = t.main_param;
+  d.g = t.main_grad;
+  d.m = t.exp_avg;
+  d.v = t.exp_avg_sq;
+  d.model = t.model_param;
+  d.numel = n;
+  d.chunk_begin = chunk_begin;
+  int32_t head = vector_head(t);
+  if (head < 0) {
+    chunks = (n + kAdamwChunk - 1) / kAdamwChunk;
+  } else {
+    if (head > n) head = static_cast<int32_t>(n);
+    const int64_t body = n - head;
+    chunks = body > 0 ? (body + kAdamwChunk - 1) / kAdamwChunk : 1;
+  }
+  d.head = head;
+  return d;
+}
+
+AdamwScalars adamw_scalars(const opt_adamw_hp* hp) {
+  // per-step scalars: double from the float hyper-parameters, rounded once
+  const double lr = hp->lr, b1 = hp->beta1, b2 = hp->beta2, wd = hp->weight_decay;
+  AdamwScalars s;
+  s.lr = hp->lr;
+  s.beta1 = hp->beta1;
+  s.beta2 = hp->beta2;
+  s.eps = hp->eps;
+  s.one_minus_beta1 = static_cast<float>(1.0 - b1);
+  s.one_minus_beta2 = static_cast<float>(1.0 - b2);
+  s.bias_c1 = static_cast<float>(1.0 - std::pow(b1, static_cast<double>(hp->step)));
+  s.bias_c2 = static_cast<float>(1.0 - std::pow(b2, static_cast<double>(hp->step)));
+  s.decay = static_cast<float>(1.0 - lr * wd);
+  return s;
+}
+
+opt_status run_adamw(const opt_adamw_hp* hp, const std::vector<const opt_tensor*>& ts, cudaStream_t stream) {
+  static thread_local AdamwBatch batch;   // ~26 KB: kept off the stack
+  batch.s = adamw_scalars(hp);
+  batch.n = 0;
+  batch.total_chunks = 0;
+  for (size_t i = 0; i <= ts.size(); ++i) {
+    const bool flush = (i == ts.size()) || batch.n == kAdamwBatch;
+    if (flush && batch.n > 0) {
+      int64_t elems = 0;
+      for (int32_t k = 0; k < batch.n; ++k) elems += batch.t[k].numel;
+      prof_begin(OPT_KERNEL_ADAMW, batch.n, elems, 0, stream);
+      const cudaError_t e = launch_adamw(batch, stream);
+      prof_end(stream);
+      if (e != cudaSuccess) return cuda_fail(e, "adamw launch");
+      batch.n = 0;
+      batch.total_chunks = 0;
+    }
+    if (i == ts.size()) break;
+    if (ts[i]->rows * ts[i]->cols == 0) continue;
+    int64_t chunks = 0;
+    batch.t[batch.n] = describe(*ts[i], batch.total_chunks, chunks);
+    batch.total_chunks += chunks;
+    ++batch.n;
+  }
+  return OPT_OK;
+}
+
+// ------------------------------------------------------------- Muon plan --
+
+struct ShapeClass {
+  int64_t A, B;
+  std::vector<const opt_tensor*> mats;
+};
+
+void shape_of(int64_t R, int64_t C, int64_t& A, int64_t& B, int64_t& Ap, int64_t& Bp) {
+  A = R < C ? R : C;
+  B = R < C ? C : R;
+  Ap = pad_to(A, kNsPad);
+  Bp = pad_to(B, kNsPad);
+}
+
+size_t group_bytes(int64_t count, int64_t R, int64_t C) {
+  int64_t A, B, Ap, Bp;
+  shape_of(R, C, A, B, Ap, Bp);
+  const size_t ab = static_cast<size_t>(Ap) * static_cast<size_t>(Bp);
+  const size_t aa = static_cast<size_t>(Ap) * static_cast<size_t>(Ap);
+  const size_t blocks = static_cast<size_t>((Ap / kPrepTile) * (Bp / kPrepTile));
+  size_t b = 0;
+  b += align_up(count * ab * 4, kAlign);      // X fp32
+  b += align_up(count * ab * 2, kAlign);      // Xb
+  b += 2 * align_up(count * ab * 2, kAlign);  // Xt ping-pong
+  b += align_up(count * aa * 4, kAlign);      // A fp32
+  b += align_up(count * aa * 2, kAlign);      // B bf16
+  b += align_up(count * blocks * 4, kAlign);  // partial sums
+  b += align_up(count * 4, kAlign);           // inverse norms
+  return b;
+}
+
+NsBuffers carve(uint8_t* base, int64_t count, int64_t R, int64_t C, uint32_t* status) {
+  int64_t A, B, Ap, Bp;
+  shape_of(R, C, A, B, Ap, Bp);
+  const size_t ab = static_cast<size_t>(Ap) * static_cast<size_t>(Bp);
+  const size_t aa = static_cast<size_t>(Ap) * static_cast<size_t>(Ap);
+  const size_t blocks = static_cast<size_t>((Ap / kPrepTile) * (Bp / kPrepTile));
+  NsBuffers b{};
+  size_t off = 0;
+  b.X = reinterpret_cast<float*>(base + off);
+  off += align_up(count * ab * 4, kAlign);
+  b.Xb = reinterpret_cast<uint16_t*>(base + off);
+  off += align_up(count * ab * 2, kAlign);
+  b.Xt[0] = reinterpret_cast<uint16_t*>(base + off);
+  off += align_up(count * ab * 2, kAlign);
+  b.Xt[1] = reinterpret_cast<uint16_t*>(base + off);
+  off += align_up(count * ab * 2, kAlign);
+  b.Af = reinterpret_cast<float*>(base + off);
+  off += align_up(count * aa * 4, kAlign);
+  b.Bb = reinterpret_cast<uint16_t*>(base + off);
+  off += align_up(count * aa * 2, kAlign);
+  b.partial = reinterpret_cast<float*>(base + off);
+  off += align_up(count * blocks * 4, kAlign);
+  b.inv_norm = reinterpret_cast<float*>(base + off);
+  b.status = status;
+  return b;
+}
+
+std::vector<ShapeClass> shape_classes(const std::vector<const opt_tensor*>& mats) {
+  std::map<std::pair<int64_t, int64_t>, size_t> index;
+  std::vector<ShapeClass> out;
+  for (const opt_tensor* t : mats) {
+    if (t->rows * t->cols == 0) continue;
+    int64_t A, B, Ap, Bp;
+    shape_of(t->rows, t->cols, A, B, Ap, Bp);
+    auto key = std::make_pair(A, B);
+    auto it = index.find(key);
+    if (it == index.end()) {
+      index[key] = out.size();
+      out.push_back(ShapeClass{A, B, {}});
+      out.back().mats.push_back(t);
+    } else {
+      out[it->second].mats.push_back(t);
+    }
+  }
+  return out;
+}
+
+// Workspace for the Muon part with full groups (up to kMaxGroup matrices).
+size_t muon_bytes(const std::vector<ShapeClass>& classes) {
+  size_t need = 0;
+  for (const ShapeClass& c : classes) {
+    const int64_t cnt = static_cast<int64_t>(c.mats.size()) < kMaxGroup ? c.mats.size() : kMaxGroup;
+    const size_t b = group_bytes(cnt, c.A, c.B);
+    if (b > need) need = b;
+  }
+  return need;
+}
+
+struct MuonPlanHp {
+  float lr, mu, wd, eps, a, b, c, scale_coeff;
+  int nesterov, ns_steps, ns_only;
+};
+
+// Runs Muon on the matrices of one shape class; all of them must have rows x
+// cols equal to (R, C) or (C, R) -- both orientations share a class.
+opt_status run_muon_class(const MuonPlanHp& hp, const ShapeClass& cls, uint8_t* region, size_t region_bytes,
+                          uint32_t* status, cudaStream_t stream, float* const* outputs /*ns_only*/) {
+  // largest group that fits the region
+  int64_t cap = static_cast<int64_t>(cls.mats.size()) < kMaxGroup ? cls.mats.size() : kMaxGroup;
+  while (cap > 0 && group_bytes(cap, cls.A, cls.B) > region_bytes) --cap;
+  if (cap == 0) return OPT_ERR_WORKSPACE;
+  // matrices of both orientations share a group (the orientation is per matrix)
+  for (size_t g0 = 0; g0 < cls.mats.size(); g0 += static_cast<size_t>(cap)) {
+    {
+      const size_t gn = std::min(cls.mats.size() - g0, static_cast<size_t>(cap));
+      MuonGroup grp{};
+      grp.count = static_cast<int32_t>(gn);
+      grp.A = cls.A;
+      grp.B = cls.B;
+      grp.Ap = pad_to(cls.A, kNsPad);
+      grp.Bp = pad_to(cls.B, kNsPad);
+      for (size_t k = 0; k < gn; ++k) {
+        const opt_tensor* t = cls.mats[g0 + k];
+        MuonMat& M = grp.mats[k];
+        M.W = t->main_param;
+        M.g = t->main_grad;
+        M.m = t->exp_avg;
+        M.Wb = t->model_param;
+        M.O = outputs ? outputs[g0 + k] : nullptr;
+        M.R = static_cast<int32_t>(t->rows);
+        M.C = static_cast<int32_t>(t->cols);
+        M.transposed = t->rows > t->cols ? 1 : 0;
+      }
+      const NsBuffers buf = carve(region, static_cast<int64_t>(gn), cls.A, cls.B, status);
+      MuonScalars s{};
+      s.mu = hp.mu;
+      s.one_minus_mu = static_cast<float>(1.0 - static_cast<double>(hp.mu));
+      s.nesterov = hp.nesterov;
+      s.eps = hp.eps;
+      s.a = hp.a;
+      s.b = hp.b;
+      s.c = hp.c;
+      s.decay = static_cast<float>(1.0 - static_cast<double>(hp.lr) * static_cast<double>(hp.wd));
+      s.step_scale = static_cast<float>(static_cast<double>(hp.lr) * static_cast<double>(hp.scale_coeff) *
+                                        std::sqrt(static_cast<double>(cls.B)));
+      s.ns_steps = hp.ns_steps;
+      s.ns_only = hp.ns_only;
+      prof_begin(OPT_KERNEL_MUON_PREP, grp.count, grp.A, grp.B, stream);
+      cudaError_t e = launch_muon_prep(grp, buf, s, stream);
+      prof_end(stream);
+      if (e != cudaSuccess) return cuda_fail(e, "muon prep");
+      prof_begin(OPT_KERNEL_MUON_NORM, grp.count, grp.A, grp.B, stream);
+      e = launch_muon_norm(grp, buf, s, stream);
+      prof_end(stream);
+      if (e != cudaSuccess) return cuda_fail(e, "muon norm");
+      if (hp.ns_steps == 0) {
+        prof_begin(OPT_KERNEL_MUON_APPLY, grp.count, grp.A, grp.B, stream);
+        e = launch_muon_apply_direct(grp, buf, s, stream);
+        prof_end(stream);
+        if (e != cudaSuccess) return cuda_fail(e, "muon apply");
+      }
+      for (int it = 0; it < hp.ns_steps; ++it) {
+        e = launch_ns_iteration(grp, buf, s, it, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "newton-schulz gemm");
+      }
+    }
+  }
+  return OPT_OK;
+}
+
+opt_status check_workspace(const void* ws, size_t bytes, size_t need) {
+  if (need == 0) return OPT_OK;
+  if (!ws) return OPT_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(ws) & 255u) return OPT_ERR_WORKSPACE;
+  if (bytes < need) return OPT_ERR_WORKSPACE;
+  return OPT_OK;
+}
+
+struct Split {
+  std::vector<const opt_tensor*> adamw, muon;
+};
+
+opt_status split_tensors(const opt_tensor* tensors, int32_t n, int32_t routing, Split& sp) {
+  if (n < 0) return OPT_ERR_INVALID_ARG;
+  if (n > 0 && !tensors) return OPT_ERR_INVALID_ARG;
+  for (int32_t i = 0; i < n; ++i) {
+    const opt_tensor& t = tensors[i];
+    if (t.kind != OPT_KIND_AUTO && t.kind != OPT_KIND_ADAMW && t.kind != OPT_KIND_MUON) return OPT_ERR_INVALID_ARG;
+    const bool muon = routes_to_muon(t, routing);
+    const opt_status s = check_tensor(t, muon);
+    if (s != OPT_OK) return s;
+    (muon ? sp.muon : sp.adamw).push_back(&t);
+  }
+  return OPT_OK;
+}
+
+// AdamW needs no workspace; Muon needs the status header and the group buffers.
+size_t total_bytes(const std::vector<ShapeClass>& classes) {
+  return classes.empty() ? 0 : kHeaderBytes + muon_bytes(classes);
+}
+
+// Minimum workspace: one matrix per Muon group.
+size_t min_bytes(const std::vector<ShapeClass>& classes) {
+  size_t m = 0;
+  for (const ShapeClass& c : classes) m = std::max(m, group_bytes(1, c.A, c.B));
+  return classes.empty() ? 0 : kHeaderBytes + m;
+}
+
+opt_status mixed_impl(const opt_muon_hp* hpm, const opt_adamw_hp* hpa, const opt_tensor* tensors, int32_t n,
+                      int32_t routing, void* workspace, size_t ws_bytes, void* stream_ptr) {
+  Split sp;
+  opt_status st = split_tensors(tensors, n, routing, sp);
+  if (st != OPT_OK) return st;
+  bool any_adamw = false, any_muon = false;
+  for (auto* t : sp.adamw) any_adamw |= (t->rows * t->cols) > 0;
+  for (auto* t : sp.muon) any_muon |= (t->rows * t->cols) > 0;
+  if (any_adamw && (st = check_adamw_hp(hpa)) != OPT_OK) return st;
+  if (any_muon && (st = check_muon_hp(hpm)) != OPT_OK) return st;
+  if (!any_adamw && !any_muon) return OPT_OK;
+  const std::vector<ShapeClass> classes = shape_classes(sp.muon);
+  if ((st = check_workspace(workspace, ws_bytes, min_bytes(classes))) != OPT_OK) return st;
+
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  if (any_adamw && (st = run_adamw(hpa, sp.adamw, stream)) != OPT_OK) return st;
+  if (any_muon) {
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    uint32_t* status = reinterpret_cast<uint32_t*>(ws);
+    const cudaError_t e = cudaMemsetAsync(ws, 0, kHeaderBytes, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "workspace header");
+    const size_t off = kHeaderBytes;
+    MuonPlanHp hp{hpm->lr, hpm->momentum, hpm->weight_decay, hpm->eps, hpm->ns_a, hpm->ns_b,
+                  hpm->ns_c, hpm->scale_coeff, hpm->nesterov ? 1 : 0, hpm->ns_steps, 0};
+    for (const ShapeClass& c : classes) {
+      if ((st = run_muon_class(hp, c, ws + off, ws_bytes - off, status, stream, nullptr)) != OPT_OK) return st;
+    }
+  }
+  return OPT_OK;
+}
+
+}  // namespace
+}  // namespace mpopt
+
+using namespace mpopt;
+
+extern "C" {
+
+size_t opt_workspace_size(const opt_tensor* tensors, int32_t n, int32_t routing) {
+  if (routing != OPT_KIND_AUTO && routing != OPT_KIND_ADAMW && routing != OPT_KIND_MUON) return 0;
+  Split sp;
+  if (split_tensors(tensors, n, routing, sp) != OPT_OK) return 0;
+  return total_bytes(shape_classes(sp.muon));
+}
+
+opt_status opt_adamw_step(const opt_adamw_hp* hp, const opt_tensor* tensors, int32_t n, void* workspace,
+                          size_t workspace_bytes, void* stream) {
+  return mixed_impl(nullptr, hp, tensors, n, OPT_KIND_ADAMW, workspace, workspace_bytes, stream);
+}
+
+opt_status opt_muon_step(const opt_muon_hp* hp, const opt_tensor* t, void* workspace, size_t workspace_bytes,
+                         void* stream) {
+  if (!t) return OPT_ERR_INVALID_ARG;
+  if (t->ndim != 2) return OPT_ERR_INVALID_ARG;
+  return mixed_impl(hp, nullptr, t, 1, OPT_KIND_MUON, workspace, workspace_bytes, stream);
+}
+
+opt_status opt_mixed_step(const opt_muon_hp* hp_muon, const opt_adamw_hp* hp_adamw, const opt_tensor* tensors,
+                          int32_t n, void* workspace, size_t workspace_bytes, void* stream) {
+  return mixed_impl(hp_muon, hp_adamw, tensors, n, OPT_KIND_AUTO, workspace, workspace_bytes, stream);
+}
+
+opt_status opt_newton_schulz(const float* G, float* O, int64_t rows, int64_t cols, int32_t ns_steps, float a,
+                             float b, float c, float eps, void* workspace, size_t workspace_bytes, void* stream) {
+  if (rows < 0 || cols < 0 || ns_steps < 0 || ns_steps > 16) return OPT_ERR_INVALID_ARG;
+  if (!std::isfinite(a) || !std::isfinite(b) || !std::isfinite(c) || !std::isfinite(eps) || eps < 0.f)
+    return OPT_ERR_INVALID_ARG;
+  if (rows > (int64_t(1) << 30) || cols > (int64_t(1) << 30)) return OPT_ERR_UNSUPPORTED;
+  if (rows * cols == 0) return OPT_OK;
+  if (!G || !O) return OPT_ERR_INVALID_ARG;
+  if (check_fp32_ptr(G) != OPT_OK || check_fp32_ptr(O) != OPT_OK) return OPT_ERR_MISALIGNED;
+  opt_tensor t{};
+  t.main_param = O;
+  t.main_grad = G;
+  t.exp_avg = O;
+  t.rows = rows;
+  t.cols = cols;
+  t.ndim = 2;
+  t.kind = OPT_KIND_MUON;
+  std::vector<const opt_tensor*> one{&t};
+  const std::vector<ShapeClass> classes = shape_classes(one);
+  opt_status st = check_workspace(workspace, workspace_bytes, min_bytes(classes));
+  if (st != OPT_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  cudaError_t e = cudaMemsetAsync(ws, 0, kHeaderBytes, s);
+  if (e != cudaSuccess) return cuda_fail(e, "workspace header");
+  MuonPlanHp hp{0.f, 0.f, 0.f, eps, a, b, c, 0.f, 0, ns_steps, 1};
+  float* outs[1] = {O};
+  return run_muon_class(hp, classes[0], ws + kHeaderBytes, workspace_bytes - kHeaderBytes,
+                        reinterpret_cast<uint32_t*>(ws), s, outs);
+}
+
+opt_status opt_device_status(const void* workspace, void* stream) {
+  if (!workspace) return OPT_ERR_WORKSPACE;
+  uint32_t code = 0;
+  cudaError_t e = cudaMemcpyAsync(&code, workspace, sizeof(code), cudaMemcpyDeviceToHost,
+                                  static_cast<cudaStream_t>(stream));
+  if (e == cudaSuccess) e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "device status");
+  return code == 0 ? OPT_OK : OPT_ERR_DEVICE_TIMEOUT;
+}
+
+const char* opt_strerror(opt_status s) {
+  switch (s) {
+    case OPT_OK: return "ok";
+    case OPT_ERR_INVALID_ARG: return "invalid argument";
+    case OPT_ERR_UNSUPPORTED: return "unsupported case";
+    case OPT_ERR_MISALIGNED: return "misaligned pointer";
+    case OPT_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case OPT_ERR_CUDA: return "CUDA error";
+    case OPT_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
+  }
+  return "unknown status";
+}
+
+const char* opt_last_cuda_error(void) { return g_last_cuda_error; }
+
+opt_status opt_profile_launches(void* const* events, opt_launch_info* info, int32_t capacity, int32_t* count) {
+  if (!events || !count) {
+    g_prof = ProfState{};
+    return OPT_OK;
+  }
+  if (capacity < 0 || (capacity > 0 && !info)) return OPT_ERR_INVALID_ARG;
+  g_prof.events = reinterpret_cast<cudaEvent_t const*>(events);
+  g_prof.info = info;
+  g_prof.capacity = capacity;
+  g_prof.count = count;
+  g_prof.open = -1;
+  return OPT_OK;
+}
+
+int32_t opt_abi_version(void) { return (1 << 16) | 0; }
+
+}  // extern "C"

@@ -1,0 +1,143 @@
+// Internal declarations shared by the host side of the C ABI (api.cu) and the
+// kernels.  Not part of the public interface.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace mpopt {
+
+// ---------------------------------------------------------------- AdamW ----
+
+// Elements per multi-tensor chunk.  A chunk is the unit of work a CTA takes.
+constexpr int64_t kAdamwChunk = 16384;
+constexpr int kAdamwThreads = 256;
+
+// One tensor of the AdamW list, as the kernel sees it (device-resident table).
+struct AdamwTensorDesc {
+  float* p;
+  const float* g;
+  float* m;
+  float* v;
+  uint16_t* model;       // bf16 bits, or nullptr (fp32-native parameter)
+  int64_t numel;
+  int64_t chunk_begin;   // index of this tensor's first chunk in the launch
+  int32_t head;          // scalar elements before the first 8-aligned group; -1: scalar only
+  int32_t pad_;
+};
+static_assert(sizeof(AdamwTensorDesc) == 64, "descriptor layout");
+
+// Per-step fp32 scalars, formed on the host in double and rounded once.
+struct AdamwScalars {
+  float lr, beta1, beta2, eps;
+  float one_minus_beta1, one_minus_beta2;
+  float bias_c1, bias_c2;   // 1 - beta^t
+  float decay;              // 1 - lr * weight_decay
+};
+
+// Descriptors travel in the kernel's parameter space (no upload, no workspace):
+// up to kAdamwBatch tensors per launch.
+constexpr int kAdamwBatch = 400;
+struct AdamwBatch {
+  AdamwScalars s;
+  int32_t n;
+  int32_t pad_;
+  int64_t total_chunks;
+  AdamwTensorDesc t[kAdamwBatch];
+};
+static_assert(sizeof(AdamwBatch) <= 32000, "kernel parameter space");
+
+cudaError_t launch_adamw(const AdamwBatch& batch, cudaStream_t stream);
+
+// ----------------------------------------------------------------- Muon ----
+
+// Newton-Schulz works on padded, wide-oriented buffers: A = min(R, C) rows
+// padded to Ap, B = max(R, C) columns padded to Bp, both multiples of kNsPad.
+constexpr int64_t kNsPad = 256;
+constexpr int kMaxGroup = 64;         // matrices per batched launch
+
+// One Muon matrix of a batched group (kernel-parameter table).
+// Matrices of one group share (A, B) = (min, max) of their shape but not
+// necessarily the orientation: an R x C matrix with R > C is transposed into
+// the wide orientation.
+struct MuonMat {
+  float* W;               // fp32 master [R x C]
+  const float* g;         // fp32 gradient [R x C]
+  float* m;               // fp32 momentum [R x C]
+  uint16_t* Wb;           // bf16 model copy or nullptr
+  float* O;               // opt_newton_schulz only: fp32 output [R x C], else nullptr
+  int32_t R, C;           // this matrix's shape (W layout)
+  int32_t transposed;     // R > C: the wide orientation is W^T
+  int32_t pad_;
+};
+
+struct MuonGroup {
+  int32_t count;          // matrices in this group
+  int32_t pad_;
+  int64_t A, B, Ap, Bp;   // A = min(R, C), B = max(R, C), padded
+  MuonMat mats[kMaxGroup];
+};
+
+// Workspace buffers of one group (all device pointers into the workspace).
+struct NsBuffers {
+  float* X;          // fp32 iterate            [count][Ap][Bp]
+  uint16_t* Xb;      // bf16 iterate            [count][Ap][Bp]
+  uint16_t* Xt[2];   // bf16 transposed iterate [count][Bp][Ap], ping-pong
+  float* Af;         // fp32 Gram matrix        [count][Ap][Ap]
+  uint16_t* Bb;      // bf16 polynomial         [count][Ap][Ap]
+  float* partial;    // per-block sums of squares [count][prep_blocks]
+  float* inv_norm;   // 1 / (||G||_F + eps)     [count]
+  uint32_t* status;  // workspace header word
+};
+
+struct MuonScalars {
+  float mu, one_minus_mu;
+  int nesterov;
+  float eps;
+  float a, b, c;
+  float decay;        // 1 - lr * weight_decay
+  float step_scale;   // lr * scale_coeff * sqrt(max(R, C))
+  int ns_steps;
+  int ns_only;        // opt_newton_schulz: G is read from g, O written, no momentum/update
+};
+
+constexpr int kPrepTile = 64;
+inline int64_t prep_blocks_per_matrix(const MuonGroup& g) {
+  // prep tiles cover the padded W-layout space (Ap x Bp or Bp x Ap)
+  return (g.Ap / kPrepTile) * (g.Bp / kPrepTile);
+}
+
+cudaError_t launch_muon_prep(const MuonGroup& grp, const NsBuffers& buf, const MuonScalars& s,
+                             cudaStream_t stream);
+cudaError_t launch_muon_norm(const MuonGroup& grp, const NsBuffers& buf, const MuonScalars& s,
+                             cudaStream_t stream);
+// ns_steps == 0: O = X0 (no tensor-core work); writes the update / output.
+cudaError_t launch_muon_apply_direct(const MuonGroup& grp, const NsBuffers& buf,
+                                     const MuonScalars& s, cudaStream_t stream);
+
+// Tensor-core GEMM stages of one Newton-Schulz iteration.
+enum NsGemmMode : int { kGram = 0, kPoly = 1, kBx = 2, kBxFinal = 3 };
+
+cudaError_t launch_ns_iteration(const MuonGroup& grp, const NsBuffers& buf, const MuonScalars& s,
+                                int iteration, cudaStream_t stream);
+
+// Device-status codes written to the workspace header.
+enum : uint32_t {
+  kStatusOk = 0,
+  kStatusTimeoutFull = 1,     // MMA waited too long for a TMA stage
+  kStatusTimeoutEmpty = 2,    // producer waited too long for a free stage
+  kStatusTimeoutAcc = 3,      // epilogue waited too long for an accumulator
+  kStatusTimeoutAccFree = 4,  // MMA waited too long for a free accumulator
+  kStatusTimeoutDrain = 5
+};
+
+int num_sms();   // SM count of the current device (cached per device)
+
+// Launch instrumentation (opt_profile_launches).  A launch site calls
+// prof_begin(kernel, count, a, b, stream) before and prof_end(stream) after
+// its launch; both are no-ops while instrumentation is off.
+void prof_begin(int kernel, int count, int64_t a, int64_t b, cudaStream_t stream);
+void prof_end(cudaStream_t stream);
+
+}  // namespace mpopt

@@ -1,0 +1,651 @@
+// Newton-Schulz GEMMs on the 5th-generation tensor cores (sm_103a).
+//
+// One quintic iteration ("02 · Optimizer：算法与 infra" §5.2; "优化器：AdamW、
+// Muon 与分布式优化器", newton_schulz in the Muon section) on the wide
+// iterate X (A x B, A <= B) is three GEMMs with fused epilogues:
+//
+//   gram : A_k = X X^T          bf16 x bf16 -> fp32 (TMEM)    -> A fp32
+//   poly : B_k = b A + c A A    tf32 x tf32 -> fp32, + b*A    -> B bf16
+//   bx   : X'  = a X + B X      bf16 x bf16 -> fp32, + a*X    -> X fp32, X bf16, X^T bf16
+//          (last iteration: W <- W (1 - lr*lambda) - lr*0.2*sqrt(max(A,B)) * X',
+//           written in W's own orientation together with its bf16 copy)
+//
+// Precision: X is carried in fp32 between iterations (the a*X term of the
+// epilogue reads the fp32 copy); bf16 appears only as MMA operands.  The
+// A*A product runs in tf32 because rounding A to bf16 there is the largest
+// single error term of the iteration.  Accumulation is fp32 in TMEM.
+//
+// Kernel structure (one CTA per SM, persistent over output tiles):
+//   warp 0    TMA producer: 128-row A tile + 256-row B tile per k-block,
+//             128-byte swizzled, into a 4-stage shared-memory ring
+//   warp 1    TMEM allocator and MMA issuer: tcgen05.mma M=128 N=256, one
+//             elected thread, 4 MMAs per 128-byte k-block, commit to free the
+//             stage; a 2 x 256-column accumulator lets the epilogue of one
+//             tile overlap the main loop of the next
+//   warps 2-5 epilogue: tcgen05.ld 32 columns at a time, fused math, stores
+//
+// The Gram matrix and the polynomial are symmetric: only 128x256 tiles of
+// 256x256 blocks on or below the diagonal are computed, and off-diagonal
+// blocks are also stored transposed.
+//
+// Every wait on an mbarrier is bounded (about 2 s of %globaltimer).  A wait
+// that runs out records a status code in the workspace header, raises a CTA
+// abort flag, and every role leaves its loop; the MMA issuer drains its
+// outstanding MMAs and the producer its outstanding copies (again with bounded
+// waits) before TMEM is released.
+
+#include <cuda.h>
+
+#include "../../include/mpopt.h"
+#include "internal.h"
+
+namespace mpopt {
+namespace {
+
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int kStages = 4;
+constexpr int kRowBytes = 128;                 // one swizzle row per k-block
+constexpr int kStageA = BM * kRowBytes;        // 16 KB
+constexpr int kStageB = BN * kRowBytes;        // 32 KB
+constexpr int kStageBytes = kStageA + kStageB;
+constexpr int kThreads = 192;
+constexpr int kTmemCols = 512;                 // 2 accumulators x 256 fp32 columns
+constexpr uint32_t kSmemBytes = kStages * kStageBytes + 1024 /*align*/ + 256 /*barriers*/;
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;
+
+struct GemmParams {
+  int mode;             // NsGemmMode
+  int k_blocks;
+  int tiles_per_mat;
+  int total_tiles;
+  int tiles_m;          // bx: Ap / BM
+  int count;
+  int64_t Ap, Bp;
+  float* Xf;            // bx: fp32 iterate (in/out)
+  uint16_t* Xb;         // bx: bf16 iterate out
+  uint16_t* Xt_out;     // bx: bf16 transposed iterate out
+  float* Af;            // gram: out; poly: in
+  uint16_t* Bb;         // poly: out
+  const float* inv_norm;
+  int scale_input;      // iteration 0: the operands hold gtilde, fold in 1/||gtilde||
+  float a, b, c;
+  float decay, step_scale;
+  int ns_only;
+  uint32_t* status;
+};
+
+// ------------------------------------------------------------ PTX helpers --
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Bounded wait: true when the phase completed; false when the CTA is aborting
+// (another role timed out) or this wait ran out of time (then it raises the
+// abort flag and records `code` in the workspace header).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
+                                          uint32_t* status, uint32_t code) {
+  if (mbar_try(bar, parity)) return true;
+  const unsigned long long t0 = global_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try(bar, parity)) return true;
+    if ((i & 255u) == 0) {
+      if (*abort_flag) return false;
+      if (global_ns() - t0 > kWaitLimitNs) {
+        *abort_flag = 1u;
+        atomicCAS(status, 0u, code);
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x,
+                                            int y, int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+      : "memory");
+}
+
+// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of
+// 128 bytes, 8-row groups 1024 bytes apart.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((addr & 0x3FFFFu) >> 4);   // start address
+  d |= static_cast<uint64_t>(1) << 16;                   // leading byte offset (unused here)
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;           // stride byte offset
+  d |= static_cast<uint64_t>(1) << 46;                   // descriptor version
+  d |= static_cast<uint64_t>(2) << 61;                   // 128-byte swizzle
+  return d;
+}
+
+// Instruction descriptor: fp32 accumulator, A and B of format `fmt`
+// (1 = bf16 for kind::f16, 2 = tf32 for kind::tf32), both K-major, M = 128, N = 256.
+template <int kFmt>
+__host__ __device__ constexpr uint32_t instr_desc() {
+  return (1u << 4) | (static_cast<uint32_t>(kFmt) << 7) | (static_cast<uint32_t>(kFmt) << 10) |
+         (static_cast<uint32_t>(BN >> 3) << 17) | (static_cast<uint32_t>(BM >> 4) << 24);
+}
+
+template <int kFmt>
+__device__ __forceinline__ void mma(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t accumulate) {
+  constexpr uint32_t idesc = instr_desc<kFmt>();
+  if constexpr (kFmt == 2) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n}" ::"r"(tmem_d),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(tmem_d),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+  }
+}
+
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+               : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]),
+        "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]),
+        "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+}
+
+__device__ __forceinline__ uint16_t bf16_rne(float x) {
+  const uint32_t u = __float_as_uint(x);
+  if ((u & 0x7fffffffu) > 0x7f800000u) return 0x7fc0u;
+  return static_cast<uint16_t>((u + 0x7fffu + ((u >> 16) & 1u)) >> 16);
+}
+
+// ------------------------------------------------------- tile scheduling --
+
+struct Tile {
+  int mat, tm, tn;
+  bool mirror;   // symmetric modes: also store the transposed tile
+};
+
+__device__ __forceinline__ Tile decode_tile(const GemmParams& P, int tile) {
+  Tile t;
+  t.mat = tile / P.tiles_per_mat;
+  const int r = tile - t.mat * P.tiles_per_mat;
+  if (P.mode == kGram || P.mode == kPoly) {
+    // r = 2 * pair + h, pair enumerates 256x256 blocks (I, J) with J <= I
+    const int pair = r >> 1, h = r & 1;
+    int I = static_cast<int>((sqrtf(8.f * static_cast<float>(pair) + 1.f) - 1.f) * 0.5f);
+    while ((I + 1) * (I + 2) / 2 <= pair) ++I;
+    while (I * (I + 1) / 2 > pair) --I;
+    const int J = pair - I * (I + 1) / 2;
+    t.tm = 2 * I + h;
+    t.tn = J;
+    t.mirror = (I != J);
+  } else {
+    t.tn = r / P.tiles_m;
+    t.tm = r - t.tn * P.tiles_m;
+    t.mirror = false;
+  }
+  return t;
+}
+
+// --------------------------------------------------------------- epilogue --
+
+__device__ __forceinline__ void epilogue_chunk(const GemmParams& P, const MuonGroup& grp, const Tile& t,
+                                               int row, int col0, float (&v)[32]) {
+  const int64_t Ap = P.Ap, Bp = P.Bp;
+  if (P.mode == kGram) {
+    float sc = 1.f;
+    if (P.scale_input) {
+      const float in = P.inv_norm[t.mat];
+      sc = in * in;
+    }
+    float* Am = P.Af + static_cast<int64_t>(t.mat) * Ap * Ap;
+    float* dst = Am + static_cast<int64_t>(row) * Ap + col0;
+#pragma unroll
+    for (int j = 0; j < 32; j += 4) {
+      *reinterpret_cast<float4*>(dst + j) = make_float4(v[j] * sc, v[j + 1] * sc, v[j + 2] * sc, v[j + 3] * sc);
+    }
+    if (t.mirror) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) Am[static_cast<int64_t>(col0 + j) * Ap + row] = v[j] * sc;
+    }
+  } else if (P.mode == kPoly) {
+    const float* Am = P.Af + static_cast<int64_t>(t.mat) * Ap * Ap + static_cast<int64_t>(row) * Ap + col0;
+    uint16_t* Bm = P.Bb + static_cast<int64_t>(t.mat) * Ap * Ap;
+    uint32_t packed[16];
+#pragma unroll
+    for (int j = 0; j < 32; j += 4) {
+      const float4 a4 = *reinterpret_cast<const float4*>(Am + j);
+      v[j] = P.b * a4.x + P.c * v[j];
+      v[j + 1] = P.b * a4.y + P.c * v[j + 1];
+      v[j + 2] = P.b * a4.z + P.c * v[j + 2];
+      v[j + 3] = P.b * a4.w + P.c * v[j + 3];
+    }
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+      packed[j] = static_cast<uint32_t>(bf16_rne(v[2 * j])) | (static_cast<uint32_t>(bf16_rne(v[2 * j + 1])) << 16);
+    uint4* dst = reinterpret_cast<uint4*>(Bm + static_cast<int64_t>(row) * Ap + col0);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) dst[j] = make_uint4(packed[4 * j], packed[4 * j + 1], packed[4 * j + 2], packed[4 * j + 3]);
+    if (t.mirror) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        Bm[static_cast<int64_t>(col0 + j) * Ap + row] = static_cast<uint16_t>(packed[j >> 1] >> ((j & 1) * 16));
+    }
+  } else {
+    const float sc = P.scale_input ? P.inv_norm[t.mat] : 1.f;
+    float* Xrow = P.Xf + static_cast<int64_t>(t.mat) * Ap * Bp + static_cast<int64_t>(row) * Bp + col0;
+#pragma unroll
+    for (int j = 0; j < 32; j += 4) {
+      const float4 x4 = *reinterpret_cast<const float4*>(Xrow + j);
+      v[j] = sc * (P.a * x4.x + v[j]);
+      v[j + 1] = sc * (P.a * x4.y + v[j + 1]);
+      v[j + 2] = sc * (P.a * x4.z + v[j + 2]);
+      v[j + 3] = sc * (P.a * x4.w + v[j + 3]);
+    }
+    if (P.mode == kBx) {
+#pragma unroll
+      for (int j = 0; j < 32; j += 4)
+        *reinterpret_cast<float4*>(Xrow + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+      uint32_t packed[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+        packed[j] = static_cast<uint32_t>(bf16_rne(v[2 * j])) | (static_cast<uint32_t>(bf16_rne(v[2 * j + 1])) << 16);
+      uint4* xb = reinterpret_cast<uint4*>(P.Xb + static_cast<int64_t>(t.mat) * Ap * Bp +
+                                           static_cast<int64_t>(row) * Bp + col0);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) xb[j] = make_uint4(packed[4 * j], packed[4 * j + 1], packed[4 * j + 2], packed[4 * j + 3]);
+      uint16_t* xt = P.Xt_out + static_cast<int64_t>(t.mat) * Ap * Bp;
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        xt[static_cast<int64_t>(col0 + j) * Ap + row] = static_cast<uint16_t>(packed[j >> 1] >> ((j & 1) * 16));
+    } else {
+      // last iteration: O = X' (wide orientation, row = A index, col = B index)
+      const MuonMat& M = grp.mats[t.mat];
+      const int64_t A = grp.A, B = grp.B;
+      if (row >= A) return;
+      if (!M.transposed) {
+        const int64_t C = M.C;     // == B
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const int64_t col = col0 + j;
+          if (col < B) {
+            const int64_t i = static_cast<int64_t>(row) * C + col;
+            if (P.ns_only) {
+              M.O[i] = v[j];
+            } else {
+              const float w = M.W[i] * P.decay - P.step_scale * v[j];
+              M.W[i] = w;
+              if (M.Wb) M.Wb[i] = bf16_rne(w);
+            }
+          }
+        }
+      } else {
+        const int64_t C = M.C;     // == A; W[col][row]
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const int64_t col = col0 + j;
+          if (col < B) {
+            const int64_t i = col * C + row;
+            if (P.ns_only) {
+              M.O[i] = v[j];
+            } else {
+              const float w = M.W[i] * P.decay - P.step_scale * v[j];
+              M.W[i] = w;
+              if (M.Wb) M.Wb[i] = bf16_rne(w);
+            }
+          }
+        }
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------------ kernel --
+
+template <int kFmt>
+__global__ void __launch_bounds__(kThreads, 1)
+ns_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
+               const __grid_constant__ GemmParams P, const __grid_constant__ MuonGroup grp) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* stage_a = smem;                                  // kStages x 16 KB
+  uint8_t* stage_b = smem + kStages * kStageA;              // kStages x 32 KB
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
+  uint64_t* full = bars;                     // [kStages]
+  uint64_t* empty = bars + kStages;          // [kStages]
+  uint64_t* acc_full = bars + 2 * kStages;   // [2]
+  uint64_t* acc_empty = acc_full + 2;        // [2]
+  uint64_t* drain = acc_empty + 2;           // [1]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile uint32_t* abort_flag = tmem_slot + 1;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(smem_u32(&full[s]), 1);
+      mbar_init(smem_u32(&empty[s]), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(smem_u32(&acc_full[a]), 1);
+      mbar_init(smem_u32(&acc_empty[a]), 128);
+    }
+    mbar_init(smem_u32(drain), 1);
+    *abort_flag = 0u;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == 0 && lane == 0) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_a)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_b)) : "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  constexpr int kElemsPerKBlock = (kFmt == 2) ? 32 : 64;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------ TMA producer --
+      uint32_t it = 0;
+      uint32_t issued_phase_mask = 0;   // stage s in flight with phase bit
+      uint32_t in_flight = 0;           // bit s: a copy into stage s may be outstanding
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < P.total_tiles; tile += gridDim.x) {
+        const Tile t = decode_tile(P, tile);
+        const int arow = t.tm * BM, brow = t.tn * BN;
+        for (int kb = 0; kb < P.k_blocks; ++kb, ++it) {
+          const uint32_t s = it % kStages, ph = (it / kStages) & 1u;
+          if (!mbar_wait(smem_u32(&empty[s]), ph ^ 1u, abort_flag, P.status, kStatusTimeoutEmpty)) {
+            ok = false;
+            break;
+          }
+          in_flight &= ~(1u << s);   // the consumer released it: the previous copy landed
+          const uint32_t fb = smem_u32(&full[s]);
+          mbar_expect_tx(fb, kStageBytes);
+          const int kx = kb * kElemsPerKBlock;
+          tma_load_3d(smem_u32(stage_a + s * kStageA), &map_a, fb, kx, arow, t.mat);
+          tma_load_3d(smem_u32(stage_b + s * kStageB), &map_b, fb, kx, brow, t.mat);
+          in_flight |= 1u << s;
+          issued_phase_mask = (issued_phase_mask & ~(1u << s)) | (ph << s);
+        }
+      }
+      if (!ok) {
+        // abort: let the copies already issued land before the CTA exits
+        for (uint32_t s = 0; s < kStages; ++s) {
+          if (in_flight & (1u << s)) {
+            const uint32_t ph = (issued_phase_mask >> s) & 1u;
+            const unsigned long long t0 = global_ns();
+            while (!mbar_try(smem_u32(&full[s]), ph) && global_ns() - t0 < kWaitLimitNs) {
+            }
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------- MMA issuer --
+      uint32_t it = 0;
+      int lt = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < P.total_tiles; tile += gridDim.x, ++lt) {
+        const uint32_t acc = lt & 1, acc_ph = (lt >> 1) & 1u;
+        if (!mbar_wait(smem_u32(&acc_empty[acc]), acc_ph ^ 1u, abort_flag, P.status, kStatusTimeoutAccFree)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * BN;
+        for (int kb = 0; kb < P.k_blocks; ++kb, ++it) {
+          const uint32_t s = it % kStages, ph = (it / kStages) & 1u;
+          if (!mbar_wait(smem_u32(&full[s]), ph, abort_flag, P.status, kStatusTimeoutFull)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(stage_a + s * kStageA);
+          const uint32_t b_addr = smem_u32(stage_b + s * kStageB);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {   // 4 MMAs of 32 bytes of K each
+            mma<kFmt>(d_tmem, smem_desc(a_addr + kk * 32), smem_desc(b_addr + kk * 32),
+                      (kb > 0 || kk > 0) ? 1u : 0u);
+          }
+          mma_commit(smem_u32(&empty[s]));
+        }
+        if (!ok) break;
+        mma_commit(smem_u32(&acc_full[acc]));
+      }
+      // drain: every MMA issued by this thread has completed before TMEM goes
+      mma_commit(smem_u32(drain));
+      const unsigned long long t0 = global_ns();
+      while (!mbar_try(smem_u32(drain), 0) && global_ns() - t0 < kWaitLimitNs) {
+      }
+    }
+  } else {
+    // ------------------------------------------------------ epilogue --
+    const int quarter = warp & 3;             // TMEM lanes this warp may access
+    const int row_in_tile = quarter * 32 + lane;
+    int lt = 0;
+    for (int tile = blockIdx.x; tile < P.total_tiles; tile += gridDim.x, ++lt) {
+      const uint32_t acc = lt & 1, acc_ph = (lt >> 1) & 1u;
+      if (!mbar_wait(smem_u32(&acc_full[acc]), acc_ph, abort_flag, P.status, kStatusTimeoutAcc)) break;
+      tc_fence_after();
+      const Tile t = decode_tile(P, tile);
+      const int row = t.tm * BM + row_in_tile;
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * BN;
+      for (int c0 = 0; c0 < BN; c0 += 32) {
+        float v[32];
+        __syncwarp();
+        tmem_ld32(taddr + c0, v);
+        epilogue_chunk(P, grp, t, row, t.tn * BN + c0, v);
+      }
+      tc_fence_before();
+      mbar_arrive(smem_u32(&acc_empty[acc]));
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(kTmemCols)
+                 : "memory");
+  }
+}
+
+// -------------------------------------------------------------- host side --
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// 3-D map over `count` row-major matrices [rows][inner] of 2- or 4-byte
+// elements; box = (128 bytes of inner, box_rows, 1), 128-byte swizzle.
+cudaError_t make_map(CUtensorMap* map, const void* base, int elem_bytes, int64_t inner, int64_t rows,
+                     int64_t count, int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return cudaErrorNotSupported;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows),
+                              static_cast<cuuint64_t>(count)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(inner * elem_bytes),
+                                 static_cast<cuuint64_t>(inner * rows * elem_bytes)};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(kRowBytes / elem_bytes), static_cast<cuuint32_t>(box_rows), 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = fn(map, elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3,
+                        const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+template <int kFmt>
+cudaError_t launch_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const GemmParams& P, const MuonGroup& grp,
+                        cudaStream_t stream) {
+  static thread_local int configured_dev = -1;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (configured_dev != dev) {
+    e = cudaFuncSetAttribute(ns_gemm_kernel<kFmt>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    configured_dev = dev;
+  }
+  const int grid = P.total_tiles < num_sms() ? P.total_tiles : num_sms();
+  ns_gemm_kernel<kFmt><<<grid, kThreads, kSmemBytes, stream>>>(ma, mb, P, grp);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_ns_iteration(const MuonGroup& grp, const NsBuffers& buf, const MuonScalars& s, int it,
+                                cudaStream_t stream) {
+  const int64_t Ap = grp.Ap, Bp = grp.Bp, cnt = grp.count;
+  GemmParams base{};
+  base.count = grp.count;
+  base.Ap = Ap;
+  base.Bp = Bp;
+  base.inv_norm = buf.inv_norm;
+  base.scale_input = (it == 0);
+  base.a = s.a;
+  base.b = s.b;
+  base.c = s.c;
+  base.decay = s.decay;
+  base.step_scale = s.step_scale;
+  base.ns_only = s.ns_only;
+  base.status = buf.status;
+  const int T = static_cast<int>(Ap / 256);
+  cudaError_t e;
+
+  // gram: A = X X^T  (operands: bf16 X [Ap][Bp], K = Bp)
+  {
+    CUtensorMap ma, mb;
+    if ((e = make_map(&ma, buf.Xb, 2, Bp, Ap, cnt, BM)) != cudaSuccess) return e;
+    if ((e = make_map(&mb, buf.Xb, 2, Bp, Ap, cnt, BN)) != cudaSuccess) return e;
+    GemmParams P = base;
+    P.mode = kGram;
+    P.k_blocks = static_cast<int>(Bp / 64);
+    P.tiles_per_mat = T * (T + 1);
+    P.total_tiles = P.tiles_per_mat * grp.count;
+    P.Af = buf.Af;
+    prof_begin(OPT_KERNEL_NS_GRAM, grp.count, grp.A, grp.B, stream);
+    e = launch_gemm<1>(ma, mb, P, grp, stream);
+    prof_end(stream);
+    if (e != cudaSuccess) return e;
+  }
+  // poly: B = b A + c A A  (operands: fp32 A [Ap][Ap] read as tf32, K = Ap)
+  {
+    CUtensorMap ma, mb;
+    if ((e = make_map(&ma, buf.Af, 4, Ap, Ap, cnt, BM)) != cudaSuccess) return e;
+    if ((e = make_map(&mb, buf.Af, 4, Ap, Ap, cnt, BN)) != cudaSuccess) return e;
+    GemmParams P = base;
+    P.mode = kPoly;
+    P.scale_input = 0;
+    P.k_blocks = static_cast<int>(Ap / 32);
+    P.tiles_per_mat = T * (T + 1);
+    P.total_tiles = P.tiles_per_mat * grp.count;
+    P.Af = buf.Af;
+    P.Bb = buf.Bb;
+    prof_begin(OPT_KERNEL_NS_POLY, grp.count, grp.A, grp.B, stream);
+    e = launch_gemm<2>(ma, mb, P, grp, stream);
+    prof_end(stream);
+    if (e != cudaSuccess) return e;
+  }
+  // bx: X' = a X + B X  (operands: bf16 B [Ap][Ap], bf16 X^T [Bp][Ap], K = Ap)
+  {
+    CUtensorMap ma, mb;
+    if ((e = make_map(&ma, buf.Bb, 2, Ap, Ap, cnt, BM)) != cudaSuccess) return e;
+    if ((e = make_map(&mb, buf.Xt[it & 1], 2, Ap, Bp, cnt, BN)) != cudaSuccess) return e;
+    GemmParams P = base;
+    P.mode = (it == s.ns_steps - 1) ? kBxFinal : kBx;
+    P.k_blocks = static_cast<int>(Ap / 64);
+    P.tiles_m = static_cast<int>(Ap / BM);
+    P.tiles_per_mat = static_cast<int>((Ap / BM) * (Bp / BN));
+    P.total_tiles = P.tiles_per_mat * grp.count;
+    P.Xf = buf.X;
+    P.Xb = buf.Xb;
+    P.Xt_out = buf.Xt[(it + 1) & 1];
+    prof_begin(OPT_KERNEL_NS_BX, grp.count, grp.A, grp.B, stream);
+    e = launch_gemm<1>(ma, mb, P, grp, stream);
+    prof_end(stream);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+}  // namespace mpopt

@@ -1,0 +1,170 @@
+"""Host-side tests of the C ABI: the library loads without a GPU, exports
+every function include/mpopt.h declares, and rejects bad arguments on the
+host before anything is enqueued.  Pointers here are fake aligned addresses
+that are never dereferenced (every case returns before a CUDA call)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import mixed_precision_optimizer_gb300 as mp
+from mixed_precision_optimizer_gb300 import build_lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    build_lib.build()
+    return mp.lib()
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "mpopt.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(opt_[a-z_0-9]+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol(L):
+    names = declared_functions()
+    assert len(names) >= 9
+    for n in names:
+        assert hasattr(L, n), n
+    assert set(names) == set(mp.EXPORTED)
+    out = os.popen(f"nm -D --defined-only {mp.LIB_PATH}").read()
+    exported = set(re.findall(r"\bT (opt_\w+)", out))
+    assert exported == set(names), exported ^ set(names)
+
+
+def test_strerror_and_version(L):
+    for code, name in mp.STATUS_NAMES.items():
+        assert L.opt_strerror(code)
+    assert L.opt_strerror(99) == b"unknown status"
+    assert L.opt_abi_version() >> 16 == 1
+
+
+FAKE = 1 << 20     # 1 MiB: an aligned address, never dereferenced
+
+
+def tensor(rows, cols, ndim=2, kind=mp.KIND_AUTO, flags=0, base=FAKE, model=True, sq=True):
+    t = mp.OptTensor()
+    t.main_param, t.main_grad, t.exp_avg = base, base + (1 << 30), base + (2 << 30)
+    t.exp_avg_sq = base + (3 << 30) if sq else None
+    t.model_param = base + (4 << 30) if model else None
+    t.rows, t.cols, t.ndim, t.kind, t.flags = rows, cols, ndim, kind, flags
+    return t
+
+
+def arr(*ts):
+    a = (mp.OptTensor * len(ts))()
+    for i, t in enumerate(ts):
+        a[i] = t
+    return a
+
+
+def adamw(L, ts, hp=None, ws=None, nb=0):
+    hp = hp or mp.adamw_hp()
+    return L.opt_adamw_step(ctypes.byref(hp), arr(*ts), len(ts), ws, nb, None)
+
+
+def test_adamw_argument_errors(L):
+    E = mp.STATUS_NAMES
+    inv, mis = 1, 3
+    assert adamw(L, [tensor(1, 10, 1)], mp.adamw_hp(step=0)) == inv           # t counts from 1
+    assert adamw(L, [tensor(1, 10, 1)], mp.adamw_hp(beta1=1.0)) == inv
+    assert adamw(L, [tensor(1, 10, 1)], mp.adamw_hp(beta2=-0.1)) == inv
+    assert adamw(L, [tensor(1, 10, 1)], mp.adamw_hp(lr=float("nan"))) == inv
+    assert adamw(L, [tensor(1, 10, 1)], mp.adamw_hp(eps=float("inf"))) == inv
+    assert adamw(L, [tensor(1, 10, 1, sq=False)]) == inv                        # v missing
+    t = tensor(1, 10, 1)
+    t.main_grad = None
+    assert adamw(L, [t]) == inv
+    assert adamw(L, [tensor(1, 10, 1, base=FAKE + 2)]) == mis                   # fp32 not 4-B aligned
+    t = tensor(1, 10, 1)
+    t.model_param = FAKE + 1
+    assert adamw(L, [t]) == mis                                                 # bf16 not 2-B aligned
+    assert adamw(L, [tensor(-1, 10, 1)]) == inv
+    assert adamw(L, [tensor(1, 10, 1, kind=7)]) == inv
+    assert L.opt_adamw_step(ctypes.byref(mp.adamw_hp()), None, 3, None, 0, None) == inv
+    assert L.opt_adamw_step(None, arr(tensor(1, 10, 1)), 1, None, 0, None) == inv
+    # nothing to do: empty list and zero-size tensors succeed without a GPU
+    assert L.opt_adamw_step(ctypes.byref(mp.adamw_hp()), None, 0, None, 0, None) == 0
+    t = tensor(0, 5, 2)
+    t.main_param = None
+    assert adamw(L, [t]) == 0
+    assert E[inv] == "OPT_ERR_INVALID_ARG"
+
+
+def test_muon_argument_errors(L):
+    inv = 1
+    hp = mp.muon_hp()
+    ws = ctypes.c_void_p(FAKE)
+    big = 1 << 40
+    assert L.opt_muon_step(ctypes.byref(hp), arr(tensor(8, 16, 1)), ws, big, None) == inv   # not 2-D
+    assert L.opt_muon_step(ctypes.byref(mp.muon_hp(ns_steps=17)), arr(tensor(8, 16)), ws, big, None) == inv
+    assert L.opt_muon_step(ctypes.byref(mp.muon_hp(ns_steps=-1)), arr(tensor(8, 16)), ws, big, None) == inv
+    assert L.opt_muon_step(ctypes.byref(mp.muon_hp(momentum=1.0)), arr(tensor(8, 16)), ws, big, None) == inv
+    assert L.opt_muon_step(ctypes.byref(mp.muon_hp(eps=-1.0)), arr(tensor(8, 16)), ws, big, None) == inv
+    assert L.opt_muon_step(ctypes.byref(mp.muon_hp(coeffs=(1.0, float("nan"), 1.0))), arr(tensor(8, 16)),
+                           ws, big, None) == inv
+    assert L.opt_muon_step(None, arr(tensor(8, 16)), ws, big, None) == inv
+    assert L.opt_muon_step(ctypes.byref(hp), None, ws, big, None) == inv
+    # workspace: missing, misaligned, too small
+    assert L.opt_muon_step(ctypes.byref(hp), arr(tensor(8, 16)), None, 0, None) == 4
+    assert L.opt_muon_step(ctypes.byref(hp), arr(tensor(8, 16)), ctypes.c_void_p(FAKE + 64), big, None) == 4
+    need = L.opt_workspace_size(arr(tensor(8, 16)), 1, mp.KIND_MUON)
+    assert L.opt_muon_step(ctypes.byref(hp), arr(tensor(8, 16)), ws, need - 1, None) == 4
+
+
+def test_workspace_size_formula(L):
+    # one matrix 300 x 200: wide orientation A=200 -> 256, B=300 -> 512
+    Ap, Bp = 256, 512
+    al = lambda x: (x + 1023) // 1024 * 1024
+    ab, aa, blocks = Ap * Bp, Ap * Ap, (Ap // 64) * (Bp // 64)
+    want = 256 + al(ab * 4) + al(ab * 2) + 2 * al(ab * 2) + al(aa * 4) + al(aa * 2) + al(blocks * 4) + al(4)
+    assert L.opt_workspace_size(arr(tensor(300, 200)), 1, mp.KIND_MUON) == want
+    # AdamW needs none
+    assert L.opt_workspace_size(arr(tensor(1, 1000, 1), tensor(30, 40)), 2, mp.KIND_ADAMW) == 0
+    # auto routing: 2-D -> Muon unless flagged embedding/output; 1-D -> AdamW
+    assert L.opt_workspace_size(arr(tensor(1, 1000, 1)), 1, mp.KIND_AUTO) == 0
+    assert L.opt_workspace_size(arr(tensor(300, 200, flags=1)), 1, mp.KIND_AUTO) == 0
+    assert L.opt_workspace_size(arr(tensor(300, 200)), 1, mp.KIND_AUTO) == want
+    # same (min, max) shape in both orientations shares one class: two matrices
+    two = L.opt_workspace_size(arr(tensor(300, 200), tensor(200, 300)), 2, mp.KIND_AUTO)
+    assert two > want
+    # invalid list -> 0
+    assert L.opt_workspace_size(arr(tensor(300, 200, ndim=3)), 1, mp.KIND_MUON) == 0
+    assert L.opt_workspace_size(arr(tensor(300, 200)), 1, 9) == 0
+
+
+def test_newton_schulz_argument_errors(L):
+    ws = ctypes.c_void_p(FAKE)
+    f = L.opt_newton_schulz
+    c = mp.NS_COEFFS
+    assert f(FAKE, FAKE, 8, 16, 17, *c, 1e-7, ws, 1 << 40, None) == 1
+    assert f(None, FAKE, 8, 16, 5, *c, 1e-7, ws, 1 << 40, None) == 1
+    assert f(FAKE + 2, FAKE, 8, 16, 5, *c, 1e-7, ws, 1 << 40, None) == 3
+    assert f(FAKE, FAKE, 8, 16, 5, *c, -1.0, ws, 1 << 40, None) == 1
+    assert f(FAKE, FAKE, 0, 16, 5, *c, 1e-7, ws, 1 << 40, None) == 0     # empty: nothing to do
+    assert f(FAKE, FAKE, 8, 16, 5, *c, 1e-7, None, 0, None) == 4
+
+
+def test_binding_rejects_wrong_tensors():
+    import torch
+    p = torch.zeros(4)
+    with pytest.raises(ValueError):
+        mp.Param(p, p, p, p).to_c()               # CPU tensors are refused
+    with pytest.raises(TypeError):
+        mp.Param(p.double(), p, p, p).to_c()
+
+
+def test_library_has_no_cpu_fallback():
+    """The product path imports nothing from the oracle."""
+    pkg = os.path.join(ROOT, "mixed_precision_optimizer_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".h")):
+                src = open(os.path.join(dirpath, f), encoding="utf-8").read()
+                assert "oracle" not in src.replace("the oracle", ""), f
