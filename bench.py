@@ -380,20 +380,25 @@ def run_ours(args, dist: Dist):
         if k["elems"]:
             e["gbs"] = round(k["elems"] * ADAMW_BYTES_PER_PARAM / (k["ms"] * 1e-3) / 1e9, 1)
         kern_out[name] = e
-    # dominant kernel: the bf16 tensor-core GEMM (X X^T and B X share one kernel)
-    bf16_ms = sum(kernels.get(n, {}).get("ms", 0.0) for n in ("ns_gram", "ns_bx"))
+    # dominant kernel: the fp16 tensor-core GEMM (X X^T, A A and C X are one kernel)
+    ns = ("ns_gram", "ns_poly", "ns_bx")
+    gemm_ms = sum(kernels.get(n, {}).get("ms", 0.0) for n in ns)
     adamw_ms = kernels.get("adamw", {}).get("ms", 0.0)
-    if bf16_ms >= adamw_ms and bf16_ms > 0:
-        fl = sum(kernels.get(n, {}).get("flops", 0.0) for n in ("ns_gram", "ns_bx"))
-        nl = sum(kernels.get(n, {}).get("launches", 0) for n in ("ns_gram", "ns_bx"))
-        achieved = fl / nl / ((bf16_ms / nl) * 1e-3) / 1e12
+    if gemm_ms >= adamw_ms and gemm_ms > 0:
+        fl = sum(kernels.get(n, {}).get("flops", 0.0) for n in ns)
+        ex = sum(kernels.get(n, {}).get("executed", 0.0) for n in ns)
+        nl = sum(kernels.get(n, {}).get("launches", 0) for n in ns)
+        achieved = fl / nl / ((gemm_ms / nl) * 1e-3) / 1e12
+        # fp16 and bf16 share the dense tensor rate (nominal ratio 1), so the
+        # measured bf16 figure is the fp16 peak
         peak = peaks["bf16_tflops_sustained"]
-        tr = kernel_traffic("ns_gemm_bf16")
-        roofline = {"bound": "tensor", "kernel": "ns_gemm_kernel<bf16> (X X^T and B X)",
+        tr = kernel_traffic("ns_gemm")
+        roofline = {"bound": "tensor", "kernel": "ns_gemm_kernel (fp16 x fp16 -> fp32: X X^T, A A, C X)",
                     "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
                     "frac": round(achieved / peak, 4), "traffic": tr,
-                    "peak_source": f"{peak_src} bf16_tflops_sustained",
-                    "per_launch_flops": round(fl / nl), "avg_launch_ms": round(bf16_ms / nl, 4)}
+                    "peak_source": f"{peak_src} bf16_tflops_sustained x nominal fp16/bf16 ratio 1",
+                    "executed_tflops": round(ex / (gemm_ms * 1e-3) / 1e12, 1),
+                    "per_launch_flops": round(fl / nl), "avg_launch_ms": round(gemm_ms / nl, 4)}
     else:
         k = kernels["adamw"]
         achieved = k["elems"] * ADAMW_BYTES_PER_PARAM / (k["ms"] * 1e-3) / 1e9
@@ -419,7 +424,7 @@ def run_ours(args, dist: Dist):
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": dist.world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(elapsed_ms / args.steps, 3), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f32 master/state, bf16+tf32 tensor-core Newton-Schulz",
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32 (master, state, AdamW); Newton-Schulz fp16 x fp16 -> f32 on tensor cores",
         "data": "synthetic (seeded, drawn on the GPU)",
         "config": {"workload": w.name, "params": total, "muon_params": n_muon, "adamw_params": n_adamw,
                    "tensors": len(w.tensors), "parallelism": f"replicas x{dist.world}" if dist.world > 1 else "1 GPU",

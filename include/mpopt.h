@@ -154,9 +154,10 @@ typedef struct {
 /*
  * Bytes of device workspace that opt_mixed_step (and the other steps) need for
  * this tensor list: a 256-byte status header and the Newton-Schulz buffers of
- * the largest group of same-shape Muon matrices (fp32 and bf16 copies of the
- * iterate, its bf16 transpose twice, the fp32 Gram matrix, the bf16
- * polynomial).  AdamW needs no workspace: 0 for a list without Muon tensors.
+ * the largest group of same-shape Muon matrices (the fp16 iterate, its fp16
+ * transpose twice, the Gram matrix in fp32 and fp16, the fp16 polynomial
+ * a I + b A + c A A, norm partials).  Shapes are padded to multiples of 256.
+ * AdamW needs no workspace: 0 for a list without Muon tensors.
  * `routing` selects how kinds are interpreted: OPT_KIND_AUTO as in
  * opt_mixed_step, OPT_KIND_ADAMW treats every tensor as AdamW, OPT_KIND_MUON
  * every tensor as Muon.  Returns 0 if the list is invalid.
@@ -196,7 +197,7 @@ MPOPT_API opt_status opt_mixed_step(const opt_muon_hp* hp_muon, const opt_adamw_
 
 /*
  * Newton-Schulz orthogonalisation alone ("02 · Optimizer：算法与 infra" §5.2):
- * O = NS_steps(G) for one fp32 rows x cols matrix G, same bf16/tf32 tensor-core
+ * O = NS_steps(G) for one fp32 rows x cols matrix G, same fp16 tensor-core
  * path as opt_muon_step.  G and O are device fp32 [rows*cols]; O may alias G.
  * Workspace: opt_workspace_size of a one-matrix Muon list of that shape.
  */
@@ -231,13 +232,14 @@ typedef struct {
 } opt_launch_info;
 
 enum {
-  OPT_KERNEL_NS_GRAM = 0,    /* X X^T, bf16 tensor cores     */
-  OPT_KERNEL_NS_POLY = 1,    /* b A + c A A, tf32 tensor cores */
-  OPT_KERNEL_NS_BX = 2,      /* a X + B X, bf16 tensor cores (last one also updates W) */
+  OPT_KERNEL_NS_GRAM = 0,      /* A = X X^T, fp16 tensor cores                   */
+  OPT_KERNEL_NS_POLY = 1,      /* C = a I + b A + c A A, fp16 tensor cores       */
+  OPT_KERNEL_NS_BX = 2,        /* X' = C X, fp16 tensor cores (last one updates W) */
   OPT_KERNEL_ADAMW = 3,
-  OPT_KERNEL_MUON_PREP = 4,  /* momentum, Nesterov, operand copies, norm partials */
+  OPT_KERNEL_MUON_PREP = 4,    /* momentum, Nesterov, norm partials              */
   OPT_KERNEL_MUON_NORM = 5,
-  OPT_KERNEL_MUON_APPLY = 6  /* ns_steps == 0 only */
+  OPT_KERNEL_MUON_APPLY = 6,   /* ns_steps == 0 only                             */
+  OPT_KERNEL_MUON_OPERANDS = 7 /* normalised fp16 operand copies of X0 and X0^T  */
 };
 
 MPOPT_API opt_status opt_profile_launches(void* const* events, opt_launch_info* info, int32_t capacity,

@@ -72,8 +72,8 @@ EXPORTED = ("opt_workspace_size", "opt_adamw_step", "opt_muon_step", "opt_mixed_
             "opt_newton_schulz", "opt_device_status", "opt_profile_launches", "opt_strerror",
             "opt_last_cuda_error", "opt_abi_version")
 
-KERNEL_NAMES = {0: "ns_gram", 1: "ns_poly", 2: "ns_bx", 3: "adamw", 4: "muon_prep", 5: "muon_norm",
-                6: "muon_apply"}
+KERNEL_NAMES = {0: "ns_gram", 1: "ns_poly", 2: "ns_bx", 3: "adamw", 4: "muon_momentum", 5: "muon_norm",
+                6: "muon_apply", 7: "muon_operands"}
 
 
 class OptLaunchInfo(ctypes.Structure):

@@ -222,46 +222,51 @@ void shape_of(int64_t R, int64_t C, int64_t& A, int64_t& B, int64_t& Ap, int64_t
   Bp = pad_to(B, kNsPad);
 }
 
-size_t group_bytes(int64_t count, int64_t R, int64_t C) {
+// Workspace of one group of `count` matrices with (min, max) = (A, B):
+//   Xh [Ap][Bp] fp16, Xt x2 [Bp][Ap] fp16, A [Ap][Ap] fp32 and fp16,
+//   C [Ap][Ap] fp16, norm partials, inverse norms.
+struct GroupLayout {
+  size_t xh, xt0, xt1, af, ah, ch, partial, inv, total;
+};
+
+GroupLayout group_layout(int64_t count, int64_t R, int64_t C) {
   int64_t A, B, Ap, Bp;
   shape_of(R, C, A, B, Ap, Bp);
   const size_t ab = static_cast<size_t>(Ap) * static_cast<size_t>(Bp);
   const size_t aa = static_cast<size_t>(Ap) * static_cast<size_t>(Ap);
-  const size_t blocks = static_cast<size_t>((Ap / kPrepTile) * (Bp / kPrepTile));
-  size_t b = 0;
-  b += align_up(count * ab * 4, kAlign);      // X fp32
-  b += align_up(count * ab * 2, kAlign);      // Xb
-  b += 2 * align_up(count * ab * 2, kAlign);  // Xt ping-pong
-  b += align_up(count * aa * 4, kAlign);      // A fp32
-  b += align_up(count * aa * 2, kAlign);      // B bf16
-  b += align_up(count * blocks * 4, kAlign);  // partial sums
-  b += align_up(count * 4, kAlign);           // inverse norms
-  return b;
+  const size_t blocks = static_cast<size_t>((A * B + kNormElemsPerBlock - 1) / kNormElemsPerBlock);
+  GroupLayout L{};
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off += align_up(bytes, kAlign);
+    return o;
+  };
+  L.xh = take(count * ab * 2);
+  L.xt0 = take(count * ab * 2);
+  L.xt1 = take(count * ab * 2);
+  L.af = take(count * aa * 4);
+  L.ah = take(count * aa * 2);
+  L.ch = take(count * aa * 2);
+  L.partial = take(count * blocks * 4);
+  L.inv = take(count * 4);
+  L.total = off;
+  return L;
 }
 
+size_t group_bytes(int64_t count, int64_t R, int64_t C) { return group_layout(count, R, C).total; }
+
 NsBuffers carve(uint8_t* base, int64_t count, int64_t R, int64_t C, uint32_t* status) {
-  int64_t A, B, Ap, Bp;
-  shape_of(R, C, A, B, Ap, Bp);
-  const size_t ab = static_cast<size_t>(Ap) * static_cast<size_t>(Bp);
-  const size_t aa = static_cast<size_t>(Ap) * static_cast<size_t>(Ap);
-  const size_t blocks = static_cast<size_t>((Ap / kPrepTile) * (Bp / kPrepTile));
+  const GroupLayout L = group_layout(count, R, C);
   NsBuffers b{};
-  size_t off = 0;
-  b.X = reinterpret_cast<float*>(base + off);
-  off += align_up(count * ab * 4, kAlign);
-  b.Xb = reinterpret_cast<uint16_t*>(base + off);
-  off += align_up(count * ab * 2, kAlign);
-  b.Xt[0] = reinterpret_cast<uint16_t*>(base + off);
-  off += align_up(count * ab * 2, kAlign);
-  b.Xt[1] = reinterpret_cast<uint16_t*>(base + off);
-  off += align_up(count * ab * 2, kAlign);
-  b.Af = reinterpret_cast<float*>(base + off);
-  off += align_up(count * aa * 4, kAlign);
-  b.Bb = reinterpret_cast<uint16_t*>(base + off);
-  off += align_up(count * aa * 2, kAlign);
-  b.partial = reinterpret_cast<float*>(base + off);
-  off += align_up(count * blocks * 4, kAlign);
-  b.inv_norm = reinterpret_cast<float*>(base + off);
+  b.Xh = reinterpret_cast<uint16_t*>(base + L.xh);
+  b.Xt[0] = reinterpret_cast<uint16_t*>(base + L.xt0);
+  b.Xt[1] = reinterpret_cast<uint16_t*>(base + L.xt1);
+  b.Af = reinterpret_cast<float*>(base + L.af);
+  b.Ah = reinterpret_cast<uint16_t*>(base + L.ah);
+  b.Ch = reinterpret_cast<uint16_t*>(base + L.ch);
+  b.partial = reinterpret_cast<float*>(base + L.partial);
+  b.inv_norm = reinterpret_cast<float*>(base + L.inv);
   b.status = status;
   return b;
 }
@@ -331,6 +336,7 @@ opt_status run_muon_class(const MuonPlanHp& hp, const ShapeClass& cls, uint8_t* 
         M.R = static_cast<int32_t>(t->rows);
         M.C = static_cast<int32_t>(t->cols);
         M.transposed = t->rows > t->cols ? 1 : 0;
+        M.vec4 = ((reinterpret_cast<uintptr_t>(M.g) | reinterpret_cast<uintptr_t>(M.m)) & 15u) == 0 ? 1 : 0;
       }
       const NsBuffers buf = carve(region, static_cast<int64_t>(gn), cls.A, cls.B, status);
       MuonScalars s{};
@@ -347,13 +353,19 @@ opt_status run_muon_class(const MuonPlanHp& hp, const ShapeClass& cls, uint8_t* 
       s.ns_steps = hp.ns_steps;
       s.ns_only = hp.ns_only;
       prof_begin(OPT_KERNEL_MUON_PREP, grp.count, grp.A, grp.B, stream);
-      cudaError_t e = launch_muon_prep(grp, buf, s, stream);
+      cudaError_t e = launch_muon_momentum(grp, buf, s, stream);
       prof_end(stream);
-      if (e != cudaSuccess) return cuda_fail(e, "muon prep");
+      if (e != cudaSuccess) return cuda_fail(e, "muon momentum");
       prof_begin(OPT_KERNEL_MUON_NORM, grp.count, grp.A, grp.B, stream);
       e = launch_muon_norm(grp, buf, s, stream);
       prof_end(stream);
       if (e != cudaSuccess) return cuda_fail(e, "muon norm");
+      if (hp.ns_steps > 0) {
+        prof_begin(OPT_KERNEL_MUON_OPERANDS, grp.count, grp.A, grp.B, stream);
+        e = launch_muon_operands(grp, buf, s, stream);
+        prof_end(stream);
+        if (e != cudaSuccess) return cuda_fail(e, "muon operands");
+      }
       if (hp.ns_steps == 0) {
         prof_begin(OPT_KERNEL_MUON_APPLY, grp.count, grp.A, grp.B, stream);
         e = launch_muon_apply_direct(grp, buf, s, stream);

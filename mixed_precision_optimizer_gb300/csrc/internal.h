@@ -69,7 +69,7 @@ struct MuonMat {
   float* O;               // opt_newton_schulz only: fp32 output [R x C], else nullptr
   int32_t R, C;           // this matrix's shape (W layout)
   int32_t transposed;     // R > C: the wide orientation is W^T
-  int32_t pad_;
+  int32_t vec4;           // g and m 16-byte aligned: vector path in the momentum pass
 };
 
 struct MuonGroup {
@@ -80,13 +80,14 @@ struct MuonGroup {
 };
 
 // Workspace buffers of one group (all device pointers into the workspace).
+// Newton-Schulz operands are fp16 (kind::f16 tensor cores); accumulation fp32.
 struct NsBuffers {
-  float* X;          // fp32 iterate            [count][Ap][Bp]
-  uint16_t* Xb;      // bf16 iterate            [count][Ap][Bp]
-  uint16_t* Xt[2];   // bf16 transposed iterate [count][Bp][Ap], ping-pong
+  uint16_t* Xh;      // fp16 iterate            [count][Ap][Bp]
+  uint16_t* Xt[2];   // fp16 transposed iterate [count][Bp][Ap], ping-pong
   float* Af;         // fp32 Gram matrix        [count][Ap][Ap]
-  uint16_t* Bb;      // bf16 polynomial         [count][Ap][Ap]
-  float* partial;    // per-block sums of squares [count][prep_blocks]
+  uint16_t* Ah;      // fp16 Gram matrix        [count][Ap][Ap]
+  uint16_t* Ch;      // fp16 a I + b A + c A A  [count][Ap][Ap]
+  float* partial;    // per-block sums of squares [count][norm_blocks]
   float* inv_norm;   // 1 / (||G||_F + eps)     [count]
   uint32_t* status;  // workspace header word
 };
@@ -102,16 +103,24 @@ struct MuonScalars {
   int ns_only;        // opt_newton_schulz: G is read from g, O written, no momentum/update
 };
 
+// Elementwise pass 1 (momentum, norm partials): fixed elements per block so the
+// reduction order, and hence the result, does not depend on the launch.
+constexpr int64_t kNormElemsPerBlock = 8192;
+inline int64_t norm_blocks_per_matrix(const MuonGroup& g) {
+  return (g.A * g.B + kNormElemsPerBlock - 1) / kNormElemsPerBlock;
+}
+// Elementwise pass 2 (operands): 64 x 64 tiles of the padded W-layout space.
 constexpr int kPrepTile = 64;
-inline int64_t prep_blocks_per_matrix(const MuonGroup& g) {
-  // prep tiles cover the padded W-layout space (Ap x Bp or Bp x Ap)
+inline int64_t operand_blocks_per_matrix(const MuonGroup& g) {
   return (g.Ap / kPrepTile) * (g.Bp / kPrepTile);
 }
 
-cudaError_t launch_muon_prep(const MuonGroup& grp, const NsBuffers& buf, const MuonScalars& s,
-                             cudaStream_t stream);
+cudaError_t launch_muon_momentum(const MuonGroup& grp, const NsBuffers& buf, const MuonScalars& s,
+                                 cudaStream_t stream);
 cudaError_t launch_muon_norm(const MuonGroup& grp, const NsBuffers& buf, const MuonScalars& s,
                              cudaStream_t stream);
+cudaError_t launch_muon_operands(const MuonGroup& grp, const NsBuffers& buf, const MuonScalars& s,
+                                 cudaStream_t stream);
 // ns_steps == 0: O = X0 (no tensor-core work); writes the update / output.
 cudaError_t launch_muon_apply_direct(const MuonGroup& grp, const NsBuffers& buf,
                                      const MuonScalars& s, cudaStream_t stream);

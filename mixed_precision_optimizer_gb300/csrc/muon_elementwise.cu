@@ -1,6 +1,6 @@
-// Muon elementwise stages for sm_103a: momentum and Nesterov lerps, the sum of
-// squares for the Frobenius norm, and the bf16 operand copies that feed the
-// tensor-core Newton-Schulz GEMMs.
+// Muon elementwise stages for sm_103a: momentum and Nesterov lerps, the
+// Frobenius norm, and the fp16 operand copies that feed the tensor-core
+// Newton-Schulz GEMMs.
 //
 // Definitions ("02 · Optimizer：算法与 infra" §1, §5.2; "优化器：AdamW、Muon 与
 // 分布式优化器", Muon section):
@@ -8,19 +8,24 @@
 //   gtilde  = lerp(g, m, mu)     = g + mu (m - g)           (Nesterov; else m)
 //   X0      = gtilde / (||gtilde||_F + eps), transposed when rows > cols
 //
-// The normalisation is not applied here: the prep pass writes gtilde itself
-// (fp32 master copy, bf16 copy, bf16 transposed copy) into the padded,
-// wide-oriented workspace buffers together with per-block sums of squares; a
-// second tiny kernel turns those into 1/(||gtilde||_F + eps), which the first
-// Newton-Schulz GEMMs fold into their epilogues.  One pass over g and m
-// therefore does the whole elementwise part.
+// Pass 1 (muon_momentum_kernel) updates m in place and writes per-block sums
+// of gtilde^2 in a fixed order; muon_norm_kernel reduces them in double to
+// 1/(||gtilde||_F + eps).  Pass 2 (muon_operand_kernel) recomputes gtilde from
+// g and the new m (the same arithmetic, so the same values), scales it, and
+// writes the fp16 operands in both orientations -- X0 (rows = min side) for
+// X X^T and X0^T for the B X product -- into the zero-padded workspace.
+// Normalising before the fp16 conversion keeps every operand in [-1.3, 1.3].
+
+#include <cuda_fp16.h>
 
 #include "internal.h"
 
 namespace mpopt {
 namespace {
 
-constexpr int kPrepThreads = 256;
+constexpr int kThreads = 256;
+
+__device__ __forceinline__ uint16_t f16_bits(float x) { return __half_as_ushort(__float2half_rn(x)); }
 
 __device__ __forceinline__ uint16_t bf16_rne(float x) {
   const uint32_t u = __float_as_uint(x);
@@ -28,81 +33,67 @@ __device__ __forceinline__ uint16_t bf16_rne(float x) {
   return static_cast<uint16_t>((u + 0x7fffu + ((u >> 16) & 1u)) >> 16);
 }
 
-// grid: (prep tiles per matrix, matrices); block: 256 threads; one 64 x 64 tile
-// of the padded W-layout space per block.
-__global__ void __launch_bounds__(kPrepThreads)
-muon_prep_kernel(const MuonGroup grp, NsBuffers buf, MuonScalars s) {
-  __shared__ float tile[kPrepTile][kPrepTile + 1];
-  __shared__ float warp_sums[kPrepThreads / 32];
+// gtilde from g and the already-updated momentum m (or G itself for ns_only).
+__device__ __forceinline__ float gtilde(const MuonScalars& s, float g, float m_new) {
+  if (s.ns_only) return g;
+  return s.nesterov ? g + s.mu * (m_new - g) : m_new;
+}
 
+// grid: (norm blocks per matrix, matrices).  Each block owns elements
+// [blk * 8192, blk * 8192 + 8192) of its matrix in W layout.
+__global__ void __launch_bounds__(kThreads)
+muon_momentum_kernel(const MuonGroup grp, NsBuffers buf, MuonScalars s) {
+  __shared__ float warp_sums[kThreads / 32];
   const int mat = blockIdx.y;
   const MuonMat& M = grp.mats[mat];
-  const int64_t Ap = grp.Ap, Bp = grp.Bp;
-  const bool tr = M.transposed != 0;
-  // padded W-layout extents
-  const int64_t wcols_p = tr ? Ap : Bp;
-  const int64_t tiles_x = wcols_p / kPrepTile;
-  const int64_t ty = blockIdx.x / tiles_x, tx = blockIdx.x % tiles_x;
-  const int64_t r0 = ty * kPrepTile, c0 = tx * kPrepTile;
-  const int R = M.R, C = M.C;
-
-  const int lc = threadIdx.x % kPrepTile;       // column within the tile
-  const int lr0 = threadIdx.x / kPrepTile;      // first row (0..3)
-  float* X = buf.X + static_cast<int64_t>(mat) * Ap * Bp;
-  uint16_t* Xb = buf.Xb + static_cast<int64_t>(mat) * Ap * Bp;
-  uint16_t* Xt = buf.Xt[0] + static_cast<int64_t>(mat) * Ap * Bp;
-
+  const int64_t n = static_cast<int64_t>(M.R) * M.C;
+  const int64_t base = static_cast<int64_t>(blockIdx.x) * kNormElemsPerBlock;
   float ss = 0.f;
-  #pragma unroll 4
-  for (int k = 0; k < kPrepTile / 4; ++k) {
-    const int lr = lr0 + 4 * k;
-    const int64_t r = r0 + lr, c = c0 + lc;
-    float val = 0.f;
-    if (r < R && c < C) {
-      const int64_t i = r * C + c;
-      const float g = M.g[i];
+  if (M.vec4 && base + kNormElemsPerBlock <= n) {   // 16-byte aligned, full block: float4 path
+    const float4* g4 = reinterpret_cast<const float4*>(M.g + base);
+    float4* m4 = reinterpret_cast<float4*>(M.m + base);
+#pragma unroll 4
+    for (int k = 0; k < kNormElemsPerBlock / 4 / kThreads; ++k) {
+      const int j = k * kThreads + threadIdx.x;
+      const float4 g = g4[j];
+      float4 v;
       if (s.ns_only) {
-        val = g;
+        v = g;
       } else {
-        const float m = M.m[i];
-        const float mn = m + s.one_minus_mu * (g - m);
-        M.m[i] = mn;
-        val = s.nesterov ? g + s.mu * (mn - g) : mn;
+        float4 m = m4[j];
+        m.x = m.x + s.one_minus_mu * (g.x - m.x);
+        m.y = m.y + s.one_minus_mu * (g.y - m.y);
+        m.z = m.z + s.one_minus_mu * (g.z - m.z);
+        m.w = m.w + s.one_minus_mu * (g.w - m.w);
+        m4[j] = m;
+        v = make_float4(gtilde(s, g.x, m.x), gtilde(s, g.y, m.y), gtilde(s, g.z, m.z), gtilde(s, g.w, m.w));
       }
+      ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
     }
-    ss += val * val;
-    tile[lr][lc] = val;
-    // W-layout outputs: X (not transposed) or Xt (transposed)
-    if (!tr) {
-      X[r * Bp + c] = val;
-      Xb[r * Bp + c] = bf16_rne(val);
-    } else {
-      Xt[r * Ap + c] = bf16_rne(val);
-    }
-  }
-  __syncthreads();
-  // transposed outputs: element (W row r, W col c) goes to row c, column r
-  #pragma unroll 4
-  for (int k = 0; k < kPrepTile / 4; ++k) {
-    const int i = lr0 + 4 * k;                   // output row within tile (= W col)
-    const int j = lc;                            // output col within tile (= W row)
-    const float val = tile[j][i];
-    const int64_t orow = c0 + i, ocol = r0 + j;
-    if (!tr) {
-      Xt[orow * Ap + ocol] = bf16_rne(val);
-    } else {
-      X[orow * Bp + ocol] = val;
-      Xb[orow * Bp + ocol] = bf16_rne(val);
+  } else {
+    for (int k = 0; k < kNormElemsPerBlock / kThreads; ++k) {
+      const int64_t i = base + k * kThreads + threadIdx.x;
+      if (i >= n) break;
+      const float g = M.g[i];
+      float v;
+      if (s.ns_only) {
+        v = g;
+      } else {
+        const float m_old = M.m[i];
+        const float m = m_old + s.one_minus_mu * (g - m_old);
+        M.m[i] = m;
+        v = gtilde(s, g, m);
+      }
+      ss += v * v;
     }
   }
-  // block sum of squares, fixed order (deterministic)
-  #pragma unroll
+#pragma unroll
   for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
   if ((threadIdx.x & 31) == 0) warp_sums[threadIdx.x >> 5] = ss;
   __syncthreads();
   if (threadIdx.x == 0) {
     float t = 0.f;
-    for (int w = 0; w < kPrepThreads / 32; ++w) t += warp_sums[w];
+    for (int w = 0; w < kThreads / 32; ++w) t += warp_sums[w];
     buf.partial[static_cast<int64_t>(mat) * gridDim.x + blockIdx.x] = t;
   }
 }
@@ -123,18 +114,61 @@ __global__ void muon_norm_kernel(NsBuffers buf, int64_t blocks_per_mat, float ep
   if (threadIdx.x == 0) buf.inv_norm[mat] = static_cast<float>(1.0 / (sqrt(sh[0]) + static_cast<double>(eps)));
 }
 
+// grid: (operand tiles per matrix, matrices); one 64 x 64 tile of the padded
+// W-layout space per block.  Writes the fp16 operand in W layout directly and
+// in the other layout through a shared-memory transpose.
+__global__ void __launch_bounds__(kThreads)
+muon_operand_kernel(const MuonGroup grp, NsBuffers buf, MuonScalars s) {
+  __shared__ uint16_t tile[kPrepTile][kPrepTile + 2];
+  const int mat = blockIdx.y;
+  const MuonMat& M = grp.mats[mat];
+  const int64_t Ap = grp.Ap, Bp = grp.Bp;
+  const bool tr = M.transposed != 0;
+  const int64_t wcols_p = tr ? Ap : Bp;                 // padded W-layout width
+  const int64_t tiles_x = wcols_p / kPrepTile;
+  const int64_t ty = blockIdx.x / tiles_x, tx = blockIdx.x % tiles_x;
+  const int64_t r0 = ty * kPrepTile, c0 = tx * kPrepTile;
+  const int R = M.R, C = M.C;
+  const float inv = buf.inv_norm[mat];
+  const int lc = threadIdx.x % kPrepTile;
+  const int lr0 = threadIdx.x / kPrepTile;
+  uint16_t* Xh = buf.Xh + static_cast<int64_t>(mat) * Ap * Bp;   // [Ap][Bp]
+  uint16_t* Xt = buf.Xt[0] + static_cast<int64_t>(mat) * Ap * Bp; // [Bp][Ap]
+#pragma unroll 4
+  for (int k = 0; k < kPrepTile / 4; ++k) {
+    const int lr = lr0 + 4 * k;
+    const int64_t r = r0 + lr, c = c0 + lc;
+    float val = 0.f;
+    if (r < R && c < C) {
+      const int64_t i = r * C + c;
+      val = gtilde(s, M.g[i], s.ns_only ? 0.f : M.m[i]) * inv;
+    }
+    const uint16_t h = f16_bits(val);
+    tile[lr][lc] = h;
+    if (!tr) Xh[r * Bp + c] = h;     // W layout is the wide layout
+    else     Xt[r * Ap + c] = h;     // W layout is the transposed wide layout
+  }
+  __syncthreads();
+#pragma unroll 4
+  for (int k = 0; k < kPrepTile / 4; ++k) {
+    const int i = lr0 + 4 * k;       // output row within tile (= W column)
+    const int j = lc;                // output column within tile (= W row)
+    const uint16_t h = tile[j][i];
+    const int64_t orow = c0 + i, ocol = r0 + j;
+    if (!tr) Xt[orow * Ap + ocol] = h;
+    else     Xh[orow * Bp + ocol] = h;
+  }
+}
+
 // ns_steps == 0: O = X0 = gtilde * inv_norm; apply the update (or write O).
 __global__ void muon_apply_direct_kernel(const MuonGroup grp, NsBuffers buf, MuonScalars s) {
   const int mat = blockIdx.y;
   const MuonMat& M = grp.mats[mat];
   const int64_t n = static_cast<int64_t>(M.R) * M.C;
   const float inv = buf.inv_norm[mat];
-  const float* X = buf.X + static_cast<int64_t>(mat) * grp.Ap * grp.Bp;
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int64_t r = i / M.C, c = i % M.C;
-    const float x = M.transposed ? X[c * grp.Bp + r] : X[r * grp.Bp + c];
-    const float o = x * inv;
+    const float o = gtilde(s, M.g[i], s.ns_only ? 0.f : M.m[i]) * inv;
     if (s.ns_only) {
       M.O[i] = o;
     } else {
@@ -147,17 +181,23 @@ __global__ void muon_apply_direct_kernel(const MuonGroup grp, NsBuffers buf, Muo
 
 }  // namespace
 
-cudaError_t launch_muon_prep(const MuonGroup& grp, const NsBuffers& buf, const MuonScalars& s,
-                             cudaStream_t stream) {
-  const int64_t blocks = prep_blocks_per_matrix(grp);
-  dim3 grid(static_cast<unsigned>(blocks), static_cast<unsigned>(grp.count));
-  muon_prep_kernel<<<grid, kPrepThreads, 0, stream>>>(grp, buf, s);
+cudaError_t launch_muon_momentum(const MuonGroup& grp, const NsBuffers& buf, const MuonScalars& s,
+                                 cudaStream_t stream) {
+  dim3 grid(static_cast<unsigned>(norm_blocks_per_matrix(grp)), static_cast<unsigned>(grp.count));
+  muon_momentum_kernel<<<grid, kThreads, 0, stream>>>(grp, buf, s);
   return cudaGetLastError();
 }
 
 cudaError_t launch_muon_norm(const MuonGroup& grp, const NsBuffers& buf, const MuonScalars& s,
                              cudaStream_t stream) {
-  muon_norm_kernel<<<grp.count, 256, 0, stream>>>(buf, prep_blocks_per_matrix(grp), s.eps);
+  muon_norm_kernel<<<grp.count, 256, 0, stream>>>(buf, norm_blocks_per_matrix(grp), s.eps);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_muon_operands(const MuonGroup& grp, const NsBuffers& buf, const MuonScalars& s,
+                                 cudaStream_t stream) {
+  dim3 grid(static_cast<unsigned>(operand_blocks_per_matrix(grp)), static_cast<unsigned>(grp.count));
+  muon_operand_kernel<<<grid, kThreads, 0, stream>>>(grp, buf, s);
   return cudaGetLastError();
 }
 

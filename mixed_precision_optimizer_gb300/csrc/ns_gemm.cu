@@ -1,19 +1,21 @@
 // Newton-Schulz GEMMs on the 5th-generation tensor cores (sm_103a).
 //
 // One quintic iteration ("02 · Optimizer：算法与 infra" §5.2; "优化器：AdamW、
-// Muon 与分布式优化器", newton_schulz in the Muon section) on the wide
-// iterate X (A x B, A <= B) is three GEMMs with fused epilogues:
+// Muon 与分布式优化器", newton_schulz in the Muon section) on the wide iterate
+// X (A x B, A <= B), X' = a X + (b A + c A A) X with A = X X^T, is computed as
+// three GEMMs with fused epilogues, all fp16 x fp16 -> fp32 (TMEM):
 //
-//   gram : A_k = X X^T          bf16 x bf16 -> fp32 (TMEM)    -> A fp32
-//   poly : B_k = b A + c A A    tf32 x tf32 -> fp32, + b*A    -> B bf16
-//   bx   : X'  = a X + B X      bf16 x bf16 -> fp32, + a*X    -> X fp32, X bf16, X^T bf16
+//   gram : A = X X^T                        -> A fp32 (for b A), A fp16 (operand)
+//   poly : C = a I + b A + c (A A)          -> C fp16
+//   bx   : X' = C X                         -> X' fp16, X'^T fp16 (next operands)
 //          (last iteration: W <- W (1 - lr*lambda) - lr*0.2*sqrt(max(A,B)) * X',
-//           written in W's own orientation together with its bf16 copy)
+//           from the fp32 accumulator, in W's own orientation, with its bf16 copy)
 //
-// Precision: X is carried in fp32 between iterations (the a*X term of the
-// epilogue reads the fp32 copy); bf16 appears only as MMA operands.  The
-// A*A product runs in tf32 because rounding A to bf16 there is the largest
-// single error term of the iteration.  Accumulation is fp32 in TMEM.
+// Number formats: folding a I into C keeps the large cancelling terms a X and
+// B X (|a| = 3.44, B ~ -2.74 near unit singular values) inside one rounded
+// operand, and fp16 operands (11-bit significands, values normalised into
+// [-1.3, 1.3] before the first conversion) keep the rounding of C and X well
+// below the tolerance; both run at the same tensor-core rate as bf16.
 //
 // Kernel structure (one CTA per SM, persistent over output tiles):
 //   warp 0    TMA producer: 128-row A tile + 256-row B tile per k-block,
@@ -22,7 +24,9 @@
 //             elected thread, 4 MMAs per 128-byte k-block, commit to free the
 //             stage; a 2 x 256-column accumulator lets the epilogue of one
 //             tile overlap the main loop of the next
-//   warps 2-5 epilogue: tcgen05.ld 32 columns at a time, fused math, stores
+//   warps 2-5 epilogue: tcgen05.ld 32 columns at a time, fused math, stores;
+//             each warp transposes 32 x 32 blocks through its own shared-memory
+//             slab for the transposed outputs
 //
 // The Gram matrix and the polynomial are symmetric: only 128x256 tiles of
 // 256x256 blocks on or below the diagonal are computed, and off-diagonal
@@ -35,6 +39,7 @@
 // waits) before TMEM is released.
 
 #include <cuda.h>
+#include <cuda_fp16.h>
 
 #include "../../include/mpopt.h"
 #include "internal.h"
@@ -51,7 +56,9 @@ constexpr int kStageB = BN * kRowBytes;        // 32 KB
 constexpr int kStageBytes = kStageA + kStageB;
 constexpr int kThreads = 192;
 constexpr int kTmemCols = 512;                 // 2 accumulators x 256 fp32 columns
-constexpr uint32_t kSmemBytes = kStages * kStageBytes + 1024 /*align*/ + 256 /*barriers*/;
+constexpr int kSlabWords = 32 * 33;            // per epilogue warp: 32 x 32 fp32, padded rows
+constexpr int kSlabBytes = 4 * kSlabWords * 4;
+constexpr uint32_t kSmemBytes = kStages * kStageBytes + kSlabBytes + 1024 /*align*/ + 256 /*barriers*/;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 
 struct GemmParams {
@@ -62,13 +69,11 @@ struct GemmParams {
   int tiles_m;          // bx: Ap / BM
   int count;
   int64_t Ap, Bp;
-  float* Xf;            // bx: fp32 iterate (in/out)
-  uint16_t* Xb;         // bx: bf16 iterate out
-  uint16_t* Xt_out;     // bx: bf16 transposed iterate out
-  float* Af;            // gram: out; poly: in
-  uint16_t* Bb;         // poly: out
-  const float* inv_norm;
-  int scale_input;      // iteration 0: the operands hold gtilde, fold in 1/||gtilde||
+  float* Af;            // gram: out; poly: in (b A term)
+  uint16_t* Ah;         // gram: out (fp16 operand of A A)
+  uint16_t* Ch;         // poly: out
+  uint16_t* Xh;         // bx: fp16 iterate out
+  uint16_t* Xt_out;     // bx: fp16 transposed iterate out
   float a, b, c;
   float decay, step_scale;
   int ns_only;
@@ -152,30 +157,21 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr) {
   return d;
 }
 
-// Instruction descriptor: fp32 accumulator, A and B of format `fmt`
-// (1 = bf16 for kind::f16, 2 = tf32 for kind::tf32), both K-major, M = 128, N = 256.
-template <int kFmt>
+// Instruction descriptor for kind::f16: fp32 accumulator (bits 4-5 = 1), A and
+// B fp16 (format 0 in bits 7-9 and 10-12), both K-major, N = 256 (bits 17-22,
+// N >> 3), M = 128 (bits 24-28, M >> 4).
 __host__ __device__ constexpr uint32_t instr_desc() {
-  return (1u << 4) | (static_cast<uint32_t>(kFmt) << 7) | (static_cast<uint32_t>(kFmt) << 10) |
-         (static_cast<uint32_t>(BN >> 3) << 17) | (static_cast<uint32_t>(BM >> 4) << 24);
+  return (1u << 4) | (0u << 7) | (0u << 10) | (static_cast<uint32_t>(BN >> 3) << 17) |
+         (static_cast<uint32_t>(BM >> 4) << 24);
 }
 
-template <int kFmt>
 __device__ __forceinline__ void mma(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t accumulate) {
-  constexpr uint32_t idesc = instr_desc<kFmt>();
-  if constexpr (kFmt == 2) {
-    asm volatile(
-        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-        " tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n}" ::"r"(tmem_d),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-        : "memory");
-  } else {
-    asm volatile(
-        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(tmem_d),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-        : "memory");
-  }
+  constexpr uint32_t idesc = instr_desc();
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
 }
 
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
@@ -204,12 +200,6 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
   for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-}
-
-__device__ __forceinline__ uint16_t bf16_rne(float x) {
-  const uint32_t u = __float_as_uint(x);
-  if ((u & 0x7fffffffu) > 0x7f800000u) return 0x7fc0u;
-  return static_cast<uint16_t>((u + 0x7fffu + ((u >> 16) & 1u)) >> 16);
 }
 
 // ------------------------------------------------------- tile scheduling --
@@ -243,98 +233,95 @@ __device__ __forceinline__ Tile decode_tile(const GemmParams& P, int tile) {
 
 // --------------------------------------------------------------- epilogue --
 
-__device__ __forceinline__ void epilogue_chunk(const GemmParams& P, const MuonGroup& grp, const Tile& t,
-                                               int row, int col0, float (&v)[32]) {
+__device__ __forceinline__ uint16_t f16_bits(float x) { return __half_as_ushort(__float2half_rn(x)); }
+
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+  return static_cast<uint32_t>(f16_bits(lo)) | (static_cast<uint32_t>(f16_bits(hi)) << 16);
+}
+
+// Store 32 consecutive fp16 values (64 bytes, 16-byte aligned destination).
+__device__ __forceinline__ void store_f16x32(uint16_t* dst, const float (&v)[32]) {
+  uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    d[q] = make_uint4(pack_f16(v[8 * q], v[8 * q + 1]), pack_f16(v[8 * q + 2], v[8 * q + 3]),
+                      pack_f16(v[8 * q + 4], v[8 * q + 5]), pack_f16(v[8 * q + 6], v[8 * q + 7]));
+}
+
+// Store 32 consecutive fp32 values (128 bytes, 16-byte aligned destination).
+__device__ __forceinline__ void store_f32x32(float* dst, const float (&v)[32]) {
+#pragma unroll
+  for (int q = 0; q < 8; ++q)
+    reinterpret_cast<float4*>(dst)[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+}
+
+// Warp-level 32 x 32 transpose through the warp's shared-memory slab: on
+// entry lane t holds row t (columns 0..31) in v; on exit lane t holds column t
+// (rows 0..31) in w.
+__device__ __forceinline__ void warp_transpose(float* slab, int lane, const float (&v)[32], float (&w)[32]) {
+#pragma unroll
+  for (int j = 0; j < 32; ++j) slab[lane * 33 + j] = v[j];
+  __syncwarp();
+#pragma unroll
+  for (int r = 0; r < 32; ++r) w[r] = slab[r * 33 + lane];
+  __syncwarp();
+}
+
+// fp32 -> bf16 bits, round to nearest, ties to even; NaN -> 0x7FC0 (adding
+// 0x7FFF plus the lowest kept bit carries into the kept half exactly when the
+// dropped half is above one half, or one half with an odd kept half).
+__device__ __forceinline__ uint16_t bf16_rne(float x) {
+  const uint32_t u = __float_as_uint(x);
+  if ((u & 0x7fffffffu) > 0x7f800000u) return 0x7fc0u;
+  return static_cast<uint16_t>((u + 0x7fffu + ((u >> 16) & 1u)) >> 16);
+}
+
+// One 32-row x 32-column block of the tile held by one epilogue warp: lane
+// `lane` holds row row0 + lane, columns col0 .. col0 + 31, in v.
+__device__ __forceinline__ void epilogue_block(const GemmParams& P, const MuonGroup& grp, const Tile& t,
+                                               float* slab, int lane, int row0, int col0, float (&v)[32]) {
   const int64_t Ap = P.Ap, Bp = P.Bp;
+  const int row = row0 + lane;
+  float w[32];
   if (P.mode == kGram) {
-    float sc = 1.f;
-    if (P.scale_input) {
-      const float in = P.inv_norm[t.mat];
-      sc = in * in;
-    }
     float* Am = P.Af + static_cast<int64_t>(t.mat) * Ap * Ap;
-    float* dst = Am + static_cast<int64_t>(row) * Ap + col0;
-#pragma unroll
-    for (int j = 0; j < 32; j += 4) {
-      *reinterpret_cast<float4*>(dst + j) = make_float4(v[j] * sc, v[j + 1] * sc, v[j + 2] * sc, v[j + 3] * sc);
-    }
+    uint16_t* Ahm = P.Ah + static_cast<int64_t>(t.mat) * Ap * Ap;
+    store_f32x32(Am + static_cast<int64_t>(row) * Ap + col0, v);
+    store_f16x32(Ahm + static_cast<int64_t>(row) * Ap + col0, v);
     if (t.mirror) {
-#pragma unroll
-      for (int j = 0; j < 32; ++j) Am[static_cast<int64_t>(col0 + j) * Ap + row] = v[j] * sc;
+      warp_transpose(slab, lane, v, w);   // lane now holds column col0 + lane, rows row0..row0+31
+      store_f32x32(Am + static_cast<int64_t>(col0 + lane) * Ap + row0, w);
+      store_f16x32(Ahm + static_cast<int64_t>(col0 + lane) * Ap + row0, w);
     }
   } else if (P.mode == kPoly) {
-    const float* Am = P.Af + static_cast<int64_t>(t.mat) * Ap * Ap + static_cast<int64_t>(row) * Ap + col0;
-    uint16_t* Bm = P.Bb + static_cast<int64_t>(t.mat) * Ap * Ap;
-    uint32_t packed[16];
+    const float* Arow = P.Af + static_cast<int64_t>(t.mat) * Ap * Ap + static_cast<int64_t>(row) * Ap + col0;
+    uint16_t* Cm = P.Ch + static_cast<int64_t>(t.mat) * Ap * Ap;
 #pragma unroll
-    for (int j = 0; j < 32; j += 4) {
-      const float4 a4 = *reinterpret_cast<const float4*>(Am + j);
-      v[j] = P.b * a4.x + P.c * v[j];
-      v[j + 1] = P.b * a4.y + P.c * v[j + 1];
-      v[j + 2] = P.b * a4.z + P.c * v[j + 2];
-      v[j + 3] = P.b * a4.w + P.c * v[j + 3];
+    for (int q = 0; q < 8; ++q) {
+      const float4 a4 = reinterpret_cast<const float4*>(Arow)[q];
+      v[4 * q + 0] = P.b * a4.x + P.c * v[4 * q + 0];
+      v[4 * q + 1] = P.b * a4.y + P.c * v[4 * q + 1];
+      v[4 * q + 2] = P.b * a4.z + P.c * v[4 * q + 2];
+      v[4 * q + 3] = P.b * a4.w + P.c * v[4 * q + 3];
     }
 #pragma unroll
-    for (int j = 0; j < 16; ++j)
-      packed[j] = static_cast<uint32_t>(bf16_rne(v[2 * j])) | (static_cast<uint32_t>(bf16_rne(v[2 * j + 1])) << 16);
-    uint4* dst = reinterpret_cast<uint4*>(Bm + static_cast<int64_t>(row) * Ap + col0);
-#pragma unroll
-    for (int j = 0; j < 4; ++j) dst[j] = make_uint4(packed[4 * j], packed[4 * j + 1], packed[4 * j + 2], packed[4 * j + 3]);
+    for (int j = 0; j < 32; ++j) v[j] += (row == col0 + j) ? P.a : 0.f;   // + a I
+    store_f16x32(Cm + static_cast<int64_t>(row) * Ap + col0, v);
     if (t.mirror) {
-#pragma unroll
-      for (int j = 0; j < 32; ++j)
-        Bm[static_cast<int64_t>(col0 + j) * Ap + row] = static_cast<uint16_t>(packed[j >> 1] >> ((j & 1) * 16));
+      warp_transpose(slab, lane, v, w);
+      store_f16x32(Cm + static_cast<int64_t>(col0 + lane) * Ap + row0, w);
     }
+  } else if (P.mode == kBx) {
+    store_f16x32(P.Xh + static_cast<int64_t>(t.mat) * Ap * Bp + static_cast<int64_t>(row) * Bp + col0, v);
+    warp_transpose(slab, lane, v, w);
+    store_f16x32(P.Xt_out + static_cast<int64_t>(t.mat) * Ap * Bp + static_cast<int64_t>(col0 + lane) * Ap + row0, w);
   } else {
-    const float sc = P.scale_input ? P.inv_norm[t.mat] : 1.f;
-    float* Xrow = P.Xf + static_cast<int64_t>(t.mat) * Ap * Bp + static_cast<int64_t>(row) * Bp + col0;
-#pragma unroll
-    for (int j = 0; j < 32; j += 4) {
-      const float4 x4 = *reinterpret_cast<const float4*>(Xrow + j);
-      v[j] = sc * (P.a * x4.x + v[j]);
-      v[j + 1] = sc * (P.a * x4.y + v[j + 1]);
-      v[j + 2] = sc * (P.a * x4.z + v[j + 2]);
-      v[j + 3] = sc * (P.a * x4.w + v[j + 3]);
-    }
-    if (P.mode == kBx) {
-#pragma unroll
-      for (int j = 0; j < 32; j += 4)
-        *reinterpret_cast<float4*>(Xrow + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
-      uint32_t packed[16];
-#pragma unroll
-      for (int j = 0; j < 16; ++j)
-        packed[j] = static_cast<uint32_t>(bf16_rne(v[2 * j])) | (static_cast<uint32_t>(bf16_rne(v[2 * j + 1])) << 16);
-      uint4* xb = reinterpret_cast<uint4*>(P.Xb + static_cast<int64_t>(t.mat) * Ap * Bp +
-                                           static_cast<int64_t>(row) * Bp + col0);
-#pragma unroll
-      for (int j = 0; j < 4; ++j) xb[j] = make_uint4(packed[4 * j], packed[4 * j + 1], packed[4 * j + 2], packed[4 * j + 3]);
-      uint16_t* xt = P.Xt_out + static_cast<int64_t>(t.mat) * Ap * Bp;
-#pragma unroll
-      for (int j = 0; j < 32; ++j)
-        xt[static_cast<int64_t>(col0 + j) * Ap + row] = static_cast<uint16_t>(packed[j >> 1] >> ((j & 1) * 16));
-    } else {
-      // last iteration: O = X' (wide orientation, row = A index, col = B index)
-      const MuonMat& M = grp.mats[t.mat];
-      const int64_t A = grp.A, B = grp.B;
-      if (row >= A) return;
-      if (!M.transposed) {
-        const int64_t C = M.C;     // == B
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const int64_t col = col0 + j;
-          if (col < B) {
-            const int64_t i = static_cast<int64_t>(row) * C + col;
-            if (P.ns_only) {
-              M.O[i] = v[j];
-            } else {
-              const float w = M.W[i] * P.decay - P.step_scale * v[j];
-              M.W[i] = w;
-              if (M.Wb) M.Wb[i] = bf16_rne(w);
-            }
-          }
-        }
-      } else {
-        const int64_t C = M.C;     // == A; W[col][row]
+    // last iteration: O = X' in the wide orientation (rows: A index, columns: B index)
+    const MuonMat& M = grp.mats[t.mat];
+    const int64_t A = grp.A, B = grp.B, C = M.C;
+    if (M.transposed) {
+      // W[col][row]: for each column j the warp writes 32 consecutive row entries
+      if (row < A) {
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
           const int64_t col = col0 + j;
@@ -343,9 +330,29 @@ __device__ __forceinline__ void epilogue_chunk(const GemmParams& P, const MuonGr
             if (P.ns_only) {
               M.O[i] = v[j];
             } else {
-              const float w = M.W[i] * P.decay - P.step_scale * v[j];
-              M.W[i] = w;
-              if (M.Wb) M.Wb[i] = bf16_rne(w);
+              const float wv = M.W[i] * P.decay - P.step_scale * v[j];
+              M.W[i] = wv;
+              if (M.Wb) M.Wb[i] = bf16_rne(wv);
+            }
+          }
+        }
+      }
+    } else {
+      // W[row][col]: transpose so that for each row k the warp writes 32 consecutive columns
+      warp_transpose(slab, lane, v, w);
+      const int64_t col = col0 + lane;
+      if (col < B) {
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+          const int64_t r = row0 + k;
+          if (r < A) {
+            const int64_t i = r * C + col;
+            if (P.ns_only) {
+              M.O[i] = w[k];
+            } else {
+              const float wv = M.W[i] * P.decay - P.step_scale * w[k];
+              M.W[i] = wv;
+              if (M.Wb) M.Wb[i] = bf16_rne(wv);
             }
           }
         }
@@ -356,7 +363,6 @@ __device__ __forceinline__ void epilogue_chunk(const GemmParams& P, const MuonGr
 
 // ------------------------------------------------------------------ kernel --
 
-template <int kFmt>
 __global__ void __launch_bounds__(kThreads, 1)
 ns_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                const __grid_constant__ GemmParams P, const __grid_constant__ MuonGroup grp) {
@@ -364,7 +370,8 @@ ns_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* stage_a = smem;                                  // kStages x 16 KB
   uint8_t* stage_b = smem + kStages * kStageA;              // kStages x 32 KB
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
+  float* slabs = reinterpret_cast<float*>(smem + kStages * kStageBytes);   // 4 x 32 x 33 fp32
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes + kSlabBytes);
   uint64_t* full = bars;                     // [kStages]
   uint64_t* empty = bars + kStages;          // [kStages]
   uint64_t* acc_full = bars + 2 * kStages;   // [2]
@@ -405,7 +412,7 @@ ns_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  constexpr int kElemsPerKBlock = (kFmt == 2) ? 32 : 64;
+  constexpr int kElemsPerKBlock = 64;          // 128 bytes of fp16 per row
 
   if (warp == 0) {
     if (lane == 0) {
@@ -470,7 +477,7 @@ ns_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
           const uint32_t b_addr = smem_u32(stage_b + s * kStageB);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {   // 4 MMAs of 32 bytes of K each
-            mma<kFmt>(d_tmem, smem_desc(a_addr + kk * 32), smem_desc(b_addr + kk * 32),
+            mma(d_tmem, smem_desc(a_addr + kk * 32), smem_desc(b_addr + kk * 32),
                       (kb > 0 || kk > 0) ? 1u : 0u);
           }
           mma_commit(smem_u32(&empty[s]));
@@ -487,20 +494,20 @@ ns_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
   } else {
     // ------------------------------------------------------ epilogue --
     const int quarter = warp & 3;             // TMEM lanes this warp may access
-    const int row_in_tile = quarter * 32 + lane;
+    float* slab = slabs + (warp - 2) * kSlabWords;
     int lt = 0;
     for (int tile = blockIdx.x; tile < P.total_tiles; tile += gridDim.x, ++lt) {
       const uint32_t acc = lt & 1, acc_ph = (lt >> 1) & 1u;
       if (!mbar_wait(smem_u32(&acc_full[acc]), acc_ph, abort_flag, P.status, kStatusTimeoutAcc)) break;
       tc_fence_after();
       const Tile t = decode_tile(P, tile);
-      const int row = t.tm * BM + row_in_tile;
+      const int row0 = t.tm * BM + quarter * 32;
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * BN;
       for (int c0 = 0; c0 < BN; c0 += 32) {
         float v[32];
         __syncwarp();
         tmem_ld32(taddr + c0, v);
-        epilogue_chunk(P, grp, t, row, t.tn * BN + c0, v);
+        epilogue_block(P, grp, t, slab, lane, row0, t.tn * BN + c0, v);
       }
       tc_fence_before();
       mbar_arrive(smem_u32(&acc_empty[acc]));
@@ -535,26 +542,22 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// 3-D map over `count` row-major matrices [rows][inner] of 2- or 4-byte
-// elements; box = (128 bytes of inner, box_rows, 1), 128-byte swizzle.
-cudaError_t make_map(CUtensorMap* map, const void* base, int elem_bytes, int64_t inner, int64_t rows,
-                     int64_t count, int box_rows) {
+// 3-D map over `count` row-major fp16 matrices [rows][inner]; box = (64
+// elements = 128 bytes of inner, box_rows, 1), 128-byte swizzle.
+cudaError_t make_map(CUtensorMap* map, const void* base, int64_t inner, int64_t rows, int64_t count, int box_rows) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return cudaErrorNotSupported;
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows),
                               static_cast<cuuint64_t>(count)};
-  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(inner * elem_bytes),
-                                 static_cast<cuuint64_t>(inner * rows * elem_bytes)};
-  const cuuint32_t box[3] = {static_cast<cuuint32_t>(kRowBytes / elem_bytes), static_cast<cuuint32_t>(box_rows), 1};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(inner * 2), static_cast<cuuint64_t>(inner * rows * 2)};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(kRowBytes / 2), static_cast<cuuint32_t>(box_rows), 1};
   const cuuint32_t estr[3] = {1, 1, 1};
-  const CUresult r = fn(map, elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3,
-                        const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <int kFmt>
 cudaError_t launch_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const GemmParams& P, const MuonGroup& grp,
                         cudaStream_t stream) {
   static thread_local int configured_dev = -1;
@@ -562,12 +565,12 @@ cudaError_t launch_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const Gemm
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (configured_dev != dev) {
-    e = cudaFuncSetAttribute(ns_gemm_kernel<kFmt>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    e = cudaFuncSetAttribute(ns_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
     configured_dev = dev;
   }
   const int grid = P.total_tiles < num_sms() ? P.total_tiles : num_sms();
-  ns_gemm_kernel<kFmt><<<grid, kThreads, kSmemBytes, stream>>>(ma, mb, P, grp);
+  ns_gemm_kernel<<<grid, kThreads, kSmemBytes, stream>>>(ma, mb, P, grp);
   return cudaGetLastError();
 }
 
@@ -580,8 +583,6 @@ cudaError_t launch_ns_iteration(const MuonGroup& grp, const NsBuffers& buf, cons
   base.count = grp.count;
   base.Ap = Ap;
   base.Bp = Bp;
-  base.inv_norm = buf.inv_norm;
-  base.scale_input = (it == 0);
   base.a = s.a;
   base.b = s.b;
   base.c = s.c;
@@ -592,56 +593,55 @@ cudaError_t launch_ns_iteration(const MuonGroup& grp, const NsBuffers& buf, cons
   const int T = static_cast<int>(Ap / 256);
   cudaError_t e;
 
-  // gram: A = X X^T  (operands: bf16 X [Ap][Bp], K = Bp)
+  // gram: A = X X^T  (operands: fp16 X [Ap][Bp], K = Bp)
   {
     CUtensorMap ma, mb;
-    if ((e = make_map(&ma, buf.Xb, 2, Bp, Ap, cnt, BM)) != cudaSuccess) return e;
-    if ((e = make_map(&mb, buf.Xb, 2, Bp, Ap, cnt, BN)) != cudaSuccess) return e;
+    if ((e = make_map(&ma, buf.Xh, Bp, Ap, cnt, BM)) != cudaSuccess) return e;
+    if ((e = make_map(&mb, buf.Xh, Bp, Ap, cnt, BN)) != cudaSuccess) return e;
     GemmParams P = base;
     P.mode = kGram;
     P.k_blocks = static_cast<int>(Bp / 64);
     P.tiles_per_mat = T * (T + 1);
     P.total_tiles = P.tiles_per_mat * grp.count;
     P.Af = buf.Af;
+    P.Ah = buf.Ah;
     prof_begin(OPT_KERNEL_NS_GRAM, grp.count, grp.A, grp.B, stream);
-    e = launch_gemm<1>(ma, mb, P, grp, stream);
+    e = launch_gemm(ma, mb, P, grp, stream);
     prof_end(stream);
     if (e != cudaSuccess) return e;
   }
-  // poly: B = b A + c A A  (operands: fp32 A [Ap][Ap] read as tf32, K = Ap)
+  // poly: C = a I + b A + c A A  (operands: fp16 A [Ap][Ap], K = Ap)
   {
     CUtensorMap ma, mb;
-    if ((e = make_map(&ma, buf.Af, 4, Ap, Ap, cnt, BM)) != cudaSuccess) return e;
-    if ((e = make_map(&mb, buf.Af, 4, Ap, Ap, cnt, BN)) != cudaSuccess) return e;
+    if ((e = make_map(&ma, buf.Ah, Ap, Ap, cnt, BM)) != cudaSuccess) return e;
+    if ((e = make_map(&mb, buf.Ah, Ap, Ap, cnt, BN)) != cudaSuccess) return e;
     GemmParams P = base;
     P.mode = kPoly;
-    P.scale_input = 0;
-    P.k_blocks = static_cast<int>(Ap / 32);
+    P.k_blocks = static_cast<int>(Ap / 64);
     P.tiles_per_mat = T * (T + 1);
     P.total_tiles = P.tiles_per_mat * grp.count;
     P.Af = buf.Af;
-    P.Bb = buf.Bb;
+    P.Ch = buf.Ch;
     prof_begin(OPT_KERNEL_NS_POLY, grp.count, grp.A, grp.B, stream);
-    e = launch_gemm<2>(ma, mb, P, grp, stream);
+    e = launch_gemm(ma, mb, P, grp, stream);
     prof_end(stream);
     if (e != cudaSuccess) return e;
   }
-  // bx: X' = a X + B X  (operands: bf16 B [Ap][Ap], bf16 X^T [Bp][Ap], K = Ap)
+  // bx: X' = C X  (operands: fp16 C [Ap][Ap], fp16 X^T [Bp][Ap], K = Ap)
   {
     CUtensorMap ma, mb;
-    if ((e = make_map(&ma, buf.Bb, 2, Ap, Ap, cnt, BM)) != cudaSuccess) return e;
-    if ((e = make_map(&mb, buf.Xt[it & 1], 2, Ap, Bp, cnt, BN)) != cudaSuccess) return e;
+    if ((e = make_map(&ma, buf.Ch, Ap, Ap, cnt, BM)) != cudaSuccess) return e;
+    if ((e = make_map(&mb, buf.Xt[it & 1], Ap, Bp, cnt, BN)) != cudaSuccess) return e;
     GemmParams P = base;
     P.mode = (it == s.ns_steps - 1) ? kBxFinal : kBx;
     P.k_blocks = static_cast<int>(Ap / 64);
     P.tiles_m = static_cast<int>(Ap / BM);
     P.tiles_per_mat = static_cast<int>((Ap / BM) * (Bp / BN));
     P.total_tiles = P.tiles_per_mat * grp.count;
-    P.Xf = buf.X;
-    P.Xb = buf.Xb;
+    P.Xh = buf.Xh;
     P.Xt_out = buf.Xt[(it + 1) & 1];
     prof_begin(OPT_KERNEL_NS_BX, grp.count, grp.A, grp.B, stream);
-    e = launch_gemm<1>(ma, mb, P, grp, stream);
+    e = launch_gemm(ma, mb, P, grp, stream);
     prof_end(stream);
     if (e != cudaSuccess) return e;
   }

@@ -148,6 +148,24 @@ def test_muon_step_options(kw):
     muon_case((200, 328), np.random.default_rng(11), **kw)
 
 
+@pytest.mark.parametrize("scale", [1e-6, 1e-3, 1e3])
+def test_newton_schulz_scale_invariance(scale):
+    """The normalisation makes the iteration independent of the gradient's
+    scale; the fp16 operands are formed after it, so tiny and large
+    gradients keep the same accuracy."""
+    rng = np.random.default_rng(31)
+    G = (rng.standard_normal((384, 1000)) * scale).astype(np.float32)
+    want = OM.newton_schulz(G.astype(np.float64))
+    assert rel(ns_gpu(G), want) < NS_TOL
+
+
+def test_newton_schulz_many_steps():
+    rng = np.random.default_rng(32)
+    G = rng.standard_normal((256, 512)).astype(np.float32)
+    for steps in (8, 16):
+        assert rel(ns_gpu(G, steps), OM.newton_schulz(G.astype(np.float64), steps)) < NS_TOL
+
+
 def test_tiny_mixed_workload_10_steps():
     """The tiny mixed workload through opt_mixed_step: one 256x512 Muon
     matrix and one 512-vector under AdamW, 10 steps.  Each step is checked
