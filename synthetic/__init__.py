@@ -136,12 +136,21 @@ def llama16_mixed(layers=16, vocab=128256, hidden=4096):
                     adamw=AdamWHP(weight_decay=0.1), muon=MuonHP(weight_decay=0.0))
 
 
+def llama_mlp_1layer():
+    """gate, up and down of one layer of the 16-layer set: the dominant
+    Newton-Schulz shape class (4096 x 14336) at a few GB, the small case for
+    kernel profiling."""
+    ts = tuple(TensorSpec(nm, shp, "normal", 0.02) for nm, shp in LLAMA_LAYER if nm in ("gate", "up", "down"))
+    return Workload("llama_mlp_1layer", ts, steps=10, adamw=None, muon=MuonHP(weight_decay=0.0))
+
+
 WORKLOADS = {
     "tiny_mixed": tiny_mixed,
     "adamw_8m": adamw_8m,
     "muon_8m_skewed": muon_8m_skewed,
     "adamw_sweep_10k": adamw_sweep_10k,
     "llama16_mixed": llama16_mixed,
+    "llama_mlp_1layer": llama_mlp_1layer,
 }
 
 
