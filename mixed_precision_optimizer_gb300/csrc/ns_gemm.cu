@@ -316,44 +316,43 @@ __device__ __forceinline__ void epilogue_block(const GemmParams& P, const MuonGr
     warp_transpose(slab, lane, v, w);
     store_f16x32(P.Xt_out + static_cast<int64_t>(t.mat) * Ap * Bp + static_cast<int64_t>(col0 + lane) * Ap + row0, w);
   } else {
-    // last iteration: O = X' in the wide orientation (rows: A index, columns: B index)
+    // last iteration: O = X' in the wide orientation (rows: A index, columns: B index).
+    // The warp updates 32 runs of 32 consecutive W elements: for a tall W
+    // (stored as the transpose of the wide layout) run j is W[col0 + j][row0 ..
+    // row0 + 31] and lanes already hold rows; for a wide W run k is
+    // W[row0 + k][col0 .. col0 + 31] and lanes need columns (transpose first).
+    // All loads of W are issued before any store so their latencies overlap.
     const MuonMat& M = grp.mats[t.mat];
     const int64_t A = grp.A, B = grp.B, C = M.C;
+    int64_t first, n_runs;
+    bool lane_ok;
     if (M.transposed) {
-      // W[col][row]: for each column j the warp writes 32 consecutive row entries
-      if (row < A) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) w[j] = v[j];
+      first = static_cast<int64_t>(col0) * C + row;
+      n_runs = B - col0 < 32 ? B - col0 : 32;
+      lane_ok = row < A;
+    } else {
+      warp_transpose(slab, lane, v, w);
+      first = static_cast<int64_t>(row0) * C + col0 + lane;
+      n_runs = A - row0 < 32 ? A - row0 : 32;
+      lane_ok = col0 + lane < B;
+    }
+    if (lane_ok && n_runs > 0) {
+      if (P.ns_only) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (j < n_runs) M.O[first + j * C] = w[j];
+      } else {
+        float old[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) old[j] = (j < n_runs) ? M.W[first + j * C] : 0.f;
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
-          const int64_t col = col0 + j;
-          if (col < B) {
-            const int64_t i = col * C + row;
-            if (P.ns_only) {
-              M.O[i] = v[j];
-            } else {
-              const float wv = M.W[i] * P.decay - P.step_scale * v[j];
-              M.W[i] = wv;
-              if (M.Wb) M.Wb[i] = bf16_rne(wv);
-            }
-          }
-        }
-      }
-    } else {
-      // W[row][col]: transpose so that for each row k the warp writes 32 consecutive columns
-      warp_transpose(slab, lane, v, w);
-      const int64_t col = col0 + lane;
-      if (col < B) {
-#pragma unroll
-        for (int k = 0; k < 32; ++k) {
-          const int64_t r = row0 + k;
-          if (r < A) {
-            const int64_t i = r * C + col;
-            if (P.ns_only) {
-              M.O[i] = w[k];
-            } else {
-              const float wv = M.W[i] * P.decay - P.step_scale * w[k];
-              M.W[i] = wv;
-              if (M.Wb) M.Wb[i] = bf16_rne(wv);
-            }
+          if (j < n_runs) {
+            const float wv = old[j] * P.decay - P.step_scale * w[j];
+            M.W[first + j * C] = wv;
+            if (M.Wb) M.Wb[first + j * C] = bf16_rne(wv);
           }
         }
       }
