@@ -206,6 +206,32 @@ MPOPT_API opt_status opt_newton_schulz(const float* G, float* O, int64_t rows, i
                              void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * opt_newton_schulz without a workspace, for callers that cannot allocate
+ * device memory: code hosted by a runtime that owns every device allocation
+ * and gives extensions no allocator, or a path whose memory budget is fixed in
+ * advance.  No counterpart on the pages: this is an interface convenience, the
+ * arithmetic is exactly opt_newton_schulz's.
+ *   - Scratch is a 32 MiB array of device memory built into the library (a
+ *     static __device__ array).  Every GPU that loads the library holds it until
+ *     the process exits.  This entry point calls no cudaMalloc, cudaFree or
+ *     other allocating routine.
+ *   - Size limit: min(rows, cols) <= 1024 and max(rows, cols) <= 4096; larger
+ *     matrices return OPT_ERR_UNSUPPORTED (text in opt_last_cuda_error()).
+ *   - The first call on each device looks up the array's device address there
+ *     (cudaGetSymbolAddress with that device current); make that first call
+ *     before any stream capture.
+ *   - Every call on a device shares the one array, and the array keeps the last
+ *     call's contents (the status word is cleared at the start of each call).
+ *     Calls whose work overlaps on the GPU -- on different streams, or from
+ *     different threads -- race on it: serialise them on one stream.
+ *   - A device-side timeout is recorded in the array's header, which callers
+ *     cannot read; use opt_newton_schulz when that status is needed.
+ */
+MPOPT_API opt_status opt_newton_schulz_noalloc(const float* G, float* O, int64_t rows, int64_t cols,
+                                               int32_t ns_steps, float a, float b, float c, float eps,
+                                               void* stream);
+
+/*
  * Synchronises `stream` and reports whether a kernel of the last step on this
  * workspace recorded a device-side timeout (OPT_ERR_DEVICE_TIMEOUT) or not
  * (OPT_OK).  Returns OPT_ERR_CUDA if the synchronisation itself fails.

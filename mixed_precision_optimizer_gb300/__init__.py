@@ -69,7 +69,8 @@ class OptMuonHP(ctypes.Structure):
 _lib = None
 
 EXPORTED = ("opt_workspace_size", "opt_adamw_step", "opt_muon_step", "opt_mixed_step",
-            "opt_newton_schulz", "opt_device_status", "opt_profile_launches", "opt_strerror",
+            "opt_newton_schulz", "opt_newton_schulz_noalloc", "opt_device_status", "opt_profile_launches",
+            "opt_strerror",
             "opt_last_cuda_error", "opt_abi_version")
 
 KERNEL_NAMES = {0: "ns_gram", 1: "ns_poly", 2: "ns_bx", 3: "adamw", 4: "muon_momentum", 5: "muon_norm",
@@ -104,6 +105,8 @@ def lib():
     L.opt_mixed_step.restype = ctypes.c_int
     L.opt_newton_schulz.argtypes = [vp, vp, i64, i64, i32, f32, f32, f32, f32, vp, sz, vp]
     L.opt_newton_schulz.restype = ctypes.c_int
+    L.opt_newton_schulz_noalloc.argtypes = [vp, vp, i64, i64, i32, f32, f32, f32, f32, vp]
+    L.opt_newton_schulz_noalloc.restype = ctypes.c_int
     L.opt_device_status.argtypes = [vp, vp]
     L.opt_device_status.restype = ctypes.c_int
     L.opt_profile_launches.argtypes = [vp, ctypes.POINTER(OptLaunchInfo), i32, ctypes.POINTER(i32)]

@@ -6,6 +6,7 @@
 #include <cstdio>
 #include <cstring>
 #include <map>
+#include <mutex>
 #include <utility>
 #include <vector>
 
@@ -554,3 +555,109 @@ opt_status opt_profile_launches(void* const* events, opt_launch_info* info, int3
 int32_t opt_abi_version(void) { return (1 << 16) | 0; }
 
 }  // extern "C"
+
+// ------------------------------------------------- allocation-free variant --
+//
+// opt_newton_schulz_noalloc: Newton-Schulz for callers that cannot allocate
+// device memory and cannot hand the library a workspace -- for example code
+// hosted by a runtime that owns every device allocation and gives extensions
+// no allocator, or a path with a fixed memory budget where an allocation would
+// fail or stall.  Its scratch is the file-scope device array below, sized for
+// one matrix with min(rows, cols) <= 1024 and max(rows, cols) <= 4096 (padded
+// Newton-Schulz buffers of 1024 x 4096 plus the 256-byte status header, 32 MiB).
+// The array exists on every GPU that loads this library, from module load until
+// the process exits.  In host code its name is a host-side stand-in, not a
+// device address, so each device's address is taken once with
+// cudaGetSymbolAddress (with that device current) and only that address is
+// handed to kernels.
+
+namespace mpopt {
+namespace {
+
+constexpr int64_t kNoallocMaxMin = 1024;   // largest min(rows, cols)
+constexpr int64_t kNoallocMaxMax = 4096;   // largest max(rows, cols)
+
+constexpr size_t noalloc_align(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+// The same buffer layout as group_layout() for one kNoallocMaxMin x
+// kNoallocMaxMax matrix (both already multiples of the 256 padding), after the
+// status header.
+constexpr size_t kNoallocScratchBytes =
+    kHeaderBytes + 3 * noalloc_align(kNoallocMaxMin * kNoallocMaxMax * 2) +   // Xh, Xt x2
+    noalloc_align(kNoallocMaxMin * kNoallocMaxMin * 4) +                      // A fp32
+    2 * noalloc_align(kNoallocMaxMin * kNoallocMaxMin * 2) +                  // A fp16, C fp16
+    noalloc_align((kNoallocMaxMin * kNoallocMaxMax + kNormElemsPerBlock - 1) / kNormElemsPerBlock * 4) +
+    noalloc_align(4);
+
+}  // namespace
+
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoallocScratchBytes];
+
+namespace {
+
+constexpr int kNoallocMaxDevices = 64;
+std::mutex g_noalloc_mu;
+uint8_t* g_noalloc_base[kNoallocMaxDevices] = {};
+
+// Device address of the scratch array on the current device; the first call on
+// each device looks it up (once, under a lock).
+opt_status noalloc_scratch(uint8_t** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "noalloc: current device");
+  if (dev < 0 || dev >= kNoallocMaxDevices) return OPT_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_base[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "noalloc: scratch symbol address");
+    if (reinterpret_cast<uintptr_t>(p) & 255u) return OPT_ERR_WORKSPACE;
+    g_noalloc_base[dev] = static_cast<uint8_t*>(p);
+  }
+  *out = g_noalloc_base[dev];
+  return OPT_OK;
+}
+
+}  // namespace
+}  // namespace mpopt
+
+extern "C" opt_status opt_newton_schulz_noalloc(const float* G, float* O, int64_t rows, int64_t cols,
+                                                 int32_t ns_steps, float a, float b, float c, float eps,
+                                                 void* stream) {
+  using namespace mpopt;
+  if (rows < 0 || cols < 0 || ns_steps < 0 || ns_steps > 16) return OPT_ERR_INVALID_ARG;
+  if (!std::isfinite(a) || !std::isfinite(b) || !std::isfinite(c) || !std::isfinite(eps) || eps < 0.f)
+    return OPT_ERR_INVALID_ARG;
+  if (rows * cols == 0) return OPT_OK;
+  const int64_t mn = rows < cols ? rows : cols, mx = rows < cols ? cols : rows;
+  if (mn > kNoallocMaxMin || mx > kNoallocMaxMax) {
+    std::snprintf(g_last_cuda_error, sizeof(g_last_cuda_error),
+                  "opt_newton_schulz_noalloc: %lldx%lld exceeds the built-in scratch (min side <= %lld, "
+                  "max side <= %lld); use opt_newton_schulz with a workspace",
+                  static_cast<long long>(rows), static_cast<long long>(cols),
+                  static_cast<long long>(kNoallocMaxMin), static_cast<long long>(kNoallocMaxMax));
+    return OPT_ERR_UNSUPPORTED;
+  }
+  if (!G || !O) return OPT_ERR_INVALID_ARG;
+  if (check_fp32_ptr(G) != OPT_OK || check_fp32_ptr(O) != OPT_OK) return OPT_ERR_MISALIGNED;
+  opt_tensor t{};
+  t.main_param = O;
+  t.main_grad = G;
+  t.exp_avg = O;
+  t.rows = rows;
+  t.cols = cols;
+  t.ndim = 2;
+  t.kind = OPT_KIND_MUON;
+  std::vector<const opt_tensor*> one{&t};
+  const std::vector<ShapeClass> classes = shape_classes(one);
+  if (kHeaderBytes + group_bytes(1, rows, cols) > kNoallocScratchBytes) return OPT_ERR_WORKSPACE;
+  uint8_t* base = nullptr;
+  opt_status st = noalloc_scratch(&base);
+  if (st != OPT_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const cudaError_t e = cudaMemsetAsync(base, 0, kHeaderBytes, s);   // status word starts at zero
+  if (e != cudaSuccess) return cuda_fail(e, "noalloc: status header");
+  MuonPlanHp hp{0.f, 0.f, 0.f, eps, a, b, c, 0.f, 0, ns_steps, 1};
+  float* outs[1] = {O};
+  return run_muon_class(hp, classes[0], base + kHeaderBytes, kNoallocScratchBytes - kHeaderBytes,
+                        reinterpret_cast<uint32_t*>(base), s, outs);
+}
