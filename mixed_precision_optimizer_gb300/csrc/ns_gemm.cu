@@ -17,20 +17,25 @@
 // [-1.3, 1.3] before the first conversion) keep the rounding of C and X well
 // below the tolerance; both run at the same tensor-core rate as bf16.
 //
-// Kernel structure (one CTA per SM, persistent over output tiles):
-//   warp 0    TMA producer: 128-row A tile + 256-row B tile per k-block,
-//             128-byte swizzled, into a 4-stage shared-memory ring
-//   warp 1    TMEM allocator and MMA issuer: tcgen05.mma M=128 N=256, one
-//             elected thread, 4 MMAs per 128-byte k-block, commit to free the
-//             stage; a 2 x 256-column accumulator lets the epilogue of one
-//             tile overlap the main loop of the next
-//   warps 2-5 epilogue: tcgen05.ld 32 columns at a time, fused math, stores;
-//             each warp transposes 32 x 32 blocks through its own shared-memory
-//             slab for the transposed outputs
+// Kernel structure: CTA pairs (clusters of 2, one CTA per SM), persistent over
+// 256 x 256 output tiles, each pair computing a tile with cta_group::2 MMAs:
+//   warp 0    TMA producer in both CTAs: this CTA's 128 rows of A and 128 rows
+//             of B per k-block, 128-byte swizzled, into a 6-stage ring; both
+//             CTAs' copies complete on the even CTA's barrier
+//   warp 1    TMEM allocator (both CTAs) and, in the even CTA, the MMA issuer:
+//             tcgen05.mma.cta_group::2 M=256 N=256, 4 MMAs per 128-byte
+//             k-block, commits multicast to both CTAs to free the stage; a
+//             2 x 256-column accumulator per CTA lets the epilogue of one tile
+//             overlap the main loop of the next
+//   warps 2-5 epilogue in both CTAs: tcgen05.ld of this CTA's 128 rows, 32
+//             columns at a time, fused math, stores; each warp transposes
+//             32 x 32 blocks through its own shared-memory slab
+// Per MMA each SM stages 8 KB of operands (A and B halves) instead of the
+// 12 KB a single-CTA 128 x 256 tile needs.
 //
-// The Gram matrix and the polynomial are symmetric: only 128x256 tiles of
-// 256x256 blocks on or below the diagonal are computed, and off-diagonal
-// blocks are also stored transposed.
+// The Gram matrix and the polynomial are symmetric: only the 256x256 blocks
+// on or below the diagonal are computed, and off-diagonal blocks are also
+// stored transposed.
 //
 // Every wait on an mbarrier is bounded (about 2 s of %globaltimer).  A wait
 // that runs out records a status code in the workspace header, raises a CTA
@@ -47,13 +52,15 @@
 namespace mpopt {
 namespace {
 
-constexpr int BM = 128;
-constexpr int BN = 256;
-constexpr int kStages = 4;
+constexpr int BM = 128;                       // rows of the tile held by one CTA
+constexpr int BM_PAIR = 256;                  // rows of the tile of a CTA pair (MMA M)
+constexpr int BN = 256;                       // columns of the tile (MMA N)
+constexpr int BN_HALF = 128;                  // B rows staged by one CTA
+constexpr int kStages = 6;
 constexpr int kRowBytes = 128;                 // one swizzle row per k-block
-constexpr int kStageA = BM * kRowBytes;        // 16 KB
-constexpr int kStageB = BN * kRowBytes;        // 32 KB
-constexpr int kStageBytes = kStageA + kStageB;
+constexpr int kStageA = BM * kRowBytes;        // 16 KB: this CTA's 128 rows of A
+constexpr int kStageB = BN_HALF * kRowBytes;   // 16 KB: this CTA's 128 rows of B
+constexpr int kStageBytes = kStageA + kStageB; // per CTA; the pair's stage is twice this
 constexpr int kThreads = 192;
 constexpr int kTmemCols = 512;                 // 2 accumulators x 256 fp32 columns
 constexpr int kSlabWords = 32 * 33;            // per epilogue warp: 32 x 32 fp32, padded rows
@@ -66,7 +73,7 @@ struct GemmParams {
   int k_blocks;
   int tiles_per_mat;
   int total_tiles;
-  int tiles_m;          // bx: Ap / BM
+  int tiles_m;          // bx: Ap / BM_PAIR
   int count;
   int64_t Ap, Bp;
   float* Af;            // gram: out; poly: in (b A term)
@@ -93,10 +100,6 @@ __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
 __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
                : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
 __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
@@ -136,10 +139,12 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   }
 }
 
+// Tile load into this CTA's shared memory; completion is signalled on `bar`,
+// a shared::cluster address that may be the even CTA's barrier.
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x,
                                             int y, int z) {
   asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
       : "memory");
@@ -159,24 +164,60 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr) {
 
 // Instruction descriptor for kind::f16: fp32 accumulator (bits 4-5 = 1), A and
 // B fp16 (format 0 in bits 7-9 and 10-12), both K-major, N = 256 (bits 17-22,
-// N >> 3), M = 128 (bits 24-28, M >> 4).
+// N >> 3), M = 256 across the CTA pair (bits 24-28, M >> 4).
 __host__ __device__ constexpr uint32_t instr_desc() {
   return (1u << 4) | (0u << 7) | (0u << 10) | (static_cast<uint32_t>(BN >> 3) << 17) |
-         (static_cast<uint32_t>(BM >> 4) << 24);
+         (static_cast<uint32_t>(BM_PAIR >> 4) << 24);
 }
 
+// Pair MMA, issued by the even CTA: D[256 x 256] (+)= A[256 x 16] B[256 x 16]^T
+// with A's rows 0-127 / 128-255 and B's rows 0-127 / 128-255 in the shared
+// memory of the even / odd CTA at the descriptors' offsets; each CTA's TMEM
+// receives its own 128 rows of D.
 __device__ __forceinline__ void mma(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t accumulate) {
   constexpr uint32_t idesc = instr_desc();
   asm volatile(
       "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(tmem_d),
+      " tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(tmem_d),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+// Arrive on `bar` (same shared-memory offset) in both CTAs of the pair once all
+// previously issued MMAs of this thread have completed.
+__device__ __forceinline__ void mma_commit_pair(uint32_t bar) {
+  const uint16_t both = 3;
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+      "h"(both)
+      : "memory");
+}
+
+// Arrive on `bar` in this CTA only once all previously issued MMAs completed.
+__device__ __forceinline__ void mma_commit_local(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
                : "memory");
+}
+
+// The shared::cluster address of the variable at `addr` in CTA `rank` of the pair.
+__device__ __forceinline__ uint32_t peer_addr(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
 }
 
 __device__ __forceinline__ void tc_fence_before() {
@@ -209,18 +250,18 @@ struct Tile {
   bool mirror;   // symmetric modes: also store the transposed tile
 };
 
+// A tile is a 256 x 256 block (tm, tn) of the output, computed by one CTA pair.
 __device__ __forceinline__ Tile decode_tile(const GemmParams& P, int tile) {
   Tile t;
   t.mat = tile / P.tiles_per_mat;
   const int r = tile - t.mat * P.tiles_per_mat;
   if (P.mode == kGram || P.mode == kPoly) {
-    // r = 2 * pair + h, pair enumerates 256x256 blocks (I, J) with J <= I
-    const int pair = r >> 1, h = r & 1;
-    int I = static_cast<int>((sqrtf(8.f * static_cast<float>(pair) + 1.f) - 1.f) * 0.5f);
-    while ((I + 1) * (I + 2) / 2 <= pair) ++I;
-    while (I * (I + 1) / 2 > pair) --I;
-    const int J = pair - I * (I + 1) / 2;
-    t.tm = 2 * I + h;
+    // r enumerates the blocks (I, J) with J <= I of the symmetric output
+    int I = static_cast<int>((sqrtf(8.f * static_cast<float>(r) + 1.f) - 1.f) * 0.5f);
+    while ((I + 1) * (I + 2) / 2 <= r) ++I;
+    while (I * (I + 1) / 2 > r) --I;
+    const int J = r - I * (I + 1) / 2;
+    t.tm = I;
     t.tn = J;
     t.mirror = (I != J);
   } else {
@@ -362,25 +403,27 @@ __device__ __forceinline__ void epilogue_block(const GemmParams& P, const MuonGr
 
 // ------------------------------------------------------------------ kernel --
 
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 ns_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                const __grid_constant__ GemmParams P, const __grid_constant__ MuonGroup grp) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* stage_a = smem;                                  // kStages x 16 KB
-  uint8_t* stage_b = smem + kStages * kStageA;              // kStages x 32 KB
+  uint8_t* stage_b = smem + kStages * kStageA;              // kStages x 16 KB
   float* slabs = reinterpret_cast<float*>(smem + kStages * kStageBytes);   // 4 x 32 x 33 fp32
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes + kSlabBytes);
-  uint64_t* full = bars;                     // [kStages]
-  uint64_t* empty = bars + kStages;          // [kStages]
-  uint64_t* acc_full = bars + 2 * kStages;   // [2]
-  uint64_t* acc_empty = acc_full + 2;        // [2]
-  uint64_t* drain = acc_empty + 2;           // [1]
+  uint64_t* full = bars;                     // [kStages]  even CTA: both CTAs' copies landed
+  uint64_t* empty = bars + kStages;          // [kStages]  both CTAs: stage free again
+  uint64_t* acc_full = bars + 2 * kStages;   // [2]        both CTAs: accumulator ready
+  uint64_t* acc_empty = acc_full + 2;        // [2]        even CTA: both epilogues drained it
+  uint64_t* drain = acc_empty + 2;           // [1]        even CTA: all MMAs complete
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile uint32_t* abort_flag = tmem_slot + 1;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_rank();      // 0: even CTA (issues the MMAs), 1: odd CTA
+  const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -389,25 +432,24 @@ ns_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(smem_u32(&acc_full[a]), 1);
-      mbar_init(smem_u32(&acc_empty[a]), 128);
+      mbar_init(smem_u32(&acc_empty[a]), 2 * 128);
     }
     mbar_init(smem_u32(drain), 1);
     *abort_flag = 0u;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
   if (warp == 0 && lane == 0) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_a)) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_b)) : "memory");
   }
   if (warp == 1) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
                  "r"(kTmemCols)
                  : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
   }
   tc_fence_before();
-  __syncthreads();
+  cluster_sync();            // barriers of both CTAs initialised, TMEM allocated in both
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
@@ -416,48 +458,43 @@ ns_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------ TMA producer --
+      // Both CTAs load their own halves; completion is counted on the even
+      // CTA's full barrier, which expects both halves' bytes.
       uint32_t it = 0;
-      uint32_t issued_phase_mask = 0;   // stage s in flight with phase bit
-      uint32_t in_flight = 0;           // bit s: a copy into stage s may be outstanding
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < P.total_tiles; tile += gridDim.x) {
+      bool issued = false;
+      for (int tile = pair; ok && tile < P.total_tiles; tile += npairs) {
         const Tile t = decode_tile(P, tile);
-        const int arow = t.tm * BM, brow = t.tn * BN;
+        const int arow = t.tm * BM_PAIR + static_cast<int>(rank) * BM;
+        const int brow = t.tn * BN + static_cast<int>(rank) * BN_HALF;
         for (int kb = 0; kb < P.k_blocks; ++kb, ++it) {
           const uint32_t s = it % kStages, ph = (it / kStages) & 1u;
           if (!mbar_wait(smem_u32(&empty[s]), ph ^ 1u, abort_flag, P.status, kStatusTimeoutEmpty)) {
             ok = false;
             break;
           }
-          in_flight &= ~(1u << s);   // the consumer released it: the previous copy landed
-          const uint32_t fb = smem_u32(&full[s]);
-          mbar_expect_tx(fb, kStageBytes);
+          const uint32_t fb = peer_addr(smem_u32(&full[s]), 0);
+          if (rank == 0) mbar_expect_tx(smem_u32(&full[s]), 2 * kStageBytes);
           const int kx = kb * kElemsPerKBlock;
           tma_load_3d(smem_u32(stage_a + s * kStageA), &map_a, fb, kx, arow, t.mat);
           tma_load_3d(smem_u32(stage_b + s * kStageB), &map_b, fb, kx, brow, t.mat);
-          in_flight |= 1u << s;
-          issued_phase_mask = (issued_phase_mask & ~(1u << s)) | (ph << s);
+          issued = true;
         }
       }
-      if (!ok) {
-        // abort: let the copies already issued land before the CTA exits
-        for (uint32_t s = 0; s < kStages; ++s) {
-          if (in_flight & (1u << s)) {
-            const uint32_t ph = (issued_phase_mask >> s) & 1u;
-            const unsigned long long t0 = global_ns();
-            while (!mbar_try(smem_u32(&full[s]), ph) && global_ns() - t0 < kWaitLimitNs) {
-            }
-          }
+      if (!ok && issued) {
+        // abort: give copies already issued time to land before the CTA exits
+        const unsigned long long t0 = global_ns();
+        while (global_ns() - t0 < 10000000ull) {
         }
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      // ------------------------------------------------- MMA issuer --
+    if (lane == 0 && rank == 0) {
+      // ------------------------------------- MMA issuer (even CTA only) --
       uint32_t it = 0;
       int lt = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < P.total_tiles; tile += gridDim.x, ++lt) {
+      for (int tile = pair; ok && tile < P.total_tiles; tile += npairs, ++lt) {
         const uint32_t acc = lt & 1, acc_ph = (lt >> 1) & 1u;
         if (!mbar_wait(smem_u32(&acc_empty[acc]), acc_ph ^ 1u, abort_flag, P.status, kStatusTimeoutAccFree)) {
           ok = false;
@@ -476,16 +513,15 @@ ns_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
           const uint32_t b_addr = smem_u32(stage_b + s * kStageB);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {   // 4 MMAs of 32 bytes of K each
-            mma(d_tmem, smem_desc(a_addr + kk * 32), smem_desc(b_addr + kk * 32),
-                      (kb > 0 || kk > 0) ? 1u : 0u);
+            mma(d_tmem, smem_desc(a_addr + kk * 32), smem_desc(b_addr + kk * 32), (kb > 0 || kk > 0) ? 1u : 0u);
           }
-          mma_commit(smem_u32(&empty[s]));
+          mma_commit_pair(smem_u32(&empty[s]));
         }
         if (!ok) break;
-        mma_commit(smem_u32(&acc_full[acc]));
+        mma_commit_pair(smem_u32(&acc_full[acc]));
       }
       // drain: every MMA issued by this thread has completed before TMEM goes
-      mma_commit(smem_u32(drain));
+      mma_commit_local(smem_u32(drain));
       const unsigned long long t0 = global_ns();
       while (!mbar_try(smem_u32(drain), 0) && global_ns() - t0 < kWaitLimitNs) {
       }
@@ -494,13 +530,14 @@ ns_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
     // ------------------------------------------------------ epilogue --
     const int quarter = warp & 3;             // TMEM lanes this warp may access
     float* slab = slabs + (warp - 2) * kSlabWords;
+    const uint32_t empty_even = peer_addr(smem_u32(&acc_empty[0]), 0);
     int lt = 0;
-    for (int tile = blockIdx.x; tile < P.total_tiles; tile += gridDim.x, ++lt) {
+    for (int tile = pair; tile < P.total_tiles; tile += npairs, ++lt) {
       const uint32_t acc = lt & 1, acc_ph = (lt >> 1) & 1u;
       if (!mbar_wait(smem_u32(&acc_full[acc]), acc_ph, abort_flag, P.status, kStatusTimeoutAcc)) break;
       tc_fence_after();
       const Tile t = decode_tile(P, tile);
-      const int row0 = t.tm * BM + quarter * 32;
+      const int row0 = t.tm * BM_PAIR + static_cast<int>(rank) * BM + quarter * 32;
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * BN;
       for (int c0 = 0; c0 < BN; c0 += 32) {
         float v[32];
@@ -509,15 +546,16 @@ ns_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
         epilogue_block(P, grp, t, slab, lane, row0, t.tn * BN + c0, v);
       }
       tc_fence_before();
-      mbar_arrive(smem_u32(&acc_empty[acc]));
+      mbar_arrive_remote(empty_even + acc * static_cast<uint32_t>(sizeof(uint64_t)));
     }
   }
 
   tc_fence_before();
   __syncthreads();
+  cluster_sync();            // no CTA leaves while its partner may still signal it
   if (warp == 1) {
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(kTmemCols)
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(kTmemCols)
                  : "memory");
   }
 }
@@ -568,8 +606,9 @@ cudaError_t launch_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const Gemm
     if (e != cudaSuccess) return e;
     configured_dev = dev;
   }
-  const int grid = P.total_tiles < num_sms() ? P.total_tiles : num_sms();
-  ns_gemm_kernel<<<grid, kThreads, kSmemBytes, stream>>>(ma, mb, P, grp);
+  const int max_pairs = num_sms() / 2;
+  const int pairs = P.total_tiles < max_pairs ? P.total_tiles : max_pairs;
+  ns_gemm_kernel<<<2 * pairs, kThreads, kSmemBytes, stream>>>(ma, mb, P, grp);
   return cudaGetLastError();
 }
 
@@ -596,11 +635,11 @@ cudaError_t launch_ns_iteration(const MuonGroup& grp, const NsBuffers& buf, cons
   {
     CUtensorMap ma, mb;
     if ((e = make_map(&ma, buf.Xh, Bp, Ap, cnt, BM)) != cudaSuccess) return e;
-    if ((e = make_map(&mb, buf.Xh, Bp, Ap, cnt, BN)) != cudaSuccess) return e;
+    if ((e = make_map(&mb, buf.Xh, Bp, Ap, cnt, BN_HALF)) != cudaSuccess) return e;
     GemmParams P = base;
     P.mode = kGram;
     P.k_blocks = static_cast<int>(Bp / 64);
-    P.tiles_per_mat = T * (T + 1);
+    P.tiles_per_mat = T * (T + 1) / 2;
     P.total_tiles = P.tiles_per_mat * grp.count;
     P.Af = buf.Af;
     P.Ah = buf.Ah;
@@ -613,11 +652,11 @@ cudaError_t launch_ns_iteration(const MuonGroup& grp, const NsBuffers& buf, cons
   {
     CUtensorMap ma, mb;
     if ((e = make_map(&ma, buf.Ah, Ap, Ap, cnt, BM)) != cudaSuccess) return e;
-    if ((e = make_map(&mb, buf.Ah, Ap, Ap, cnt, BN)) != cudaSuccess) return e;
+    if ((e = make_map(&mb, buf.Ah, Ap, Ap, cnt, BN_HALF)) != cudaSuccess) return e;
     GemmParams P = base;
     P.mode = kPoly;
     P.k_blocks = static_cast<int>(Ap / 64);
-    P.tiles_per_mat = T * (T + 1);
+    P.tiles_per_mat = T * (T + 1) / 2;
     P.total_tiles = P.tiles_per_mat * grp.count;
     P.Af = buf.Af;
     P.Ch = buf.Ch;
@@ -630,12 +669,12 @@ cudaError_t launch_ns_iteration(const MuonGroup& grp, const NsBuffers& buf, cons
   {
     CUtensorMap ma, mb;
     if ((e = make_map(&ma, buf.Ch, Ap, Ap, cnt, BM)) != cudaSuccess) return e;
-    if ((e = make_map(&mb, buf.Xt[it & 1], Ap, Bp, cnt, BN)) != cudaSuccess) return e;
+    if ((e = make_map(&mb, buf.Xt[it & 1], Ap, Bp, cnt, BN_HALF)) != cudaSuccess) return e;
     GemmParams P = base;
     P.mode = (it == s.ns_steps - 1) ? kBxFinal : kBx;
     P.k_blocks = static_cast<int>(Ap / 64);
-    P.tiles_m = static_cast<int>(Ap / BM);
-    P.tiles_per_mat = static_cast<int>((Ap / BM) * (Bp / BN));
+    P.tiles_m = static_cast<int>(Ap / BM_PAIR);
+    P.tiles_per_mat = static_cast<int>((Ap / BM_PAIR) * (Bp / BN));
     P.total_tiles = P.tiles_per_mat * grp.count;
     P.Xh = buf.Xh;
     P.Xt_out = buf.Xt[(it + 1) & 1];
