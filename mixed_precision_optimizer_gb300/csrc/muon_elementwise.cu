@@ -116,10 +116,13 @@ __global__ void muon_norm_kernel(NsBuffers buf, int64_t blocks_per_mat, float ep
 
 // grid: (operand tiles per matrix, matrices); one 64 x 64 tile of the padded
 // W-layout space per block.  Writes the fp16 operand in W layout directly and
-// in the other layout through a shared-memory transpose.
+// in the other layout through a shared-memory transpose.  Each thread moves 4
+// consecutive elements per step: a 16-byte load of g and of m (when the rows
+// are 16-byte aligned, else four scalar loads) and an 8-byte store of 4 fp16
+// on both sides.
 __global__ void __launch_bounds__(kThreads)
 muon_operand_kernel(const MuonGroup grp, NsBuffers buf, MuonScalars s) {
-  __shared__ uint16_t tile[kPrepTile][kPrepTile + 2];
+  __shared__ uint16_t tile[kPrepTile][kPrepTile + 2];   // odd word stride: few bank conflicts
   const int mat = blockIdx.y;
   const MuonMat& M = grp.mats[mat];
   const int64_t Ap = grp.Ap, Bp = grp.Bp;
@@ -130,33 +133,54 @@ muon_operand_kernel(const MuonGroup grp, NsBuffers buf, MuonScalars s) {
   const int64_t r0 = ty * kPrepTile, c0 = tx * kPrepTile;
   const int R = M.R, C = M.C;
   const float inv = buf.inv_norm[mat];
-  const int lc = threadIdx.x % kPrepTile;
-  const int lr0 = threadIdx.x / kPrepTile;
+  const int lc = (threadIdx.x % 16) * 4;       // first of 4 columns
+  const int lr0 = threadIdx.x / 16;            // 0..15
+  const bool vec = M.vec4 && (C % 4 == 0);     // every row start 16-byte aligned
   uint16_t* Xh = buf.Xh + static_cast<int64_t>(mat) * Ap * Bp;   // [Ap][Bp]
   uint16_t* Xt = buf.Xt[0] + static_cast<int64_t>(mat) * Ap * Bp; // [Bp][Ap]
-#pragma unroll 4
-  for (int k = 0; k < kPrepTile / 4; ++k) {
-    const int lr = lr0 + 4 * k;
+  uint16_t* direct = tr ? Xt : Xh;             // the operand stored in W layout
+  const int64_t direct_ld = tr ? Ap : Bp;
+  uint16_t* other = tr ? Xh : Xt;              // the operand stored transposed
+  const int64_t other_ld = tr ? Bp : Ap;
+#pragma unroll
+  for (int k = 0; k < kPrepTile / 16; ++k) {
+    const int lr = lr0 + 16 * k;
     const int64_t r = r0 + lr, c = c0 + lc;
-    float val = 0.f;
-    if (r < R && c < C) {
+    float val[4] = {0.f, 0.f, 0.f, 0.f};
+    if (r < R) {
       const int64_t i = r * C + c;
-      val = gtilde(s, M.g[i], s.ns_only ? 0.f : M.m[i]) * inv;
+      if (vec && c + 3 < C) {
+        const float4 g = *reinterpret_cast<const float4*>(M.g + i);
+        float4 m = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (!s.ns_only) m = *reinterpret_cast<const float4*>(M.m + i);
+        val[0] = gtilde(s, g.x, m.x) * inv;
+        val[1] = gtilde(s, g.y, m.y) * inv;
+        val[2] = gtilde(s, g.z, m.z) * inv;
+        val[3] = gtilde(s, g.w, m.w) * inv;
+      } else {
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          if (c + q < C) val[q] = gtilde(s, M.g[i + q], s.ns_only ? 0.f : M.m[i + q]) * inv;
+      }
     }
-    const uint16_t h = f16_bits(val);
-    tile[lr][lc] = h;
-    if (!tr) Xh[r * Bp + c] = h;     // W layout is the wide layout
-    else     Xt[r * Ap + c] = h;     // W layout is the transposed wide layout
+    const uint16_t h0 = f16_bits(val[0]), h1 = f16_bits(val[1]), h2 = f16_bits(val[2]), h3 = f16_bits(val[3]);
+    tile[lr][lc + 0] = h0;
+    tile[lr][lc + 1] = h1;
+    tile[lr][lc + 2] = h2;
+    tile[lr][lc + 3] = h3;
+    const uint2 packed = make_uint2(static_cast<uint32_t>(h0) | (static_cast<uint32_t>(h1) << 16),
+                                    static_cast<uint32_t>(h2) | (static_cast<uint32_t>(h3) << 16));
+    *reinterpret_cast<uint2*>(direct + r * direct_ld + c) = packed;
   }
   __syncthreads();
-#pragma unroll 4
-  for (int k = 0; k < kPrepTile / 4; ++k) {
-    const int i = lr0 + 4 * k;       // output row within tile (= W column)
-    const int j = lc;                // output column within tile (= W row)
-    const uint16_t h = tile[j][i];
-    const int64_t orow = c0 + i, ocol = r0 + j;
-    if (!tr) Xt[orow * Ap + ocol] = h;
-    else     Xh[orow * Bp + ocol] = h;
+  // transposed side: output row i (= W column c0 + i) gets W rows r0 .. r0 + 63
+#pragma unroll
+  for (int k = 0; k < kPrepTile / 16; ++k) {
+    const int i = lr0 + 16 * k;
+    const int j = lc;
+    const uint2 packed = make_uint2(static_cast<uint32_t>(tile[j][i]) | (static_cast<uint32_t>(tile[j + 1][i]) << 16),
+                                    static_cast<uint32_t>(tile[j + 2][i]) | (static_cast<uint32_t>(tile[j + 3][i]) << 16));
+    *reinterpret_cast<uint2*>(other + (c0 + i) * other_ld + r0 + j) = packed;
   }
 }
 
