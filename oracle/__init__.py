@@ -21,9 +21,13 @@ the pages by eye.
   Sources: "02 · Optimizer：算法与 infra" §1, §5.1, §5.2, §5.4, §14.1;
   "优化器：AdamW、Muon 与分布式优化器", section "Muon：把更新“正交化”".
 
+* ``clip``   -- global gradient-norm clipping, fp64.
+  Source: "02 · Optimizer：算法与 infra" §11.1 (definition) and §11.4 (one
+  global norm shared by the Muon and AdamW groups).
+
 Every function is pinned by a CPU test in ``tests/test_oracle_pins.py``
 against values the pages print, closed forms, or library routines.  No
 function here is "parity unpinned".
 """
 
-from . import adamw, muon  # noqa: F401
+from . import adamw, clip, muon  # noqa: F401

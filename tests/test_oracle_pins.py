@@ -308,3 +308,55 @@ def test_muon_step_composes():
 
 def test_oracle_header_says_test_infrastructure():
     assert "TEST INFRASTRUCTURE ONLY" in oracle.__doc__
+
+
+# ------------------------------------------------------------- clipping ----
+
+from oracle import clip as OC  # noqa: E402
+
+
+def _clip_pin_failures(total_norm, clip_scale):
+    """Pins of the clipping definition ("02 · Optimizer：算法与 infra" §11.1):
+    a 3-4-5 triangle, a norm below the threshold, a disabled clip, and the
+    post-clip norm landing on max_norm up to the 1e-6 guard."""
+    fails = []
+    g = [np.array([3.0]), np.array([[4.0]])]           # two tensors: the norm is global
+    if abs(total_norm(g) - 5.0) > 1e-15:
+        fails.append("3-4-5 norm")
+    if abs(clip_scale(g, 1.0) - 1.0 / (5.0 + 1e-6)) > 1e-15:
+        fails.append("coefficient")
+    if clip_scale(g, 10.0) != 1.0:
+        fails.append("below threshold must not scale")
+    if clip_scale(g, 0.0) != 1.0 or clip_scale(g, -1.0) != 1.0:
+        fails.append("max_norm <= 0 disables")
+    rng = np.random.default_rng(0)
+    gs = [rng.standard_normal(s) for s in ((7,), (3, 5), (11, 2))]
+    s = clip_scale(gs, 0.5)
+    clipped = total_norm([x * s for x in gs])
+    if not (0.5 - 1e-5 < clipped <= 0.5):
+        fails.append(f"post-clip norm {clipped}")
+    # the coefficient is the same for every tensor (global, not per-tensor)
+    per = [clip_scale([x], 0.5) for x in gs]
+    if all(abs(p - s) < 1e-12 for p in per):
+        fails.append("per-tensor norm")
+    return fails
+
+
+def test_clip_pins():
+    assert _clip_pin_failures(OC.total_norm, OC.clip_scale) == []
+
+
+@pytest.mark.parametrize("kind", ["no_sqrt", "per_tensor", "always_scale", "eps_missing_sign"])
+def test_clip_pins_catch_planted_mistakes(kind):
+    def tn(grads):
+        s = sum(float(np.sum(np.asarray(g, np.float64) ** 2)) for g in grads)
+        return s if kind == "no_sqrt" else float(np.sqrt(s))
+
+    def cs(grads, max_norm):
+        if max_norm <= 0:
+            return 1.0
+        if kind == "per_tensor":
+            return max_norm / (tn(grads[:1]) + 1e-6)
+        coeff = max_norm / (tn(grads) + (-1e-6 if kind == "eps_missing_sign" else 1e-6))
+        return coeff if (coeff < 1.0 or kind == "always_scale") else 1.0
+    assert _clip_pin_failures(tn, cs) != []
