@@ -52,6 +52,8 @@ def parse():
     ap.add_argument("--workload", default="llama16_mixed", choices=sorted(S.WORKLOADS))
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--clip", type=float, default=0.0,
+                    help="max_norm of global grad-norm clipping fused into the step (0: off)")
     return ap.parse_args()
 
 
@@ -327,12 +329,19 @@ def run_ours(args, dist: Dist):
     w = S.WORKLOADS[args.workload]()
     params, n_muon, n_adamw = build_device_workload(w, device)
     total = n_muon + n_adamw
-    ws = mp.alloc_workspace(mp.workspace_size(params), device)
+    ws = mp.alloc_workspace(mp.workspace_size(params, clip=args.clip > 0), device)
     hm, ha = hyper(w)
+
+    def step(t):
+        if args.clip > 0:
+            mp.mixed_step_clipped(params, hm, ha(t), args.clip, ws)
+        else:
+            mp.mixed_step(params, hm, ha(t), ws)
+
     stream = torch.cuda.current_stream()
     t = 1
     for _ in range(args.warmup):
-        mp.mixed_step(params, hm, ha(t), ws)
+        step(t)
         t += 1
     torch.cuda.synchronize()
     if mp.device_status(ws) != mp.OPT_OK:
@@ -347,7 +356,7 @@ def run_ours(args, dist: Dist):
         start.record(stream)
         with prof:
             for _ in range(args.steps):
-                mp.mixed_step(params, hm, ha(t), ws)
+                step(t)
                 t += 1
         end.record(stream)
         torch.cuda.synchronize()
@@ -416,7 +425,7 @@ def run_ours(args, dist: Dist):
         roofline_adamw = None
 
     # ---- end to end through the public API with host buffers
-    e2e = run_e2e(args, params, hm, ha, t, ws, total, dist)
+    e2e = run_e2e(args, step, params, t, total, dist)
     t += args.e2e_steps
 
     value = total * args.steps * dist.world / (elapsed_ms * 1e-3)
@@ -426,7 +435,7 @@ def run_ours(args, dist: Dist):
         "warmup": args.warmup, "ms_per_step": round(elapsed_ms / args.steps, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32 (master, state, AdamW); Newton-Schulz fp16 x fp16 -> f32 on tensor cores",
         "data": "synthetic (seeded, drawn on the GPU)",
-        "config": {"workload": w.name, "params": total, "muon_params": n_muon, "adamw_params": n_adamw,
+        "config": {"workload": w.name, "params": total, "grad_clip_max_norm": args.clip if args.clip > 0 else None, "muon_params": n_muon, "adamw_params": n_adamw,
                    "tensors": len(w.tensors), "parallelism": f"replicas x{dist.world}" if dist.world > 1 else "1 GPU",
                    "l2": "inputs larger than L2 (all state resident, ~18 B/param touched per step)"
                    if total * 14 > 4 * 129e6 else "L2 not flushed: workload smaller than L2",
@@ -446,7 +455,26 @@ def run_ours(args, dist: Dist):
     return line
 
 
-def run_e2e(args, params, hm, ha, t, ws, total, dist: Dist):
+def pinned_host_buffers(shapes_dtypes):
+    """Page-locked host buffers, one per tensor: numpy memory registered with
+    cudaHostRegister (return code checked), else torch's pinned allocator."""
+    import numpy as np
+    import torch
+    cudart = torch.cuda.cudart()
+    out, registered = [], []
+    for n, npdt, tdt in shapes_dtypes:
+        a = np.empty(n, dtype=npdt)
+        rc = cudart.cudaHostRegister(a.ctypes.data, a.nbytes, 0)
+        if int(rc) == 0:
+            t = torch.from_numpy(a)
+            registered.append(a)
+            out.append(t.view(tdt) if tdt != t.dtype else t)
+        else:
+            out.append(torch.empty(n, dtype=tdt, pin_memory=True))
+    return out, registered
+
+
+def run_e2e(args, step, params, t, total, dist: Dist):
     """The same step through the public API, with main_grad arriving from
     pinned host memory and the bf16 model parameters read back to host
     memory inside the timed region."""
@@ -455,20 +483,12 @@ def run_e2e(args, params, hm, ha, t, ws, total, dist: Dist):
     import mixed_precision_optimizer_gb300 as mp
     if args.e2e_steps <= 0:
         return None
-    cudart = torch.cuda.cudart()
-    g_host = np.empty(total, dtype=np.float32)
-    b_host = np.empty(total, dtype=np.uint16)
-    for arr in (g_host, b_host):
-        cudart.cudaHostRegister(arr.ctypes.data, arr.nbytes, 0)
-    g_t = torch.from_numpy(g_host)
-    b_t = torch.from_numpy(b_host).view(torch.bfloat16)
-    off = 0
-    slices = []
-    for p in params:
-        n = p.main_param.numel()
-        g_t[off:off + n].copy_(p.main_grad.reshape(-1))
-        slices.append((off, n))
-        off += n
+    g_host, reg_g = pinned_host_buffers([(p.main_param.numel(), np.float32, torch.float32) for p in params])
+    b_host, reg_b = pinned_host_buffers([(p.main_param.numel(), np.int16, torch.bfloat16) for p in params])
+    for p, gh in zip(params, g_host):
+        gh.copy_(p.main_grad.reshape(-1))
+    if not all(x.is_pinned() for x in g_host + b_host):
+        raise SystemExit("e2e: host buffers are not page-locked")
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -476,20 +496,23 @@ def run_e2e(args, params, hm, ha, t, ws, total, dist: Dist):
     torch.cuda.synchronize()
     start.record(stream)
     for _ in range(args.e2e_steps):
-        for p, (o, n) in zip(params, slices):
-            p.main_grad.reshape(-1).copy_(g_t[o:o + n], non_blocking=True)
-        mp.mixed_step(params, hm, ha(t), ws)
+        for p, gh in zip(params, g_host):
+            p.main_grad.reshape(-1).copy_(gh, non_blocking=True)
+        step(t)
         t += 1
-        for p, (o, n) in zip(params, slices):
-            b_t[o:o + n].copy_(p.model.reshape(-1), non_blocking=True)
+        for p, bh in zip(params, b_host):
+            bh.copy_(p.model.reshape(-1), non_blocking=True)
     end.record(stream)
     torch.cuda.synchronize()
     dist.barrier()
     ms = dist.max(start.elapsed_time(end))
-    for arr in (g_host, b_host):
-        cudart.cudaHostUnregister(arr.ctypes.data)
+    cudart = torch.cuda.cudart()
+    for a in reg_g + reg_b:
+        cudart.cudaHostUnregister(a.ctypes.data)
+    h2d = sum(x.numel() * x.element_size() for x in g_host)
+    d2h = sum(x.numel() * x.element_size() for x in b_host)
     return {"value": round(total * args.e2e_steps * dist.world / (ms * 1e-3), 1), "unit": UNIT,
-            "h2d_bytes_per_step": int(g_host.nbytes), "d2h_bytes_per_step": int(b_host.nbytes),
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
             "steps": args.e2e_steps, "ms_per_step": round(ms / args.e2e_steps, 3)}
 
 
@@ -510,7 +533,7 @@ def run_reference(args, dist: Dist):
             "warmup": args.warmup, "ms_per_step": round(t_step * 1e3, 1), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32 AdamW / f64 Newton-Schulz (CPU oracle)",
             "data": "synthetic (seeded)", "impl": "reference",
-            "config": {"workload": w.name, "params": total, "parallelism": "CPU oracle on rank 0"},
+            "config": {"workload": w.name, "params": total, "grad_clip_max_norm": args.clip if args.clip > 0 else None, "parallelism": "CPU oracle on rank 0"},
             "cpu_baseline": {"value": round(value, 1), "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
                              "sample": sample + " (per step; step time extrapolated from the sample)"},
             "e2e": {"value": round(value, 1), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}

@@ -76,6 +76,10 @@ enum {
 /* opt_tensor.flags */
 enum { OPT_FLAG_EMBEDDING_OR_OUTPUT = 1 };
 
+/* OR into opt_workspace_size's `routing` to size a workspace for
+   opt_mixed_step_clipped (adds one float per 16K gradient elements). */
+enum { OPT_WORKSPACE_CLIP = 0x10 };
+
 /*
  * AdamW hyper-parameters for one step ("02 · Optimizer：算法与 infra" §2, §3).
  *   lr            eta, the step size
@@ -196,6 +200,25 @@ MPOPT_API opt_status opt_mixed_step(const opt_muon_hp* hp_muon, const opt_adamw_
                           void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * opt_mixed_step with global gradient-norm clipping fused in front
+ * ("02 · Optimizer：算法与 infra" §11.1; §11.4: one norm over the gradients of
+ * both optimizer groups):
+ *   total_norm = sqrt(sum over every tensor of ||main_grad||^2)
+ *   clip_coeff = max_norm / (total_norm + 1e-6)
+ *   every gradient is multiplied by clip_coeff when clip_coeff < 1.
+ * The factor is computed on the device (fp32 sums of squares per 16K-element
+ * chunk, added in double in a fixed order) and applied by the AdamW and Muon
+ * kernels as they load each gradient; main_grad itself is not rewritten.
+ * max_norm <= 0 disables clipping (no norm pass, outputs untouched).
+ * total_norm_out and clip_scale_out are optional 4-byte-aligned DEVICE fp32
+ * pointers receiving the norm and the factor applied.  Workspace:
+ * opt_workspace_size(tensors, n, OPT_KIND_AUTO | OPT_WORKSPACE_CLIP).
+ */
+MPOPT_API opt_status opt_mixed_step_clipped(const opt_muon_hp* hp_muon, const opt_adamw_hp* hp_adamw, float max_norm,
+                                            float* total_norm_out, float* clip_scale_out, const opt_tensor* tensors,
+                                            int32_t n, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Newton-Schulz orthogonalisation alone ("02 · Optimizer：算法与 infra" §5.2):
  * O = NS_steps(G) for one fp32 rows x cols matrix G, same fp16 tensor-core
  * path as opt_muon_step.  G and O are device fp32 [rows*cols]; O may alias G.
@@ -265,7 +288,9 @@ enum {
   OPT_KERNEL_MUON_PREP = 4,    /* momentum, Nesterov, norm partials              */
   OPT_KERNEL_MUON_NORM = 5,
   OPT_KERNEL_MUON_APPLY = 6,   /* ns_steps == 0 only                             */
-  OPT_KERNEL_MUON_OPERANDS = 7 /* normalised fp16 operand copies of X0 and X0^T  */
+  OPT_KERNEL_MUON_OPERANDS = 7, /* normalised fp16 operand copies of X0 and X0^T */
+  OPT_KERNEL_GRAD_NORM = 8,     /* clipping: sums of squares of the gradients      */
+  OPT_KERNEL_CLIP_FINALIZE = 9  /* clipping: total norm and factor                 */
 };
 
 MPOPT_API opt_status opt_profile_launches(void* const* events, opt_launch_info* info, int32_t capacity,

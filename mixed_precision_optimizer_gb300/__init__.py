@@ -68,13 +68,14 @@ class OptMuonHP(ctypes.Structure):
 
 _lib = None
 
-EXPORTED = ("opt_workspace_size", "opt_adamw_step", "opt_muon_step", "opt_mixed_step",
+EXPORTED = ("opt_workspace_size", "opt_adamw_step", "opt_muon_step", "opt_mixed_step", "opt_mixed_step_clipped",
             "opt_newton_schulz", "opt_newton_schulz_noalloc", "opt_device_status", "opt_profile_launches",
             "opt_strerror",
             "opt_last_cuda_error", "opt_abi_version")
 
 KERNEL_NAMES = {0: "ns_gram", 1: "ns_poly", 2: "ns_bx", 3: "adamw", 4: "muon_momentum", 5: "muon_norm",
-                6: "muon_apply", 7: "muon_operands"}
+                6: "muon_apply", 7: "muon_operands", 8: "grad_norm", 9: "clip_finalize"}
+WORKSPACE_CLIP = 0x10
 
 
 class OptLaunchInfo(ctypes.Structure):
@@ -103,6 +104,9 @@ def lib():
     L.opt_muon_step.restype = ctypes.c_int
     L.opt_mixed_step.argtypes = [ctypes.POINTER(OptMuonHP), ctypes.POINTER(OptAdamwHP), T, i32, vp, sz, vp]
     L.opt_mixed_step.restype = ctypes.c_int
+    L.opt_mixed_step_clipped.argtypes = [ctypes.POINTER(OptMuonHP), ctypes.POINTER(OptAdamwHP), f32, vp, vp, T, i32,
+                                         vp, sz, vp]
+    L.opt_mixed_step_clipped.restype = ctypes.c_int
     L.opt_newton_schulz.argtypes = [vp, vp, i64, i64, i32, f32, f32, f32, f32, vp, sz, vp]
     L.opt_newton_schulz.restype = ctypes.c_int
     L.opt_newton_schulz_noalloc.argtypes = [vp, vp, i64, i64, i32, f32, f32, f32, f32, vp]
@@ -210,10 +214,10 @@ def muon_hp(lr=0.02, momentum=0.95, weight_decay=0.0, eps=1e-7, nesterov=True, n
     return OptMuonHP(lr, momentum, weight_decay, eps, 1 if nesterov else 0, int(ns_steps), a, b, c, scale_coeff)
 
 
-def workspace_size(params: Sequence[Param], routing="auto") -> int:
+def workspace_size(params: Sequence[Param], routing="auto", clip=False) -> int:
     r = {"auto": KIND_AUTO, "adamw": KIND_ADAMW, "muon": KIND_MUON}[routing]
     arr = _array(params)
-    return int(lib().opt_workspace_size(arr, len(params), r))
+    return int(lib().opt_workspace_size(arr, len(params), r | (WORKSPACE_CLIP if clip else 0)))
 
 
 def alloc_workspace(nbytes, device=None):
@@ -249,6 +253,21 @@ def mixed_step(params: Sequence[Param], hp_muon: Optional[OptMuonHP], hp_adamw: 
     _check(lib().opt_mixed_step(ctypes.byref(hp_muon) if hp_muon is not None else None,
                                 ctypes.byref(hp_adamw) if hp_adamw is not None else None,
                                 arr, len(params), w, nb, _stream(stream)), "opt_mixed_step")
+
+
+def mixed_step_clipped(params: Sequence[Param], hp_muon: Optional[OptMuonHP], hp_adamw: Optional[OptAdamwHP],
+                       max_norm: float, workspace, total_norm_out=None, clip_scale_out=None, stream=None):
+    """mixed_step with global gradient-norm clipping; the optional outputs are
+    1-element fp32 CUDA tensors receiving the norm and the factor applied."""
+    import torch
+    arr = _array(params)
+    w, nb = _ws(workspace)
+    tn = _ptr(total_norm_out, torch.float32, "total_norm_out", 1) if total_norm_out is not None else None
+    cs = _ptr(clip_scale_out, torch.float32, "clip_scale_out", 1) if clip_scale_out is not None else None
+    _check(lib().opt_mixed_step_clipped(ctypes.byref(hp_muon) if hp_muon is not None else None,
+                                        ctypes.byref(hp_adamw) if hp_adamw is not None else None,
+                                        float(max_norm), tn, cs, arr, len(params), w, nb, _stream(stream)),
+           "opt_mixed_step_clipped")
 
 
 def newton_schulz(G, out, steps=5, coeffs=NS_COEFFS, eps=1e-7, workspace=None, stream=None):

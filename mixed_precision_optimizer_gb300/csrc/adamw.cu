@@ -6,6 +6,7 @@
 // bf16 writeback of §9.2.  Per element, in fp32, every operation rounded to
 // nearest and no contraction into FMA (the __f*_rn intrinsics):
 //
+//   g = main_grad * clip_scale         (clip_scale = 1 without clipping)
 //   m = beta1*m + (1-beta1)*g          v = beta2*v + (1-beta2)*(g*g)
 //   mhat = m / (1-beta1^t)             vhat = v / (1-beta2^t)
 //   p = p*(1 - lr*lambda) - lr * (mhat / (sqrt(vhat) + eps))
@@ -74,10 +75,10 @@ __device__ __forceinline__ int find_tensor(const AdamwTensorDesc* t, int n, int6
 }
 
 __device__ __forceinline__ void scalar_range(const AdamwTensorDesc& d, int64_t begin, int64_t end,
-                                             const AdamwScalars& s) {
+                                             const AdamwScalars& s, float gs) {
   for (int64_t i = begin + threadIdx.x; i < end; i += blockDim.x) {
     float p = d.p[i], m = d.m[i], v = d.v[i];
-    adamw_elem(p, d.g[i], m, v, s);
+    adamw_elem(p, __fmul_rn(d.g[i], gs), m, v, s);
     d.p[i] = p;
     d.m[i] = m;
     d.v[i] = v;
@@ -88,24 +89,28 @@ __device__ __forceinline__ void scalar_range(const AdamwTensorDesc& d, int64_t b
 __global__ void __launch_bounds__(kAdamwThreads, 4)
 adamw_mta_kernel(const __grid_constant__ AdamwBatch batch) {
   const AdamwScalars& s = batch.s;
+  // clipping factor (exactly 1 without clipping, so g * gs == g)
+  const float gs = s.grad_scale ? *s.grad_scale : 1.f;
   for (int64_t chunk = blockIdx.x; chunk < batch.total_chunks; chunk += gridDim.x) {
     const int ti = find_tensor(batch.t, batch.n, chunk);
     const AdamwTensorDesc d = batch.t[ti];
     const int64_t c = chunk - d.chunk_begin;
     if (d.head < 0) {          // pointers cannot be co-aligned: element at a time
       const int64_t b = c * kAdamwChunk;
-      scalar_range(d, b, min(b + kAdamwChunk, d.numel), s);
+      scalar_range(d, b, min(b + kAdamwChunk, d.numel), s, gs);
       continue;
     }
     const int64_t head = d.head;
     const int64_t begin = head + c * kAdamwChunk;
     const int64_t end = min(begin + kAdamwChunk, d.numel);
-    if (c == 0) scalar_range(d, 0, head, s);
+    if (c == 0) scalar_range(d, 0, head, s, gs);
     const int64_t ngroups = (end > begin) ? (end - begin) / 8 : 0;
     for (int64_t j = threadIdx.x; j < ngroups; j += blockDim.x) {
       const int64_t e = begin + 8 * j;
       float4 p0 = ld_v4(d.p + e), p1 = ld_v4(d.p + e + 4);
-      const float4 g0 = ld_stream(d.g + e), g1 = ld_stream(d.g + e + 4);
+      float4 g0 = ld_stream(d.g + e), g1 = ld_stream(d.g + e + 4);
+      g0.x = __fmul_rn(g0.x, gs); g0.y = __fmul_rn(g0.y, gs); g0.z = __fmul_rn(g0.z, gs); g0.w = __fmul_rn(g0.w, gs);
+      g1.x = __fmul_rn(g1.x, gs); g1.y = __fmul_rn(g1.y, gs); g1.z = __fmul_rn(g1.z, gs); g1.w = __fmul_rn(g1.w, gs);
       float4 m0 = ld_v4(d.m + e), m1 = ld_v4(d.m + e + 4);
       float4 v0 = ld_v4(d.v + e), v1 = ld_v4(d.v + e + 4);
       adamw_elem(p0.x, g0.x, m0.x, v0.x, s);
@@ -132,7 +137,7 @@ adamw_mta_kernel(const __grid_constant__ AdamwBatch batch) {
       }
     }
     // ragged tail of the tensor (only the last chunk has one)
-    if (end == d.numel) scalar_range(d, begin + 8 * ngroups, end, s);
+    if (end == d.numel) scalar_range(d, begin + 8 * ngroups, end, s, gs);
   }
 }
 

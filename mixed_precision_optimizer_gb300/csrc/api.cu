@@ -169,7 +169,7 @@ AdamwTensorDesc describe(const opt_tensor& t, int64_t chunk_begin, int64_t& chun
 AdamwScalars adamw_scalars(const opt_adamw_hp* hp) {
   // per-step scalars: double from the float hyper-parameters, rounded once
   const double lr = hp->lr, b1 = hp->beta1, b2 = hp->beta2, wd = hp->weight_decay;
-  AdamwScalars s;
+  AdamwScalars s{};
   s.lr = hp->lr;
   s.beta1 = hp->beta1;
   s.beta2 = hp->beta2;
@@ -182,9 +182,11 @@ AdamwScalars adamw_scalars(const opt_adamw_hp* hp) {
   return s;
 }
 
-opt_status run_adamw(const opt_adamw_hp* hp, const std::vector<const opt_tensor*>& ts, cudaStream_t stream) {
+opt_status run_adamw(const opt_adamw_hp* hp, const std::vector<const opt_tensor*>& ts, cudaStream_t stream,
+                     const float* grad_scale = nullptr) {
   static thread_local AdamwBatch batch;   // ~26 KB: kept off the stack
   batch.s = adamw_scalars(hp);
+  batch.s.grad_scale = grad_scale;
   batch.n = 0;
   batch.total_chunks = 0;
   for (size_t i = 0; i <= ts.size(); ++i) {
@@ -306,6 +308,7 @@ size_t muon_bytes(const std::vector<ShapeClass>& classes) {
 struct MuonPlanHp {
   float lr, mu, wd, eps, a, b, c, scale_coeff;
   int nesterov, ns_steps, ns_only;
+  const float* grad_scale;   // clipping factor on the device, or nullptr
 };
 
 // Runs Muon on the matrices of one shape class; all of them must have rows x
@@ -353,6 +356,7 @@ opt_status run_muon_class(const MuonPlanHp& hp, const ShapeClass& cls, uint8_t* 
                                         std::sqrt(static_cast<double>(cls.B)));
       s.ns_steps = hp.ns_steps;
       s.ns_only = hp.ns_only;
+      s.grad_scale = hp.grad_scale;
       prof_begin(OPT_KERNEL_MUON_PREP, grp.count, grp.A, grp.B, stream);
       cudaError_t e = launch_muon_momentum(grp, buf, s, stream);
       prof_end(stream);
@@ -420,8 +424,66 @@ size_t min_bytes(const std::vector<ShapeClass>& classes) {
   return classes.empty() ? 0 : kHeaderBytes + m;
 }
 
+// Global-norm clipping of one step (opt_mixed_step_clipped).
+struct ClipPlan {
+  float max_norm;
+  float* user_norm;
+  float* user_scale;
+};
+
+// Header slots for the clipping factor and norm of the current step.
+constexpr size_t kScaleSlot = 64, kNormSlot = 68;
+
+int64_t clip_chunks(const Split& sp) {
+  int64_t chunks = 0;
+  for (const auto* list : {&sp.adamw, &sp.muon})
+    for (const opt_tensor* t : *list) chunks += (t->rows * t->cols + kAdamwChunk - 1) / kAdamwChunk;
+  return chunks;
+}
+
+size_t clip_bytes(const Split& sp) { return align_up(static_cast<size_t>(clip_chunks(sp)) * 4, kAlign); }
+
+// Sum of squares of every gradient, then the clipping factor (device scalar).
+opt_status run_clip(const Split& sp, const ClipPlan& clip, uint8_t* ws, cudaStream_t stream) {
+  static thread_local NormBatch batch;
+  float* partials = reinterpret_cast<float*>(ws + kHeaderBytes);
+  int64_t offset = 0;
+  batch.n = 0;
+  batch.total_chunks = 0;
+  batch.partial_offset = 0;
+  std::vector<const opt_tensor*> all(sp.adamw);
+  all.insert(all.end(), sp.muon.begin(), sp.muon.end());
+  for (size_t i = 0; i <= all.size(); ++i) {
+    const bool flush = (i == all.size()) || batch.n == kNormBatch;
+    if (flush && batch.n > 0) {
+      prof_begin(OPT_KERNEL_GRAD_NORM, batch.n, batch.total_chunks, 0, stream);
+      const cudaError_t e = launch_grad_sumsq(batch, partials, stream);
+      prof_end(stream);
+      if (e != cudaSuccess) return cuda_fail(e, "gradient norm");
+      offset += batch.total_chunks;
+      batch.n = 0;
+      batch.total_chunks = 0;
+      batch.partial_offset = offset;
+    }
+    if (i == all.size()) break;
+    const int64_t n = all[i]->rows * all[i]->cols;
+    if (n == 0) continue;
+    batch.t[batch.n] = NormTensorDesc{all[i]->main_grad, n, batch.total_chunks};
+    batch.total_chunks += (n + kAdamwChunk - 1) / kAdamwChunk;
+    ++batch.n;
+  }
+  prof_begin(OPT_KERNEL_CLIP_FINALIZE, 1, offset, 0, stream);
+  const cudaError_t e = launch_clip_finalize(partials, offset, clip.max_norm, reinterpret_cast<float*>(ws + kScaleSlot),
+                                             reinterpret_cast<float*>(ws + kNormSlot), clip.user_scale,
+                                             clip.user_norm, stream);
+  prof_end(stream);
+  if (e != cudaSuccess) return cuda_fail(e, "clip factor");
+  return OPT_OK;
+}
+
 opt_status mixed_impl(const opt_muon_hp* hpm, const opt_adamw_hp* hpa, const opt_tensor* tensors, int32_t n,
-                      int32_t routing, void* workspace, size_t ws_bytes, void* stream_ptr) {
+                      int32_t routing, void* workspace, size_t ws_bytes, void* stream_ptr,
+                      const ClipPlan* clip = nullptr) {
   Split sp;
   opt_status st = split_tensors(tensors, n, routing, sp);
   if (st != OPT_OK) return st;
@@ -430,20 +492,34 @@ opt_status mixed_impl(const opt_muon_hp* hpm, const opt_adamw_hp* hpa, const opt
   for (auto* t : sp.muon) any_muon |= (t->rows * t->cols) > 0;
   if (any_adamw && (st = check_adamw_hp(hpa)) != OPT_OK) return st;
   if (any_muon && (st = check_muon_hp(hpm)) != OPT_OK) return st;
+  if (clip && !std::isfinite(clip->max_norm)) return OPT_ERR_INVALID_ARG;
+  if (clip && ((reinterpret_cast<uintptr_t>(clip->user_norm) | reinterpret_cast<uintptr_t>(clip->user_scale)) & 3u))
+    return OPT_ERR_MISALIGNED;
   if (!any_adamw && !any_muon) return OPT_OK;
+  const bool clipping = clip && clip->max_norm > 0.f;   // max_norm <= 0: no clipping at all
   const std::vector<ShapeClass> classes = shape_classes(sp.muon);
-  if ((st = check_workspace(workspace, ws_bytes, min_bytes(classes))) != OPT_OK) return st;
+  const size_t clip_region = clipping ? clip_bytes(sp) : 0;
+  size_t need = min_bytes(classes);
+  if (clipping) need = (need ? need : kHeaderBytes) + clip_region;
+  if ((st = check_workspace(workspace, ws_bytes, need)) != OPT_OK) return st;
 
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
-  if (any_adamw && (st = run_adamw(hpa, sp.adamw, stream)) != OPT_OK) return st;
-  if (any_muon) {
-    uint8_t* ws = static_cast<uint8_t*>(workspace);
-    uint32_t* status = reinterpret_cast<uint32_t*>(ws);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const float* grad_scale = nullptr;
+  if (any_muon || clipping) {
     const cudaError_t e = cudaMemsetAsync(ws, 0, kHeaderBytes, stream);
     if (e != cudaSuccess) return cuda_fail(e, "workspace header");
-    const size_t off = kHeaderBytes;
+  }
+  if (clipping) {
+    if ((st = run_clip(sp, *clip, ws, stream)) != OPT_OK) return st;
+    grad_scale = reinterpret_cast<const float*>(ws + kScaleSlot);
+  }
+  if (any_adamw && (st = run_adamw(hpa, sp.adamw, stream, grad_scale)) != OPT_OK) return st;
+  if (any_muon) {
+    uint32_t* status = reinterpret_cast<uint32_t*>(ws);
+    const size_t off = kHeaderBytes + clip_region;
     MuonPlanHp hp{hpm->lr, hpm->momentum, hpm->weight_decay, hpm->eps, hpm->ns_a, hpm->ns_b,
-                  hpm->ns_c, hpm->scale_coeff, hpm->nesterov ? 1 : 0, hpm->ns_steps, 0};
+                  hpm->ns_c, hpm->scale_coeff, hpm->nesterov ? 1 : 0, hpm->ns_steps, 0, grad_scale};
     for (const ShapeClass& c : classes) {
       if ((st = run_muon_class(hp, c, ws + off, ws_bytes - off, status, stream, nullptr)) != OPT_OK) return st;
     }
@@ -459,10 +535,14 @@ using namespace mpopt;
 extern "C" {
 
 size_t opt_workspace_size(const opt_tensor* tensors, int32_t n, int32_t routing) {
+  const bool with_clip = (routing & OPT_WORKSPACE_CLIP) != 0;
+  routing &= ~OPT_WORKSPACE_CLIP;
   if (routing != OPT_KIND_AUTO && routing != OPT_KIND_ADAMW && routing != OPT_KIND_MUON) return 0;
   Split sp;
   if (split_tensors(tensors, n, routing, sp) != OPT_OK) return 0;
-  return total_bytes(shape_classes(sp.muon));
+  const size_t base = total_bytes(shape_classes(sp.muon));
+  if (!with_clip) return base;
+  return (base ? base : kHeaderBytes) + clip_bytes(sp);
 }
 
 opt_status opt_adamw_step(const opt_adamw_hp* hp, const opt_tensor* tensors, int32_t n, void* workspace,
@@ -480,6 +560,13 @@ opt_status opt_muon_step(const opt_muon_hp* hp, const opt_tensor* t, void* works
 opt_status opt_mixed_step(const opt_muon_hp* hp_muon, const opt_adamw_hp* hp_adamw, const opt_tensor* tensors,
                           int32_t n, void* workspace, size_t workspace_bytes, void* stream) {
   return mixed_impl(hp_muon, hp_adamw, tensors, n, OPT_KIND_AUTO, workspace, workspace_bytes, stream);
+}
+
+opt_status opt_mixed_step_clipped(const opt_muon_hp* hp_muon, const opt_adamw_hp* hp_adamw, float max_norm,
+                                  float* total_norm_out, float* clip_scale_out, const opt_tensor* tensors, int32_t n,
+                                  void* workspace, size_t workspace_bytes, void* stream) {
+  const ClipPlan clip{max_norm, total_norm_out, clip_scale_out};
+  return mixed_impl(hp_muon, hp_adamw, tensors, n, OPT_KIND_AUTO, workspace, workspace_bytes, stream, &clip);
 }
 
 opt_status opt_newton_schulz(const float* G, float* O, int64_t rows, int64_t cols, int32_t ns_steps, float a,

@@ -34,6 +34,8 @@ struct AdamwScalars {
   float one_minus_beta1, one_minus_beta2;
   float bias_c1, bias_c2;   // 1 - beta^t
   float decay;              // 1 - lr * weight_decay
+  int32_t pad_;
+  const float* grad_scale;  // device scalar multiplying every gradient (clipping), or nullptr
 };
 
 // Descriptors travel in the kernel's parameter space (no upload, no workspace):
@@ -101,6 +103,7 @@ struct MuonScalars {
   float step_scale;   // lr * scale_coeff * sqrt(max(R, C))
   int ns_steps;
   int ns_only;        // opt_newton_schulz: G is read from g, O written, no momentum/update
+  const float* grad_scale;  // device scalar multiplying every gradient (clipping), or nullptr
 };
 
 // Elementwise pass 1 (momentum, norm partials): fixed elements per block so the
@@ -140,6 +143,32 @@ enum : uint32_t {
   kStatusTimeoutAccFree = 4,  // MMA waited too long for a free accumulator
   kStatusTimeoutDrain = 5
 };
+
+// ------------------------------------------------------------- clipping ----
+
+// Global gradient norm: one fp32 partial sum of squares per 16K-element chunk
+// of every gradient (Muon and AdamW alike), then one fp64 reduction.
+constexpr int kNormBatch = 1200;
+struct NormTensorDesc {
+  const float* g;
+  int64_t numel;
+  int64_t chunk_begin;   // first chunk of this tensor within the launch
+};
+struct NormBatch {
+  int32_t n;
+  int32_t pad_;
+  int64_t total_chunks;
+  int64_t partial_offset;   // where this launch's chunks start in the partial buffer
+  NormTensorDesc t[kNormBatch];
+};
+static_assert(sizeof(NormBatch) <= 32000, "kernel parameter space");
+
+cudaError_t launch_grad_sumsq(const NormBatch& batch, float* partials, cudaStream_t stream);
+// scale_out = max_norm / (sqrt(sum) + 1e-6) when that is below 1, else 1
+// (1 as well when max_norm <= 0); norm_out = sqrt(sum); user_scale and
+// user_norm (optional) receive copies.
+cudaError_t launch_clip_finalize(const float* partials, int64_t n_partials, float max_norm, float* scale_out,
+                                 float* norm_out, float* user_scale, float* user_norm, cudaStream_t stream);
 
 int num_sms();   // SM count of the current device (cached per device)
 

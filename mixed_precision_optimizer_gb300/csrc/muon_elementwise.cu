@@ -48,6 +48,7 @@ muon_momentum_kernel(const MuonGroup grp, NsBuffers buf, MuonScalars s) {
   const MuonMat& M = grp.mats[mat];
   const int64_t n = static_cast<int64_t>(M.R) * M.C;
   const int64_t base = static_cast<int64_t>(blockIdx.x) * kNormElemsPerBlock;
+  const float gs = s.grad_scale ? *s.grad_scale : 1.f;   // clipping factor (1: none)
   float ss = 0.f;
   if (M.vec4 && base + kNormElemsPerBlock <= n) {   // 16-byte aligned, full block: float4 path
     const float4* g4 = reinterpret_cast<const float4*>(M.g + base);
@@ -55,7 +56,11 @@ muon_momentum_kernel(const MuonGroup grp, NsBuffers buf, MuonScalars s) {
 #pragma unroll 4
     for (int k = 0; k < kNormElemsPerBlock / 4 / kThreads; ++k) {
       const int j = k * kThreads + threadIdx.x;
-      const float4 g = g4[j];
+      float4 g = g4[j];
+      g.x *= gs;
+      g.y *= gs;
+      g.z *= gs;
+      g.w *= gs;
       float4 v;
       if (s.ns_only) {
         v = g;
@@ -74,7 +79,7 @@ muon_momentum_kernel(const MuonGroup grp, NsBuffers buf, MuonScalars s) {
     for (int k = 0; k < kNormElemsPerBlock / kThreads; ++k) {
       const int64_t i = base + k * kThreads + threadIdx.x;
       if (i >= n) break;
-      const float g = M.g[i];
+      const float g = M.g[i] * gs;
       float v;
       if (s.ns_only) {
         v = g;
@@ -133,6 +138,7 @@ muon_operand_kernel(const MuonGroup grp, NsBuffers buf, MuonScalars s) {
   const int64_t r0 = ty * kPrepTile, c0 = tx * kPrepTile;
   const int R = M.R, C = M.C;
   const float inv = buf.inv_norm[mat];
+  const float gs = s.grad_scale ? *s.grad_scale : 1.f;   // clipping factor (1: none)
   const int lc = (threadIdx.x % 16) * 4;       // first of 4 columns
   const int lr0 = threadIdx.x / 16;            // 0..15
   const bool vec = M.vec4 && (C % 4 == 0);     // every row start 16-byte aligned
@@ -153,14 +159,14 @@ muon_operand_kernel(const MuonGroup grp, NsBuffers buf, MuonScalars s) {
         const float4 g = *reinterpret_cast<const float4*>(M.g + i);
         float4 m = make_float4(0.f, 0.f, 0.f, 0.f);
         if (!s.ns_only) m = *reinterpret_cast<const float4*>(M.m + i);
-        val[0] = gtilde(s, g.x, m.x) * inv;
-        val[1] = gtilde(s, g.y, m.y) * inv;
-        val[2] = gtilde(s, g.z, m.z) * inv;
-        val[3] = gtilde(s, g.w, m.w) * inv;
+        val[0] = gtilde(s, g.x * gs, m.x) * inv;
+        val[1] = gtilde(s, g.y * gs, m.y) * inv;
+        val[2] = gtilde(s, g.z * gs, m.z) * inv;
+        val[3] = gtilde(s, g.w * gs, m.w) * inv;
       } else {
 #pragma unroll
         for (int q = 0; q < 4; ++q)
-          if (c + q < C) val[q] = gtilde(s, M.g[i + q], s.ns_only ? 0.f : M.m[i + q]) * inv;
+          if (c + q < C) val[q] = gtilde(s, M.g[i + q] * gs, s.ns_only ? 0.f : M.m[i + q]) * inv;
       }
     }
     const uint16_t h0 = f16_bits(val[0]), h1 = f16_bits(val[1]), h2 = f16_bits(val[2]), h3 = f16_bits(val[3]);
@@ -190,9 +196,10 @@ __global__ void muon_apply_direct_kernel(const MuonGroup grp, NsBuffers buf, Muo
   const MuonMat& M = grp.mats[mat];
   const int64_t n = static_cast<int64_t>(M.R) * M.C;
   const float inv = buf.inv_norm[mat];
+  const float gs = s.grad_scale ? *s.grad_scale : 1.f;
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const float o = gtilde(s, M.g[i], s.ns_only ? 0.f : M.m[i]) * inv;
+    const float o = gtilde(s, M.g[i] * gs, s.ns_only ? 0.f : M.m[i]) * inv;
     if (s.ns_only) {
       M.O[i] = o;
     } else {

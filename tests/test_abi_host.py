@@ -136,9 +136,22 @@ def test_workspace_size_formula(L):
     # same (min, max) shape in both orientations shares one class: two matrices
     two = L.opt_workspace_size(arr(tensor(300, 200), tensor(200, 300)), 2, mp.KIND_AUTO)
     assert two > want
+    # clipping adds the header (if absent) and one float per 16K gradient elements
+    assert L.opt_workspace_size(arr(tensor(1, 1000, 1)), 1, mp.KIND_AUTO | mp.WORKSPACE_CLIP) == 256 + 1024
+    assert L.opt_workspace_size(arr(tensor(300, 200)), 1, mp.KIND_AUTO | mp.WORKSPACE_CLIP) == want + 1024
     # invalid list -> 0
     assert L.opt_workspace_size(arr(tensor(300, 200, ndim=3)), 1, mp.KIND_MUON) == 0
     assert L.opt_workspace_size(arr(tensor(300, 200)), 1, 9) == 0
+
+
+def test_clipped_step_argument_errors(L):
+    hpa = mp.adamw_hp()
+    f = L.opt_mixed_step_clipped
+    one = arr(tensor(1, 10, 1))
+    assert f(None, ctypes.byref(hpa), float("nan"), None, None, one, 1, None, 0, None) == 1
+    assert f(None, ctypes.byref(hpa), 1.0, ctypes.c_void_p(FAKE + 2), None, one, 1, None, 0, None) == 3
+    assert f(None, ctypes.byref(hpa), 1.0, None, None, one, 1, None, 0, None) == 4      # needs workspace
+    assert f(None, ctypes.byref(mp.adamw_hp(step=0)), 1.0, None, None, one, 1, None, 0, None) == 1
 
 
 def test_newton_schulz_argument_errors(L):
