@@ -103,15 +103,25 @@ typedef struct {
 } opt_adamw_hp;
 
 /*
- * Muon hyper-parameters ("02 · Optimizer：算法与 infra" §1, §5.2, §5.4, §14.1).
+ * Muon hyper-parameters ("02 · Optimizer：算法与 infra" §1, §5.2, §5.4, §14.1,
+ * §14.6).
  *   lr            eta
  *   momentum      mu in [0, 1): m <- lerp(m, g, 1 - mu)
  *   weight_decay  lambda, decoupled, applied to W_{t-1}
  *   eps           Newton-Schulz normalisation X = G / (||G||_F + eps); 1e-7
  *   nesterov      nonzero: Newton-Schulz input lerp(g, m, mu); zero: m
  *   ns_steps      number of quintic iterations, 0..16 (5 on the pages)
- *   ns_a, ns_b, ns_c  quintic coefficients, (3.4445, -4.7750, 2.0315)
- *   scale_coeff   update scale factor k in k*sqrt(max(A, B)); 0.2
+ *   ns_a, ns_b, ns_c  quintic coefficients, (3.4445, -4.7750, 2.0315), used
+ *                 for every iteration unless ns_schedule is given
+ *   scale_coeff   free factor k of the update scale (0.2 on the pages)
+ *   scale_mode    OPT_SCALE_SPECTRAL: k * sqrt(max(m, n)) (the default, §5.4
+ *                 Eq. 4); OPT_SCALE_SHAPE: k * sqrt(max(1, m / n));
+ *                 OPT_SCALE_UNIT_RMS: k * sqrt(m / n) (§14.6), where
+ *                 m = rows (fan_out) and n = cols (fan_in) of the parameter
+ *   flags         OPT_MUON_NO_ORTHOGONALIZE: plain momentum SGD,
+ *                 W <- W (1 - lr lambda) - lr * k * gtilde (§1), no Newton-Schulz
+ *   ns_schedule   optional HOST array of ns_steps triples (a, b, c), one per
+ *                 iteration in order (a coefficient schedule); NULL: ns_a..c
  */
 typedef struct {
   float lr;
@@ -124,7 +134,13 @@ typedef struct {
   float ns_b;
   float ns_c;
   float scale_coeff;
+  int32_t scale_mode;
+  int32_t flags;
+  const float* ns_schedule;
 } opt_muon_hp;
+
+enum { OPT_SCALE_SPECTRAL = 0, OPT_SCALE_SHAPE = 1, OPT_SCALE_UNIT_RMS = 2 };
+enum { OPT_MUON_NO_ORTHOGONALIZE = 1 };
 
 /*
  * One parameter tensor.
@@ -140,6 +156,12 @@ typedef struct {
  *                rows*cols == 0 is allowed and does nothing.
  *   ndim         the parameter's dimensionality (used by OPT_KIND_AUTO)
  *   kind, flags  routing, see above
+ *   scale_rows, scale_cols  Muon only: the shape whose (fan_out, fan_in) set
+ *                the update scale; 0, 0 means this tensor's own shape.  A block
+ *                of a split parameter (QKV split, "02 · Optimizer：算法与 infra"
+ *                §5.5 / §14.4: Q, K and V rows orthogonalised separately) is
+ *                passed as its own row-block view with the whole parameter's
+ *                shape here.
  */
 typedef struct {
   float* main_param;
@@ -153,6 +175,8 @@ typedef struct {
   int32_t kind;
   int32_t flags;
   int32_t reserved;
+  int64_t scale_rows;
+  int64_t scale_cols;
 } opt_tensor;
 
 /*
@@ -302,7 +326,7 @@ MPOPT_API const char* opt_strerror(opt_status status);
 /* Text of the last CUDA error seen by this thread's calls ("" if none). */
 MPOPT_API const char* opt_last_cuda_error(void);
 
-/* ABI version: (major << 16) | minor. */
+/* ABI version: (major << 16) | minor (2.0: Muon variants, scale shapes, clipping). */
 MPOPT_API int32_t opt_abi_version(void);
 
 #ifdef __cplusplus

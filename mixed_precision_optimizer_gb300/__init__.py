@@ -30,6 +30,8 @@ OPT_OK = 0
 STATUS_NAMES = {0: "OPT_OK", 1: "OPT_ERR_INVALID_ARG", 2: "OPT_ERR_UNSUPPORTED", 3: "OPT_ERR_MISALIGNED",
                 4: "OPT_ERR_WORKSPACE", 5: "OPT_ERR_CUDA", 6: "OPT_ERR_DEVICE_TIMEOUT"}
 KIND_AUTO, KIND_ADAMW, KIND_MUON = 0, 1, 2
+SCALE_MODES = {"spectral": 0, "shape_scaling": 1, "unit_rms_norm": 2}
+MUON_NO_ORTHOGONALIZE = 1
 FLAG_EMBEDDING_OR_OUTPUT = 1
 NS_COEFFS = (3.4445, -4.7750, 2.0315)
 
@@ -50,7 +52,7 @@ class OptTensor(ctypes.Structure):
                 ("exp_avg", ctypes.c_void_p), ("exp_avg_sq", ctypes.c_void_p),
                 ("model_param", ctypes.c_void_p), ("rows", ctypes.c_int64), ("cols", ctypes.c_int64),
                 ("ndim", ctypes.c_int32), ("kind", ctypes.c_int32), ("flags", ctypes.c_int32),
-                ("reserved", ctypes.c_int32)]
+                ("reserved", ctypes.c_int32), ("scale_rows", ctypes.c_int64), ("scale_cols", ctypes.c_int64)]
 
 
 class OptAdamwHP(ctypes.Structure):
@@ -63,7 +65,8 @@ class OptMuonHP(ctypes.Structure):
     _fields_ = [("lr", ctypes.c_float), ("momentum", ctypes.c_float), ("weight_decay", ctypes.c_float),
                 ("eps", ctypes.c_float), ("nesterov", ctypes.c_int32), ("ns_steps", ctypes.c_int32),
                 ("ns_a", ctypes.c_float), ("ns_b", ctypes.c_float), ("ns_c", ctypes.c_float),
-                ("scale_coeff", ctypes.c_float)]
+                ("scale_coeff", ctypes.c_float), ("scale_mode", ctypes.c_int32), ("flags", ctypes.c_int32),
+                ("ns_schedule", ctypes.POINTER(ctypes.c_float))]
 
 
 _lib = None
@@ -166,6 +169,7 @@ class Param:
     model: object = None
     embedding_or_output: bool = False
     kind: Optional[str] = None
+    scale_shape: Optional[tuple] = None   # Muon: shape setting the update scale (split blocks)
 
     def to_c(self, force=None):
         import torch
@@ -187,7 +191,25 @@ class Param:
         ct.rows, ct.cols, ct.ndim = rows, cols, ndim
         ct.kind = {None: KIND_AUTO, "adamw": KIND_ADAMW, "muon": KIND_MUON}[kind]
         ct.flags = FLAG_EMBEDDING_OR_OUTPUT if self.embedding_or_output else 0
+        if self.scale_shape is not None:
+            ct.scale_rows, ct.scale_cols = (int(x) for x in self.scale_shape)
         return ct
+
+    def split_rows(self, sizes):
+        """Row-block views of a 2-D parameter (QKV split: the blocks are
+        orthogonalised separately, the update scale stays the whole
+        parameter's).  No copies: every block writes into this parameter."""
+        import torch
+        shape = tuple(self.main_param.shape)
+        if len(shape) != 2 or sum(sizes) != shape[0]:
+            raise ValueError("split sizes must add up to the number of rows")
+        out, r0 = [], 0
+        for n in sizes:
+            sl = lambda t: None if t is None else t[r0:r0 + n]
+            out.append(Param(sl(self.main_param), sl(self.main_grad), sl(self.exp_avg), sl(self.exp_avg_sq),
+                             sl(self.model), self.embedding_or_output, "muon", shape))
+            r0 += n
+        return out
 
 
 def _array(params: Sequence[Param], force=None):
@@ -209,9 +231,16 @@ def adamw_hp(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01, step=
 
 
 def muon_hp(lr=0.02, momentum=0.95, weight_decay=0.0, eps=1e-7, nesterov=True, ns_steps=5,
-            coeffs=NS_COEFFS, scale_coeff=0.2):
+            coeffs=NS_COEFFS, scale_coeff=0.2, scale_mode="spectral", orthogonalize=True, schedule=None):
+    """schedule: optional list of ns_steps (a, b, c) triples, one per iteration."""
     a, b, c = coeffs
-    return OptMuonHP(lr, momentum, weight_decay, eps, 1 if nesterov else 0, int(ns_steps), a, b, c, scale_coeff)
+    hp = OptMuonHP(lr, momentum, weight_decay, eps, 1 if nesterov else 0, int(ns_steps), a, b, c, scale_coeff,
+                   SCALE_MODES[scale_mode], 0 if orthogonalize else MUON_NO_ORTHOGONALIZE, None)
+    if schedule is not None:
+        flat = [float(x) for trip in schedule for x in trip]
+        hp._schedule_buf = (ctypes.c_float * len(flat))(*flat)   # kept alive with the struct
+        hp.ns_schedule = ctypes.cast(hp._schedule_buf, ctypes.POINTER(ctypes.c_float))
+    return hp
 
 
 def workspace_size(params: Sequence[Param], routing="auto", clip=False) -> int:

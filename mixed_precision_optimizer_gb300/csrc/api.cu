@@ -88,6 +88,8 @@ opt_status check_tensor(const opt_tensor& t, bool muon) {
   if (muon) {
     if (t.ndim != 2) return OPT_ERR_INVALID_ARG;
     if (t.rows > (int64_t(1) << 30) || t.cols > (int64_t(1) << 30)) return OPT_ERR_UNSUPPORTED;
+    if (t.scale_rows < 0 || t.scale_cols < 0 || ((t.scale_rows == 0) != (t.scale_cols == 0)))
+      return OPT_ERR_INVALID_ARG;
   }
   if (n == 0) return OPT_OK;
   if (!t.main_param || !t.main_grad || !t.exp_avg) return OPT_ERR_INVALID_ARG;
@@ -117,6 +119,11 @@ opt_status check_muon_hp(const opt_muon_hp* hp) {
   if (!(hp->momentum >= 0.f && hp->momentum < 1.f)) return OPT_ERR_INVALID_ARG;
   if (hp->eps < 0.f) return OPT_ERR_INVALID_ARG;
   if (hp->ns_steps < 0 || hp->ns_steps > 16) return OPT_ERR_INVALID_ARG;
+  if (hp->scale_mode < OPT_SCALE_SPECTRAL || hp->scale_mode > OPT_SCALE_UNIT_RMS) return OPT_ERR_INVALID_ARG;
+  if (hp->flags & ~OPT_MUON_NO_ORTHOGONALIZE) return OPT_ERR_INVALID_ARG;
+  if (hp->ns_schedule)
+    for (int i = 0; i < 3 * hp->ns_steps; ++i)
+      if (!finite(hp->ns_schedule[i])) return OPT_ERR_INVALID_ARG;
   return OPT_OK;
 }
 
@@ -309,7 +316,24 @@ struct MuonPlanHp {
   float lr, mu, wd, eps, a, b, c, scale_coeff;
   int nesterov, ns_steps, ns_only;
   const float* grad_scale;   // clipping factor on the device, or nullptr
+  int scale_mode;            // OPT_SCALE_*
+  int no_ortho;              // plain momentum SGD
+  const float* schedule;     // host (a, b, c) per iteration, or nullptr: (a, b, c) every time
 };
+
+// lr * update scale for a parameter of shape R x C ("02 · Optimizer：算法与
+// infra" §5.4 Eq. 4 and §14.6): k sqrt(max(m, n)), k sqrt(max(1, m/n)) or
+// k sqrt(m/n) with m = fan_out = R, n = fan_in = C; plain momentum SGD: k.
+float step_scale_of(const MuonPlanHp& hp, int64_t R, int64_t C) {
+  const double m = static_cast<double>(R), n = static_cast<double>(C);
+  double f = 1.0;
+  if (!hp.no_ortho) {
+    if (hp.scale_mode == OPT_SCALE_SHAPE) f = std::sqrt(m / n > 1.0 ? m / n : 1.0);
+    else if (hp.scale_mode == OPT_SCALE_UNIT_RMS) f = std::sqrt(m / n);
+    else f = std::sqrt(m > n ? m : n);
+  }
+  return static_cast<float>(static_cast<double>(hp.lr) * static_cast<double>(hp.scale_coeff) * f);
+}
 
 // Runs Muon on the matrices of one shape class; all of them must have rows x
 // cols equal to (R, C) or (C, R) -- both orientations share a class.
@@ -341,6 +365,9 @@ opt_status run_muon_class(const MuonPlanHp& hp, const ShapeClass& cls, uint8_t* 
         M.C = static_cast<int32_t>(t->cols);
         M.transposed = t->rows > t->cols ? 1 : 0;
         M.vec4 = ((reinterpret_cast<uintptr_t>(M.g) | reinterpret_cast<uintptr_t>(M.m)) & 15u) == 0 ? 1 : 0;
+        const int64_t sr = t->scale_rows > 0 ? t->scale_rows : t->rows;
+        const int64_t sc = t->scale_cols > 0 ? t->scale_cols : t->cols;
+        M.step_scale = step_scale_of(hp, sr, sc);
       }
       const NsBuffers buf = carve(region, static_cast<int64_t>(gn), cls.A, cls.B, status);
       MuonScalars s{};
@@ -348,12 +375,13 @@ opt_status run_muon_class(const MuonPlanHp& hp, const ShapeClass& cls, uint8_t* 
       s.one_minus_mu = static_cast<float>(1.0 - static_cast<double>(hp.mu));
       s.nesterov = hp.nesterov;
       s.eps = hp.eps;
-      s.a = hp.a;
-      s.b = hp.b;
-      s.c = hp.c;
+      for (int it = 0; it < hp.ns_steps && it < 16; ++it) {
+        s.sched[it][0] = hp.schedule ? hp.schedule[3 * it + 0] : hp.a;
+        s.sched[it][1] = hp.schedule ? hp.schedule[3 * it + 1] : hp.b;
+        s.sched[it][2] = hp.schedule ? hp.schedule[3 * it + 2] : hp.c;
+      }
       s.decay = static_cast<float>(1.0 - static_cast<double>(hp.lr) * static_cast<double>(hp.wd));
-      s.step_scale = static_cast<float>(static_cast<double>(hp.lr) * static_cast<double>(hp.scale_coeff) *
-                                        std::sqrt(static_cast<double>(cls.B)));
+      s.no_normalize = hp.no_ortho;
       s.ns_steps = hp.ns_steps;
       s.ns_only = hp.ns_only;
       s.grad_scale = hp.grad_scale;
@@ -365,19 +393,20 @@ opt_status run_muon_class(const MuonPlanHp& hp, const ShapeClass& cls, uint8_t* 
       e = launch_muon_norm(grp, buf, s, stream);
       prof_end(stream);
       if (e != cudaSuccess) return cuda_fail(e, "muon norm");
-      if (hp.ns_steps > 0) {
+      const int ns_steps = hp.no_ortho ? 0 : hp.ns_steps;
+      if (ns_steps > 0) {
         prof_begin(OPT_KERNEL_MUON_OPERANDS, grp.count, grp.A, grp.B, stream);
         e = launch_muon_operands(grp, buf, s, stream);
         prof_end(stream);
         if (e != cudaSuccess) return cuda_fail(e, "muon operands");
       }
-      if (hp.ns_steps == 0) {
+      if (ns_steps == 0) {
         prof_begin(OPT_KERNEL_MUON_APPLY, grp.count, grp.A, grp.B, stream);
         e = launch_muon_apply_direct(grp, buf, s, stream);
         prof_end(stream);
         if (e != cudaSuccess) return cuda_fail(e, "muon apply");
       }
-      for (int it = 0; it < hp.ns_steps; ++it) {
+      for (int it = 0; it < ns_steps; ++it) {
         e = launch_ns_iteration(grp, buf, s, it, stream);
         if (e != cudaSuccess) return cuda_fail(e, "newton-schulz gemm");
       }
@@ -518,8 +547,10 @@ opt_status mixed_impl(const opt_muon_hp* hpm, const opt_adamw_hp* hpa, const opt
   if (any_muon) {
     uint32_t* status = reinterpret_cast<uint32_t*>(ws);
     const size_t off = kHeaderBytes + clip_region;
-    MuonPlanHp hp{hpm->lr, hpm->momentum, hpm->weight_decay, hpm->eps, hpm->ns_a, hpm->ns_b,
-                  hpm->ns_c, hpm->scale_coeff, hpm->nesterov ? 1 : 0, hpm->ns_steps, 0, grad_scale};
+    MuonPlanHp hp{hpm->lr,         hpm->momentum,           hpm->weight_decay, hpm->eps,
+                  hpm->ns_a,       hpm->ns_b,               hpm->ns_c,         hpm->scale_coeff,
+                  hpm->nesterov ? 1 : 0, hpm->ns_steps, 0,  grad_scale,        hpm->scale_mode,
+                  (hpm->flags & OPT_MUON_NO_ORTHOGONALIZE) ? 1 : 0,          hpm->ns_schedule};
     for (const ShapeClass& c : classes) {
       if ((st = run_muon_class(hp, c, ws + off, ws_bytes - off, status, stream, nullptr)) != OPT_OK) return st;
     }
@@ -639,7 +670,7 @@ opt_status opt_profile_launches(void* const* events, opt_launch_info* info, int3
   return OPT_OK;
 }
 
-int32_t opt_abi_version(void) { return (1 << 16) | 0; }
+int32_t opt_abi_version(void) { return (2 << 16) | 0; }
 
 }  // extern "C"
 

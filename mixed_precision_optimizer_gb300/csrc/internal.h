@@ -72,6 +72,8 @@ struct MuonMat {
   int32_t R, C;           // this matrix's shape (W layout)
   int32_t transposed;     // R > C: the wide orientation is W^T
   int32_t vec4;           // g and m 16-byte aligned: vector path in the momentum pass
+  float step_scale;       // lr * update scale of this matrix (scale mode, shape)
+  int32_t pad_;
 };
 
 struct MuonGroup {
@@ -100,10 +102,11 @@ struct MuonScalars {
   float eps;
   float a, b, c;
   float decay;        // 1 - lr * weight_decay
-  float step_scale;   // lr * scale_coeff * sqrt(max(R, C))
   int ns_steps;
   int ns_only;        // opt_newton_schulz: G is read from g, O written, no momentum/update
+  int no_normalize;   // plain momentum SGD: the direction is gtilde itself
   const float* grad_scale;  // device scalar multiplying every gradient (clipping), or nullptr
+  float sched[16][3]; // (a, b, c) of each iteration
 };
 
 // Elementwise pass 1 (momentum, norm partials): fixed elements per block so the

@@ -190,7 +190,8 @@ muon_operand_kernel(const MuonGroup grp, NsBuffers buf, MuonScalars s) {
   }
 }
 
-// ns_steps == 0: O = X0 = gtilde * inv_norm; apply the update (or write O).
+// ns_steps == 0: O = X0 = gtilde * inv_norm (plain momentum SGD: O = gtilde);
+// apply the update (or write O).
 __global__ void muon_apply_direct_kernel(const MuonGroup grp, NsBuffers buf, MuonScalars s) {
   const int mat = blockIdx.y;
   const MuonMat& M = grp.mats[mat];
@@ -199,11 +200,11 @@ __global__ void muon_apply_direct_kernel(const MuonGroup grp, NsBuffers buf, Muo
   const float gs = s.grad_scale ? *s.grad_scale : 1.f;
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const float o = gtilde(s, M.g[i] * gs, s.ns_only ? 0.f : M.m[i]) * inv;
+    const float o = gtilde(s, M.g[i] * gs, s.ns_only ? 0.f : M.m[i]) * (s.no_normalize ? 1.f : inv);
     if (s.ns_only) {
       M.O[i] = o;
     } else {
-      const float w = M.W[i] * s.decay - s.step_scale * o;
+      const float w = M.W[i] * s.decay - M.step_scale * o;
       M.W[i] = w;
       if (M.Wb) M.Wb[i] = bf16_rne(w);
     }

@@ -82,7 +82,7 @@ struct GemmParams {
   uint16_t* Xh;         // bx: fp16 iterate out
   uint16_t* Xt_out;     // bx: fp16 transposed iterate out
   float a, b, c;
-  float decay, step_scale;
+  float decay;
   int ns_only;
   uint32_t* status;
 };
@@ -391,7 +391,7 @@ __device__ __forceinline__ void epilogue_block(const GemmParams& P, const MuonGr
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
           if (j < n_runs) {
-            const float wv = old[j] * P.decay - P.step_scale * w[j];
+            const float wv = old[j] * P.decay - M.step_scale * w[j];
             M.W[first + j * C] = wv;
             if (M.Wb) M.Wb[first + j * C] = bf16_rne(wv);
           }
@@ -621,11 +621,10 @@ cudaError_t launch_ns_iteration(const MuonGroup& grp, const NsBuffers& buf, cons
   base.count = grp.count;
   base.Ap = Ap;
   base.Bp = Bp;
-  base.a = s.a;
-  base.b = s.b;
-  base.c = s.c;
+  base.a = s.sched[it][0];
+  base.b = s.sched[it][1];
+  base.c = s.sched[it][2];
   base.decay = s.decay;
-  base.step_scale = s.step_scale;
   base.ns_only = s.ns_only;
   base.status = buf.status;
   const int T = static_cast<int>(Ap / 256);

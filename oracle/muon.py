@@ -21,6 +21,18 @@ and Eq. 4; §14.1 decay before the update)::
 
     W_t = W_{t-1} * (1 - lr * lambda) - lr * 0.2 * sqrt(max(A, B)) * O_t
 
+Variants (same page, §14.6 and §14.4, §5.5, §1):
+
+* scale modes on the Newton-Schulz output, with fan_out = rows (m) and
+  fan_in = cols (n) of the parameter: ``spectral`` sqrt(max(m, n)) (the
+  default, Eq. 4's shape factor), ``shape_scaling`` sqrt(max(1, m / n)),
+  ``unit_rms_norm`` sqrt(m / n), each times a free factor (0.2 above);
+* QKV split: a [q + k + v, h] parameter is orthogonalised block by block
+  (rows q, k, v separately) and the blocks are put back together; the scale
+  factor uses the whole parameter's shape;
+* a per-iteration coefficient schedule (a list of (a, b, c), one per step);
+* plain momentum SGD (no orthogonalisation): W -= lr * gtilde (§1).
+
 The iteration is the oracle; ``polar_svd`` (U V^T from an SVD, §5.1) is only
 a sanity reference, since five quintic steps do not converge to it.
 
@@ -60,44 +72,81 @@ def momentum_update(m, g, mu, nesterov=True):
     return m_new, gt
 
 
+def _schedule(coeffs, steps):
+    """One (a, b, c) per iteration: a single triple repeats; a list gives the
+    coefficients of each iteration in order."""
+    if len(coeffs) == 3 and np.isscalar(coeffs[0]):
+        return [tuple(coeffs)] * int(steps)
+    assert len(coeffs) == int(steps)
+    return [tuple(c) for c in coeffs]
+
+
 def newton_schulz(G, steps=5, coeffs=NS_COEFFS, eps=NS_EPS):
     """Quintic Newton-Schulz iteration in fp64, literally as printed."""
-    a, b, c = coeffs
     G = np.asarray(G, dtype=np.float64)
     assert G.ndim == 2
     X = G / (np.linalg.norm(G) + eps)          # ||.||_F for a 2-D array
     transposed = G.shape[0] > G.shape[1]
     if transposed:
         X = X.T
-    for _ in range(int(steps)):
+    for a, b, c in _schedule(coeffs, steps):
         A = X @ X.T
         B = b * A + c * (A @ A)
         X = a * X + B @ X
     return X.T if transposed else X
 
 
-def update_scale(rows, cols, scale_coeff=0.2):
-    """0.2 * sqrt(max(A, B)) (§5.4 Eq. 4: max of the two dimensions, not fan_in)."""
-    return scale_coeff * math.sqrt(max(int(rows), int(cols)))
+SCALE_MODES = ("spectral", "shape_scaling", "unit_rms_norm")
 
 
-def apply_update(W, O, lr, weight_decay, scale_coeff=0.2):
-    """W_t = W_{t-1} (1 - lr lambda) - lr * 0.2 sqrt(max(A,B)) O, in fp64."""
+def update_scale(rows, cols, scale_coeff=0.2, mode="spectral"):
+    """The factor on the Newton-Schulz output, fan_out = rows, fan_in = cols:
+    spectral 0.2 * sqrt(max(m, n)) (§5.4 Eq. 4: max of the two dimensions, not
+    fan_in), shape_scaling sqrt(max(1, m / n)), unit_rms_norm sqrt(m / n)
+    (§14.6), times the free factor scale_coeff."""
+    m, n = float(rows), float(cols)
+    if mode == "spectral":
+        f = math.sqrt(max(m, n))
+    elif mode == "shape_scaling":
+        f = math.sqrt(max(1.0, m / n))
+    elif mode == "unit_rms_norm":
+        f = math.sqrt(m / n)
+    else:
+        raise ValueError(mode)
+    return scale_coeff * f
+
+
+def apply_update(W, O, lr, weight_decay, scale_coeff=0.2, mode="spectral", scale_shape=None):
+    """W_t = W_{t-1} (1 - lr lambda) - lr * scale * O, in fp64; the scale is
+    that of `scale_shape` (the whole parameter) when given, else W's shape."""
     W = np.asarray(W, dtype=np.float64)
-    s = update_scale(W.shape[0], W.shape[1], scale_coeff)
+    R, C = scale_shape if scale_shape is not None else W.shape
+    s = update_scale(R, C, scale_coeff, mode)
     return W * (1.0 - lr * weight_decay) - lr * s * np.asarray(O, dtype=np.float64)
 
 
 def muon_step(W, g, m, *, lr, momentum, weight_decay=0.0, nesterov=True,
-              ns_steps=5, coeffs=NS_COEFFS, eps=NS_EPS, scale_coeff=0.2):
+              ns_steps=5, coeffs=NS_COEFFS, eps=NS_EPS, scale_coeff=0.2, mode="spectral",
+              split_rows=None, orthogonalize=True):
     """One Muon step for one 2-D matrix, everything in fp64.
 
-    Returns (W_new, m_new, O) where O is the Newton-Schulz output (unscaled).
+    split_rows: row counts of blocks orthogonalised separately (QKV split);
+    orthogonalize=False gives plain momentum SGD (W -= lr * scale_coeff *
+    gtilde, no Newton-Schulz and no shape factor).
+    Returns (W_new, m_new, O) where O is the (unscaled) direction.
     Inputs are not modified.
     """
     m_new, gt = momentum_update(m, g, momentum, nesterov)
-    O = newton_schulz(gt, ns_steps, coeffs, eps)
-    W_new = apply_update(W, O, lr, weight_decay, scale_coeff)
+    if not orthogonalize:
+        W = np.asarray(W, dtype=np.float64)
+        return W * (1.0 - lr * weight_decay) - lr * scale_coeff * gt, m_new, gt
+    if split_rows:
+        assert sum(split_rows) == gt.shape[0]
+        edges = np.cumsum([0] + list(split_rows))
+        O = np.concatenate([newton_schulz(gt[a:b], ns_steps, coeffs, eps) for a, b in zip(edges[:-1], edges[1:])])
+    else:
+        O = newton_schulz(gt, ns_steps, coeffs, eps)
+    W_new = apply_update(W, O, lr, weight_decay, scale_coeff, mode, scale_shape=np.shape(W))
     return W_new, m_new, O
 
 

@@ -42,7 +42,7 @@ def test_strerror_and_version(L):
     for code, name in mp.STATUS_NAMES.items():
         assert L.opt_strerror(code)
     assert L.opt_strerror(99) == b"unknown status"
-    assert L.opt_abi_version() >> 16 == 1
+    assert L.opt_abi_version() >> 16 == 2
 
 
 FAKE = 1 << 20     # 1 MiB: an aligned address, never dereferenced
@@ -110,6 +110,17 @@ def test_muon_argument_errors(L):
     assert L.opt_muon_step(ctypes.byref(mp.muon_hp(coeffs=(1.0, float("nan"), 1.0))), arr(tensor(8, 16)),
                            ws, big, None) == inv
     assert L.opt_muon_step(None, arr(tensor(8, 16)), ws, big, None) == inv
+    bad = mp.muon_hp()
+    bad.scale_mode = 3
+    assert L.opt_muon_step(ctypes.byref(bad), arr(tensor(8, 16)), ws, big, None) == inv
+    bad = mp.muon_hp()
+    bad.flags = 4
+    assert L.opt_muon_step(ctypes.byref(bad), arr(tensor(8, 16)), ws, big, None) == inv
+    sched = mp.muon_hp(ns_steps=2, schedule=[(1.0, 2.0, 3.0), (1.0, float("inf"), 3.0)])
+    assert L.opt_muon_step(ctypes.byref(sched), arr(tensor(8, 16)), ws, big, None) == inv
+    t = tensor(8, 16)
+    t.scale_rows = 24                                       # scale shape needs both dims
+    assert L.opt_muon_step(ctypes.byref(hp), arr(t), ws, big, None) == inv
     assert L.opt_muon_step(ctypes.byref(hp), None, ws, big, None) == inv
     # workspace: missing, misaligned, too small
     assert L.opt_muon_step(ctypes.byref(hp), arr(tensor(8, 16)), None, 0, None) == 4

@@ -360,3 +360,61 @@ def test_clip_pins_catch_planted_mistakes(kind):
         coeff = max_norm / (tn(grads) + (-1e-6 if kind == "eps_missing_sign" else 1e-6))
         return coeff if (coeff < 1.0 or kind == "always_scale") else 1.0
     assert _clip_pin_failures(tn, cs) != []
+
+
+# ------------------------------------------------------- Muon variants ----
+
+def test_scale_modes_follow_the_printed_formulas():
+    """§14.6 of "02 · Optimizer：算法与 infra": spectral = max(m,n)**0.5,
+    shape_scaling = max(1, m/n)**0.5, unit_rms_norm = (m/n)**0.5, with
+    m = fan_out (rows) and n = fan_in (cols)."""
+    for (m, n), want in {(4096, 1024): (64.0, 2.0, 2.0), (1024, 4096): (64.0, 1.0, 0.5),
+                         (14336, 4096): (math.sqrt(14336), math.sqrt(3.5), math.sqrt(3.5))}.items():
+        got = tuple(OM.update_scale(m, n, 1.0, mode) for mode in OM.SCALE_MODES)
+        assert np.allclose(got, want, rtol=1e-15)
+    assert OM.update_scale(256, 512, 0.2) == 0.2 * math.sqrt(512)
+
+
+def test_coefficient_schedule_is_composition_of_quintics():
+    """With a different (a, b, c) in each iteration, every singular value goes
+    through the composition of the per-iteration quintics (§5.2's
+    per-singular-value argument does not need equal coefficients); a schedule
+    of identical triples equals the single triple."""
+    rng = np.random.default_rng(13)
+    U = P.random_orthonormal(rng, 30, 30)
+    V = P.random_orthonormal(rng, 50, 30)
+    S = np.linspace(0.05, 1.0, 30)
+    G = (U * S) @ V.T
+    sched = [(3.4445, -4.7750, 2.0315), (3.0, -3.2, 1.2), (2.5, -2.0, 0.5), (1.875, -1.25, 0.375)]
+    s = S / (np.linalg.norm(S) + 1e-7)
+    for a, b, c in sched:
+        s = a * s + b * s ** 3 + c * s ** 5
+    assert np.allclose(OM.newton_schulz(G, 4, sched), (U * s) @ V.T, atol=1e-12)
+    assert np.array_equal(OM.newton_schulz(G, 3, [P.COEFFS] * 3), OM.newton_schulz(G, 3))
+
+
+def test_split_blocks_are_orthogonalised_separately():
+    """QKV split (§5.5, §14.4): each row block is orthogonalised on its own, so
+    the split result differs from the whole-matrix result but each block
+    equals Newton-Schulz of that block; the scale uses the full shape."""
+    rng = np.random.default_rng(14)
+    W = rng.standard_normal((48, 32)) * 0.02
+    g = rng.standard_normal((48, 32)) * 1e-2
+    m = np.zeros((48, 32))
+    Wn, _, O = OM.muon_step(W, g, m, lr=0.02, momentum=0.95, split_rows=[16, 16, 16])
+    gt = OM.momentum_update(m, g, 0.95)[1]
+    for a in (0, 16, 32):
+        assert np.allclose(O[a:a + 16], OM.newton_schulz(gt[a:a + 16]), atol=1e-13)
+    assert np.allclose(Wn, W - 0.02 * 0.2 * math.sqrt(48) * O, atol=1e-15)
+    whole = OM.muon_step(W, g, m, lr=0.02, momentum=0.95)[2]
+    assert np.linalg.norm(whole - O) > 1e-3
+
+
+def test_plain_momentum_sgd():
+    """Without orthogonalisation the step is theta -= lr * gtilde (§1)."""
+    W = np.ones((3, 4))
+    g = np.full((3, 4), 2.0)
+    m = np.zeros((3, 4))
+    Wn, mn, _ = OM.muon_step(W, g, m, lr=0.1, momentum=0.5, orthogonalize=False, scale_coeff=1.0)
+    # m = 0.5 * 2 = 1; gtilde = lerp(2, 1, 0.5) = 1.5
+    assert np.allclose(mn, 1.0) and np.allclose(Wn, 1 - 0.1 * 1.5)
