@@ -491,21 +491,26 @@ def run_e2e(args, step, params, t, total, dist: Dist):
         raise SystemExit("e2e: host buffers are not page-locked")
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream()
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.e2e_steps)]
     dist.barrier()
     torch.cuda.synchronize()
-    start.record(stream)
-    for _ in range(args.e2e_steps):
+    t_wall = time.perf_counter()
+    for k in range(args.e2e_steps):
+        ev[k][0].record(stream)
         for p, gh in zip(params, g_host):
             p.main_grad.reshape(-1).copy_(gh, non_blocking=True)
+        ev[k][1].record(stream)
         step(t)
         t += 1
+        ev[k][2].record(stream)
         for p, bh in zip(params, b_host):
             bh.copy_(p.model.reshape(-1), non_blocking=True)
-    end.record(stream)
+        ev[k][3].record(stream)
     torch.cuda.synchronize()
+    wall_ms = (time.perf_counter() - t_wall) * 1e3
     dist.barrier()
-    ms = dist.max(start.elapsed_time(end))
+    ms = dist.max(ev[0][0].elapsed_time(ev[-1][3]))
+    phase = [sum(e[i].elapsed_time(e[i + 1]) for e in ev) / args.e2e_steps for i in range(3)]
     cudart = torch.cuda.cudart()
     for a in reg_g + reg_b:
         cudart.cudaHostUnregister(a.ctypes.data)
@@ -513,7 +518,9 @@ def run_e2e(args, step, params, t, total, dist: Dist):
     d2h = sum(x.numel() * x.element_size() for x in b_host)
     return {"value": round(total * args.e2e_steps * dist.world / (ms * 1e-3), 1), "unit": UNIT,
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-            "steps": args.e2e_steps, "ms_per_step": round(ms / args.e2e_steps, 3)}
+            "steps": args.e2e_steps, "ms_per_step": round(ms / args.e2e_steps, 3),
+            "h2d_ms": round(phase[0], 3), "step_ms": round(phase[1], 3), "d2h_ms": round(phase[2], 3),
+            "host_wall_ms_per_step": round(wall_ms / args.e2e_steps, 3)}
 
 
 # --------------------------------------------------------- reference arm --

@@ -243,6 +243,18 @@ MPOPT_API opt_status opt_mixed_step_clipped(const opt_muon_hp* hp_muon, const op
                                             int32_t n, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * main_param <- fp32(model_param) for every tensor that has a bf16 model copy
+ * ("02 · Optimizer：算法与 infra" §9.2 reload_model_params: refresh the masters
+ * after the model copy was changed from outside; "支持FP32优化器" §9.3-§9.4:
+ * the plain-checkpoint and model-only restore branches).  Exact (bf16 widens
+ * to fp32 without rounding).  fp32-native tensors (model_param NULL) are left
+ * alone.  Only main_param, model_param and the shape are read; no workspace.
+ * Note the fp32 tail the masters had is not recoverable this way: a resume
+ * that must continue bit for bit restores main_param itself.
+ */
+MPOPT_API opt_status opt_reload_model_params(const opt_tensor* tensors, int32_t n, void* stream);
+
+/*
  * Newton-Schulz orthogonalisation alone ("02 · Optimizer：算法与 infra" §5.2):
  * O = NS_steps(G) for one fp32 rows x cols matrix G, same fp16 tensor-core
  * path as opt_muon_step.  G and O are device fp32 [rows*cols]; O may alias G.

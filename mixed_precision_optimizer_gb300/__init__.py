@@ -72,7 +72,8 @@ class OptMuonHP(ctypes.Structure):
 _lib = None
 
 EXPORTED = ("opt_workspace_size", "opt_adamw_step", "opt_muon_step", "opt_mixed_step", "opt_mixed_step_clipped",
-            "opt_newton_schulz", "opt_newton_schulz_noalloc", "opt_device_status", "opt_profile_launches",
+            "opt_newton_schulz", "opt_newton_schulz_noalloc", "opt_reload_model_params", "opt_device_status",
+            "opt_profile_launches",
             "opt_strerror",
             "opt_last_cuda_error", "opt_abi_version")
 
@@ -114,6 +115,8 @@ def lib():
     L.opt_newton_schulz.restype = ctypes.c_int
     L.opt_newton_schulz_noalloc.argtypes = [vp, vp, i64, i64, i32, f32, f32, f32, f32, vp]
     L.opt_newton_schulz_noalloc.restype = ctypes.c_int
+    L.opt_reload_model_params.argtypes = [T, i32, vp]
+    L.opt_reload_model_params.restype = ctypes.c_int
     L.opt_device_status.argtypes = [vp, vp]
     L.opt_device_status.restype = ctypes.c_int
     L.opt_profile_launches.argtypes = [vp, ctypes.POINTER(OptLaunchInfo), i32, ctypes.POINTER(i32)]
@@ -297,6 +300,12 @@ def mixed_step_clipped(params: Sequence[Param], hp_muon: Optional[OptMuonHP], hp
                                         ctypes.byref(hp_adamw) if hp_adamw is not None else None,
                                         float(max_norm), tn, cs, arr, len(params), w, nb, _stream(stream)),
            "opt_mixed_step_clipped")
+
+
+def reload_model_params(params: Sequence[Param], stream=None):
+    """main_param <- fp32(model) for every parameter with a bf16 model copy."""
+    arr = _array(params)
+    _check(lib().opt_reload_model_params(arr, len(params), _stream(stream)), "opt_reload_model_params")
 
 
 def newton_schulz(G, out, steps=5, coeffs=NS_COEFFS, eps=1e-7, workspace=None, stream=None):

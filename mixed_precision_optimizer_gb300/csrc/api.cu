@@ -600,6 +600,40 @@ opt_status opt_mixed_step_clipped(const opt_muon_hp* hp_muon, const opt_adamw_hp
   return mixed_impl(hp_muon, hp_adamw, tensors, n, OPT_KIND_AUTO, workspace, workspace_bytes, stream, &clip);
 }
 
+opt_status opt_reload_model_params(const opt_tensor* tensors, int32_t n, void* stream) {
+  if (n < 0 || (n > 0 && !tensors)) return OPT_ERR_INVALID_ARG;
+  for (int32_t i = 0; i < n; ++i) {
+    const opt_tensor& t = tensors[i];
+    if (t.rows < 0 || t.cols < 0) return OPT_ERR_INVALID_ARG;
+    if (t.rows > 0 && t.cols > (INT64_MAX / t.rows)) return OPT_ERR_INVALID_ARG;
+    if (t.rows * t.cols == 0 || !t.model_param) continue;
+    if (!t.main_param) return OPT_ERR_INVALID_ARG;
+    if (check_fp32_ptr(t.main_param) != OPT_OK || (reinterpret_cast<uintptr_t>(t.model_param) & 1u))
+      return OPT_ERR_MISALIGNED;
+  }
+  static thread_local ReloadBatch batch;
+  batch.n = 0;
+  batch.total_chunks = 0;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  for (int32_t i = 0; i <= n; ++i) {
+    const bool flush = (i == n) || batch.n == kReloadBatch;
+    if (flush && batch.n > 0) {
+      const cudaError_t e = launch_reload(batch, s);
+      if (e != cudaSuccess) return cuda_fail(e, "reload model params");
+      batch.n = 0;
+      batch.total_chunks = 0;
+    }
+    if (i == n) break;
+    const opt_tensor& t = tensors[i];
+    const int64_t numel = t.rows * t.cols;
+    if (numel == 0 || !t.model_param) continue;
+    batch.t[batch.n] = ReloadDesc{t.model_param, t.main_param, numel, batch.total_chunks};
+    batch.total_chunks += (numel + kAdamwChunk - 1) / kAdamwChunk;
+    ++batch.n;
+  }
+  return OPT_OK;
+}
+
 opt_status opt_newton_schulz(const float* G, float* O, int64_t rows, int64_t cols, int32_t ns_steps, float a,
                              float b, float c, float eps, void* workspace, size_t workspace_bytes, void* stream) {
   if (rows < 0 || cols < 0 || ns_steps < 0 || ns_steps > 16) return OPT_ERR_INVALID_ARG;

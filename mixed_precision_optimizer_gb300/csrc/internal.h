@@ -173,6 +173,25 @@ cudaError_t launch_grad_sumsq(const NormBatch& batch, float* partials, cudaStrea
 cudaError_t launch_clip_finalize(const float* partials, int64_t n_partials, float max_norm, float* scale_out,
                                  float* norm_out, float* user_scale, float* user_norm, cudaStream_t stream);
 
+// ------------------------------------------------------------ lifecycle ----
+
+constexpr int kReloadBatch = 900;
+struct ReloadDesc {
+  const uint16_t* src;   // bf16 model parameter
+  float* dst;            // fp32 main_param
+  int64_t numel;
+  int64_t chunk_begin;
+};
+struct ReloadBatch {
+  int32_t n;
+  int32_t pad_;
+  int64_t total_chunks;
+  ReloadDesc t[kReloadBatch];
+};
+static_assert(sizeof(ReloadBatch) <= 32000, "kernel parameter space");
+
+cudaError_t launch_reload(const ReloadBatch& batch, cudaStream_t stream);
+
 int num_sms();   // SM count of the current device (cached per device)
 
 // Launch instrumentation (opt_profile_launches).  A launch site calls
