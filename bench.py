@@ -401,7 +401,7 @@ def run_ours(args, dist: Dist):
         # fp16 and bf16 share the dense tensor rate (nominal ratio 1), so the
         # measured bf16 figure is the fp16 peak
         peak = peaks["bf16_tflops_sustained"]
-        tr = kernel_traffic("ns_gemm")
+        tr = kernel_traffic("ns_gemm")   # mean DRAM bytes per GEMM launch of one step
         roofline = {"bound": "tensor", "kernel": "ns_gemm_kernel (fp16 x fp16 -> fp32: X X^T, A A, C X)",
                     "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
                     "frac": round(achieved / peak, 4), "traffic": tr,
@@ -419,8 +419,11 @@ def run_ours(args, dist: Dist):
                     "avg_launch_ms": round(k["ms"] / k["launches"], 4)}
     if "adamw" in kernels:
         k = kernels["adamw"]
-        roofline_adamw = {"bound": "hbm", "achieved": kern_out["adamw"]["gbs"], "peak": peaks["hbm_gbs"],
-                          "unit": "GB/s", "frac": round(kern_out["adamw"]["gbs"] / peaks["hbm_gbs"], 4)}
+        roofline_adamw = {"bound": "hbm", "kernel": "adamw_mta_kernel", "achieved": kern_out["adamw"]["gbs"],
+                          "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                          "frac": round(kern_out["adamw"]["gbs"] / peaks["hbm_gbs"], 4),
+                          "traffic": kernel_traffic("adamw"), "peak_source": f"{peak_src} hbm_gbs",
+                          "per_launch_bytes": round(k["elems"] * ADAMW_BYTES_PER_PARAM / k["launches"])}
     else:
         roofline_adamw = None
 
