@@ -427,6 +427,10 @@ def run_ours(args, dist: Dist):
     else:
         roofline_adamw = None
 
+    # ---- AdamW GB/s per size decade (the sweep workload reports it per bucket)
+    buckets = adamw_buckets(params, ha(t)) if w.name == "adamw_sweep_10k" else None
+    t += 1 if buckets else 0
+
     # ---- end to end through the public API with host buffers
     e2e = run_e2e(args, step, params, t, total, dist)
     t += args.e2e_steps
@@ -447,6 +451,7 @@ def run_ours(args, dist: Dist):
         "roofline": roofline,
         "roofline_adamw": roofline_adamw,
         "kernels": kern_out,
+        "adamw_gbs_by_size": buckets,
         "gpu_launches": launches,
         "e2e": e2e,
         "clocks": csum,
@@ -475,6 +480,34 @@ def pinned_host_buffers(shapes_dtypes):
         else:
             out.append(torch.empty(n, dtype=tdt, pin_memory=True))
     return out, registered
+
+
+def adamw_buckets(params, hp, reps=5):
+    """AdamW throughput (GB/s at 30 B/param) for the tensors of each size
+    decade [10^k, 10^(k+1)), each decade timed as its own multi-tensor launch
+    sequence with CUDA events."""
+    import math as _m
+    import torch
+    import mixed_precision_optimizer_gb300 as mp
+    groups = {}
+    for p in params:
+        n = p.main_param.numel()
+        groups.setdefault(int(_m.log10(n)) if n > 0 else 0, []).append(p)
+    out = {}
+    for k in sorted(groups):
+        g = groups[k]
+        n = sum(p.main_param.numel() for p in g)
+        mp.adamw_step(g, hp)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            mp.adamw_step(g, hp)
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / reps
+        out[f"1e{k}-1e{k + 1}"] = {"tensors": len(g), "params": n, "ms": round(ms, 4),
+                                   "gbs": round(n * ADAMW_BYTES_PER_PARAM / (ms * 1e-3) / 1e9, 1)}
+    return out
 
 
 def run_e2e(args, step_fn, params, t, total, dist: Dist):
