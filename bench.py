@@ -331,8 +331,9 @@ def run_ours(args, dist: Dist):
     total = n_muon + n_adamw
     ws = mp.alloc_workspace(mp.workspace_size(params, clip=args.clip > 0), device)
     hm, ha = hyper(w)
+    prepared = mp.prepare(params)
 
-    def step(t, plist=params):
+    def step(t, plist=prepared):
         if args.clip > 0:
             mp.mixed_step_clipped(plist, hm, ha(t), args.clip, ws)
         else:
@@ -484,8 +485,9 @@ def pinned_host_buffers(shapes_dtypes):
 
 def adamw_buckets(params, hp, reps=5):
     """AdamW throughput (GB/s at 30 B/param) for the tensors of each size
-    decade [10^k, 10^(k+1)), each decade timed as its own multi-tensor launch
-    sequence with CUDA events."""
+    decade [10^k, 10^(k+1)), each decade stepped as its own multi-tensor list
+    (marshalled once) and timed on the device by the library's launch events
+    (kernel time only)."""
     import math as _m
     import torch
     import mixed_precision_optimizer_gb300 as mp
@@ -495,17 +497,18 @@ def adamw_buckets(params, hp, reps=5):
         groups.setdefault(int(_m.log10(n)) if n > 0 else 0, []).append(p)
     out = {}
     for k in sorted(groups):
-        g = groups[k]
-        n = sum(p.main_param.numel() for p in g)
+        g = mp.prepare(groups[k], "adamw")
+        n = sum(p.main_param.numel() for p in groups[k])
         mp.adamw_step(g, hp)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        for _ in range(reps):
-            mp.adamw_step(g, hp)
-        e1.record()
+        prof = mp.LaunchProfiler(capacity=64 * reps)
+        with prof:
+            for _ in range(reps):
+                mp.adamw_step(g, hp)
         torch.cuda.synchronize()
-        ms = e0.elapsed_time(e1) / reps
-        out[f"1e{k}-1e{k + 1}"] = {"tensors": len(g), "params": n, "ms": round(ms, 4),
+        recs = prof.records()
+        ms = sum(r["ms"] for r in recs) / reps
+        out[f"1e{k}-1e{k + 1}"] = {"tensors": len(groups[k]), "params": n, "launches": len(recs) // reps,
+                                   "kernel_ms": round(ms, 4),
                                    "gbs": round(n * ADAMW_BYTES_PER_PARAM / (ms * 1e-3) / 1e9, 1)}
     return out
 
@@ -534,6 +537,7 @@ def run_e2e(args, step_fn, params, t, total, dist: Dist):
     # second device set of gradients and model copies
     sets = [params, [mp.Param(p.main_param, torch.empty_like(p.main_grad), p.exp_avg, p.exp_avg_sq,
                               torch.empty_like(p.model), p.embedding_or_output, p.kind) for p in params]]
+    prepared_sets = [mp.prepare(x) for x in sets]
     compute = torch.cuda.current_stream()
     s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
     E = lambda: torch.cuda.Event(enable_timing=True)
@@ -559,7 +563,7 @@ def run_e2e(args, step_fn, params, t, total, dist: Dist):
         compute.wait_event(h2d_done[k])
         if k >= 2:
             compute.wait_event(d2h_done[k - 2])       # model copy of set k % 2 read back
-        step_fn(t, cur)
+        step_fn(t, prepared_sets[k % 2])
         t += 1
         step_done[k].record(compute)
         with torch.cuda.stream(s_out):                 # model parameters of step k

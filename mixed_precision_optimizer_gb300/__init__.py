@@ -215,7 +215,29 @@ class Param:
         return out
 
 
-def _array(params: Sequence[Param], force=None):
+class Prepared:
+    """A parameter list marshalled once into the C descriptor array, for
+    callers that step the same tensors many times (the pointers must stay
+    valid: keep the tensors alive and do not reallocate them)."""
+
+    def __init__(self, params: Sequence[Param], force=None):
+        self.params = list(params)
+        self.force = force
+        self.array = (OptTensor * max(1, len(self.params)))()
+        for i, p in enumerate(self.params):
+            self.array[i] = p.to_c(force)
+
+    def __len__(self):
+        return len(self.params)
+
+
+def prepare(params: Sequence[Param], force=None) -> Prepared:
+    return Prepared(params, force)
+
+
+def _array(params, force=None):
+    if isinstance(params, Prepared):
+        return params.array
     arr = (OptTensor * max(1, len(params)))()
     for i, p in enumerate(params):
         arr[i] = p.to_c(force)
@@ -266,7 +288,8 @@ def _ws(workspace):
     return ctypes.c_void_p(workspace.data_ptr()), workspace.numel() * workspace.element_size()
 
 
-def adamw_step(params: Sequence[Param], hp: OptAdamwHP, workspace=None, stream=None):
+def adamw_step(params, hp: OptAdamwHP, workspace=None, stream=None):
+    """params: a list of Param or a Prepared list (marshalled once)."""
     arr = _array(params, "adamw")
     w, nb = _ws(workspace)
     _check(lib().opt_adamw_step(ctypes.byref(hp), arr, len(params), w, nb, _stream(stream)), "opt_adamw_step")
@@ -278,7 +301,7 @@ def muon_step(param: Param, hp: OptMuonHP, workspace, stream=None):
     _check(lib().opt_muon_step(ctypes.byref(hp), arr, w, nb, _stream(stream)), "opt_muon_step")
 
 
-def mixed_step(params: Sequence[Param], hp_muon: Optional[OptMuonHP], hp_adamw: Optional[OptAdamwHP],
+def mixed_step(params, hp_muon: Optional[OptMuonHP], hp_adamw: Optional[OptAdamwHP],
                workspace, stream=None):
     arr = _array(params)
     w, nb = _ws(workspace)
@@ -287,7 +310,7 @@ def mixed_step(params: Sequence[Param], hp_muon: Optional[OptMuonHP], hp_adamw: 
                                 arr, len(params), w, nb, _stream(stream)), "opt_mixed_step")
 
 
-def mixed_step_clipped(params: Sequence[Param], hp_muon: Optional[OptMuonHP], hp_adamw: Optional[OptAdamwHP],
+def mixed_step_clipped(params, hp_muon: Optional[OptMuonHP], hp_adamw: Optional[OptAdamwHP],
                        max_norm: float, workspace, total_norm_out=None, clip_scale_out=None, stream=None):
     """mixed_step with global gradient-norm clipping; the optional outputs are
     1-element fp32 CUDA tensors receiving the norm and the factor applied."""

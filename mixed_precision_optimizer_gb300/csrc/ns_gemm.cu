@@ -20,15 +20,16 @@
 // Kernel structure: CTA pairs (clusters of 2, one CTA per SM), persistent over
 // 256 x 256 output tiles, each pair computing a tile with cta_group::2 MMAs:
 //   warp 0    TMA producer in both CTAs: this CTA's 128 rows of A and 128 rows
-//             of B per k-block, 128-byte swizzled, into a 6-stage ring; both
+//             of B per k-block, 128-byte swizzled, into a 5-stage ring; both
 //             CTAs' copies complete on the even CTA's barrier
 //   warp 1    TMEM allocator (both CTAs) and, in the even CTA, the MMA issuer:
 //             tcgen05.mma.cta_group::2 M=256 N=256, 4 MMAs per 128-byte
 //             k-block, commits multicast to both CTAs to free the stage; a
 //             2 x 256-column accumulator per CTA lets the epilogue of one tile
 //             overlap the main loop of the next
-//   warps 2-5 epilogue in both CTAs: tcgen05.ld of this CTA's 128 rows, 32
-//             columns at a time, fused math, stores; each warp transposes
+//   warps 2-9 epilogue in both CTAs: two warps per TMEM lane quarter, each
+//             taking 128 of the 256 columns of this CTA's 128 rows, 32 at a
+//             time (tcgen05.ld), fused math, stores; each warp transposes
 //             32 x 32 blocks through its own shared-memory slab
 // Per MMA each SM stages 8 KB of operands (A and B halves) instead of the
 // 12 KB a single-CTA 128 x 256 tile needs.
@@ -56,15 +57,16 @@ constexpr int BM = 128;                       // rows of the tile held by one CT
 constexpr int BM_PAIR = 256;                  // rows of the tile of a CTA pair (MMA M)
 constexpr int BN = 256;                       // columns of the tile (MMA N)
 constexpr int BN_HALF = 128;                  // B rows staged by one CTA
-constexpr int kStages = 6;
+constexpr int kStages = 5;
 constexpr int kRowBytes = 128;                 // one swizzle row per k-block
 constexpr int kStageA = BM * kRowBytes;        // 16 KB: this CTA's 128 rows of A
 constexpr int kStageB = BN_HALF * kRowBytes;   // 16 KB: this CTA's 128 rows of B
 constexpr int kStageBytes = kStageA + kStageB; // per CTA; the pair's stage is twice this
-constexpr int kThreads = 192;
+constexpr int kEpiWarps = 8;                   // two warps per TMEM lane quarter
+constexpr int kThreads = 64 + 32 * kEpiWarps;  // TMA warp, MMA warp, epilogue warps
 constexpr int kTmemCols = 512;                 // 2 accumulators x 256 fp32 columns
 constexpr int kSlabWords = 32 * 33;            // per epilogue warp: 32 x 32 fp32, padded rows
-constexpr int kSlabBytes = 4 * kSlabWords * 4;
+constexpr int kSlabBytes = kEpiWarps * kSlabWords * 4;
 constexpr uint32_t kSmemBytes = kStages * kStageBytes + kSlabBytes + 1024 /*align*/ + 256 /*barriers*/;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 
@@ -432,7 +434,7 @@ ns_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(smem_u32(&acc_full[a]), 1);
-      mbar_init(smem_u32(&acc_empty[a]), 2 * 128);
+      mbar_init(smem_u32(&acc_empty[a]), 2 * 32 * kEpiWarps);
     }
     mbar_init(smem_u32(drain), 1);
     *abort_flag = 0u;
@@ -529,6 +531,7 @@ ns_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
   } else {
     // ------------------------------------------------------ epilogue --
     const int quarter = warp & 3;             // TMEM lanes this warp may access
+    const int half = (warp - 2) >> 2;         // which 128 of the 256 columns
     float* slab = slabs + (warp - 2) * kSlabWords;
     const uint32_t empty_even = peer_addr(smem_u32(&acc_empty[0]), 0);
     int lt = 0;
@@ -539,7 +542,7 @@ ns_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
       const Tile t = decode_tile(P, tile);
       const int row0 = t.tm * BM_PAIR + static_cast<int>(rank) * BM + quarter * 32;
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * BN;
-      for (int c0 = 0; c0 < BN; c0 += 32) {
+      for (int c0 = half * (BN / 2); c0 < (half + 1) * (BN / 2); c0 += 32) {
         float v[32];
         __syncwarp();
         tmem_ld32(taddr + c0, v);
