@@ -441,7 +441,9 @@ def run_ours(args, dist: Dist):
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": dist.world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(elapsed_ms / args.steps, 3), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f32 (master, state, AdamW); Newton-Schulz fp16 x fp16 -> f32 on tensor cores",
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "dtype_detail": "fp32 master weights, gradients, state and AdamW arithmetic; Newton-Schulz GEMMs take fp16 "
+                        "operands with fp32 accumulation on the tensor cores; bf16 model writeback",
         "data": "synthetic (seeded, drawn on the GPU)",
         "config": {"workload": w.name, "params": total, "grad_clip_max_norm": args.clip if args.clip > 0 else None, "muon_params": n_muon, "adamw_params": n_adamw,
                    "tensors": len(w.tensors), "parallelism": f"replicas x{dist.world}" if dist.world > 1 else "1 GPU",
@@ -604,7 +606,8 @@ def run_reference(args, dist: Dist):
     value = total / t_step
     return {"metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": dist.world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(t_step * 1e3, 1), "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f32 AdamW / f64 Newton-Schulz (CPU oracle)",
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "dtype_detail": "CPU oracle: fp32 AdamW in literal operation order, fp64 Muon and Newton-Schulz",
             "data": "synthetic (seeded)", "impl": "reference",
             "config": {"workload": w.name, "params": total, "grad_clip_max_norm": args.clip if args.clip > 0 else None, "parallelism": "CPU oracle on rank 0"},
             "cpu_baseline": {"value": round(value, 1), "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
