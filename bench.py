@@ -304,6 +304,7 @@ def cpu_oracle_sample(w: S.Workload, budget_s=20.0):
         notes.append("Muon fp64 oracle on one " + ", one ".join(f"{a}x{b}" for a, b in measured)
                      + (" matrix; larger shapes extrapolated by Newton-Schulz flop count"
                         if len(measured) < len(shapes) else " matrix"))
+    notes.append(f"numpy elementwise on 1 thread, BLAS matmul on up to {cpu_threads()} threads")
     return t_total, "; ".join(notes)
 
 
