@@ -59,6 +59,14 @@ def test_clock_summary_parsing(tmp_path):
     cs.proc = object()
     s = cs.summary()
     assert s["sm_mhz"] == 1925.0 and s["sm_max_mhz"] == 2070.0 and s["reasons"] == ["sw_power_cap"]
+    assert "mem_mhz" not in s
+    # with the memory clock and temperature columns
+    with open(cs.path, "w") as f:
+        f.write("0, 1900, 2070, 900.5, 0x0, Not Active, Not Active, Not Active, Active, 3996, 61\n")
+        f.write("0, 1700, 2070, 1000.0, 0x0, Not Active, Active, Not Active, Not Active, 3996, 74\n")
+    s = cs.summary()
+    assert s["sm_mhz"] == 1800.0 and s["mem_mhz"] == 3996.0 and s["temp_c_max"] == 74.0
+    assert s["reasons"] == ["hw_thermal_slowdown", "sw_power_cap"]
 
 
 def test_smi_index(monkeypatch):
