@@ -5,7 +5,8 @@
 // X (A x B, A <= B), X' = a X + (b A + c A A) X with A = X X^T, is computed as
 // three GEMMs with fused epilogues, all fp16 x fp16 -> fp32 (TMEM):
 //
-//   gram : A = X X^T                        -> A fp32 (for b A), A fp16 (operand)
+//   gram : A = X X^T                        -> A fp32 on and below the diagonal blocks
+//                                              (for b A), A fp16 in full (operand)
 //   poly : C = a I + b A + c (A A)          -> C fp16
 //   bx   : X' = C X                         -> X' fp16, X'^T fp16 (next operands)
 //          (last iteration: W <- W (1 - lr*lambda) - lr*0.2*sqrt(max(A,B)) * X',
@@ -144,12 +145,18 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
 // Tile load into this CTA's shared memory; completion is signalled on `bar`,
 // a shared::cluster address that may be the even CTA's barrier.
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x,
-                                            int y, int z) {
+                                            int y, int z, uint64_t policy) {
   asm volatile(
-      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar), "l"(policy)
       : "memory");
+}
+
+__device__ __forceinline__ uint64_t l2_evict_last_policy() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
 }
 
 // Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of
@@ -327,13 +334,14 @@ __device__ __forceinline__ void epilogue_block(const GemmParams& P, const MuonGr
   const int row = row0 + lane;
   float w[32];
   if (P.mode == kGram) {
+    // fp32 A only on and below the diagonal blocks (the only blocks the poly
+    // stage reads for its b A term); the fp16 operand in full.
     float* Am = P.Af + static_cast<int64_t>(t.mat) * Ap * Ap;
     uint16_t* Ahm = P.Ah + static_cast<int64_t>(t.mat) * Ap * Ap;
     store_f32x32(Am + static_cast<int64_t>(row) * Ap + col0, v);
     store_f16x32(Ahm + static_cast<int64_t>(row) * Ap + col0, v);
     if (t.mirror) {
       warp_transpose(slab, lane, v, w);   // lane now holds column col0 + lane, rows row0..row0+31
-      store_f32x32(Am + static_cast<int64_t>(col0 + lane) * Ap + row0, w);
       store_f16x32(Ahm + static_cast<int64_t>(col0 + lane) * Ap + row0, w);
     }
   } else if (P.mode == kPoly) {
@@ -341,7 +349,7 @@ __device__ __forceinline__ void epilogue_block(const GemmParams& P, const MuonGr
     uint16_t* Cm = P.Ch + static_cast<int64_t>(t.mat) * Ap * Ap;
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
-      const float4 a4 = reinterpret_cast<const float4*>(Arow)[q];
+      const float4 a4 = __ldcs(reinterpret_cast<const float4*>(Arow) + q);
       v[4 * q + 0] = P.b * a4.x + P.c * v[4 * q + 0];
       v[4 * q + 1] = P.b * a4.y + P.c * v[4 * q + 1];
       v[4 * q + 2] = P.b * a4.z + P.c * v[4 * q + 2];
@@ -385,17 +393,17 @@ __device__ __forceinline__ void epilogue_block(const GemmParams& P, const MuonGr
       if (P.ns_only) {
 #pragma unroll
         for (int j = 0; j < 32; ++j)
-          if (j < n_runs) M.O[first + j * C] = w[j];
+          if (j < n_runs) __stcs(M.O + first + j * C, w[j]);
       } else {
         float old[32];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) old[j] = (j < n_runs) ? M.W[first + j * C] : 0.f;
+        for (int j = 0; j < 32; ++j) old[j] = (j < n_runs) ? __ldcs(M.W + first + j * C) : 0.f;
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
           if (j < n_runs) {
             const float wv = old[j] * P.decay - M.step_scale * w[j];
-            M.W[first + j * C] = wv;
-            if (M.Wb) M.Wb[first + j * C] = bf16_rne(wv);
+            __stcs(M.W + first + j * C, wv);
+            if (M.Wb) __stcs(M.Wb + first + j * C, bf16_rne(wv));
           }
         }
       }
@@ -465,6 +473,7 @@ ns_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
       uint32_t it = 0;
       bool ok = true;
       bool issued = false;
+      const uint64_t policy = l2_evict_last_policy();
       for (int tile = pair; ok && tile < P.total_tiles; tile += npairs) {
         const Tile t = decode_tile(P, tile);
         const int arow = t.tm * BM_PAIR + static_cast<int>(rank) * BM;
@@ -478,8 +487,8 @@ ns_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
           const uint32_t fb = peer_addr(smem_u32(&full[s]), 0);
           if (rank == 0) mbar_expect_tx(smem_u32(&full[s]), 2 * kStageBytes);
           const int kx = kb * kElemsPerKBlock;
-          tma_load_3d(smem_u32(stage_a + s * kStageA), &map_a, fb, kx, arow, t.mat);
-          tma_load_3d(smem_u32(stage_b + s * kStageB), &map_b, fb, kx, brow, t.mat);
+          tma_load_3d(smem_u32(stage_a + s * kStageA), &map_a, fb, kx, arow, t.mat, policy);
+          tma_load_3d(smem_u32(stage_b + s * kStageB), &map_b, fb, kx, brow, t.mat, policy);
           issued = true;
         }
       }
