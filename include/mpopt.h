@@ -182,8 +182,8 @@ typedef struct {
 /*
  * Bytes of device workspace that opt_mixed_step (and the other steps) need for
  * this tensor list: a 256-byte status header and the Newton-Schulz buffers of
- * the largest group of same-shape Muon matrices (the fp16 iterate, its fp16
- * transpose twice, the Gram matrix in fp32 and fp16, the fp16 polynomial
+ * the largest group of same-shape Muon matrices (the fp16 iterate twice, as a
+ * ping-pong pair, the Gram matrix in fp32 and fp16, the fp16 polynomial
  * a I + b A + c A A, norm partials).  Shapes are padded to multiples of 256.
  * AdamW needs no workspace: 0 for a list without Muon tensors.
  * `routing` selects how kinds are interpreted: OPT_KIND_AUTO as in
@@ -270,7 +270,7 @@ MPOPT_API opt_status opt_newton_schulz(const float* G, float* O, int64_t rows, i
  * and gives extensions no allocator, or a path whose memory budget is fixed in
  * advance.  No counterpart on the pages: this is an interface convenience, the
  * arithmetic is exactly opt_newton_schulz's.
- *   - Scratch is a 32 MiB array of device memory built into the library (a
+ *   - Scratch is a 24 MiB array of device memory built into the library (a
  *     static __device__ array).  Every GPU that loads the library holds it until
  *     the process exits.  This entry point calls no cudaMalloc, cudaFree or
  *     other allocating routine.

@@ -86,8 +86,7 @@ struct MuonGroup {
 // Workspace buffers of one group (all device pointers into the workspace).
 // Newton-Schulz operands are fp16 (kind::f16 tensor cores); accumulation fp32.
 struct NsBuffers {
-  uint16_t* Xh;      // fp16 iterate            [count][Ap][Bp]
-  uint16_t* Xt[2];   // fp16 transposed iterate [count][Bp][Ap], ping-pong
+  uint16_t* Xh[2];   // fp16 iterate            [count][Ap][Bp], ping-pong
   float* Af;         // fp32 Gram matrix        [count][Ap][Ap]
   uint16_t* Ah;      // fp16 Gram matrix        [count][Ap][Ap]
   uint16_t* Ch;      // fp16 a I + b A + c A A  [count][Ap][Ap]

@@ -12,8 +12,8 @@
 // of gtilde^2 in a fixed order; muon_norm_kernel reduces them in double to
 // 1/(||gtilde||_F + eps).  Pass 2 (muon_operand_kernel) recomputes gtilde from
 // g and the new m (the same arithmetic, so the same values), scales it, and
-// writes the fp16 operands in both orientations -- X0 (rows = min side) for
-// X X^T and X0^T for the B X product -- into the zero-padded workspace.
+// writes the fp16 operand X0 in the wide orientation (rows = min side) into the
+// zero-padded workspace; both X X^T and C X read that one copy.
 // Normalising before the fp16 conversion keeps every operand in [-1.3, 1.3].
 
 #include <cuda_fp16.h>
@@ -120,11 +120,11 @@ __global__ void muon_norm_kernel(NsBuffers buf, int64_t blocks_per_mat, float ep
 }
 
 // grid: (operand tiles per matrix, matrices); one 64 x 64 tile of the padded
-// W-layout space per block.  Writes the fp16 operand in W layout directly and
-// in the other layout through a shared-memory transpose.  Each thread moves 4
+// W-layout space per block.  Writes the fp16 operand X0 in the wide layout
+// [Ap][Bp]: directly when W is wide, through a shared-memory transpose when W
+// is tall (stored as the transpose of the wide layout).  Each thread moves 4
 // consecutive elements per step: a 16-byte load of g and of m (when the rows
-// are 16-byte aligned, else four scalar loads) and an 8-byte store of 4 fp16
-// on both sides.
+// are 16-byte aligned, else four scalar loads) and an 8-byte store of 4 fp16.
 __global__ void __launch_bounds__(kThreads)
 muon_operand_kernel(const MuonGroup grp, NsBuffers buf, MuonScalars s) {
   __shared__ uint16_t tile[kPrepTile][kPrepTile + 2];   // odd word stride: few bank conflicts
@@ -142,12 +142,7 @@ muon_operand_kernel(const MuonGroup grp, NsBuffers buf, MuonScalars s) {
   const int lc = (threadIdx.x % 16) * 4;       // first of 4 columns
   const int lr0 = threadIdx.x / 16;            // 0..15
   const bool vec = M.vec4 && (C % 4 == 0);     // every row start 16-byte aligned
-  uint16_t* Xh = buf.Xh + static_cast<int64_t>(mat) * Ap * Bp;   // [Ap][Bp]
-  uint16_t* Xt = buf.Xt[0] + static_cast<int64_t>(mat) * Ap * Bp; // [Bp][Ap]
-  uint16_t* direct = tr ? Xt : Xh;             // the operand stored in W layout
-  const int64_t direct_ld = tr ? Ap : Bp;
-  uint16_t* other = tr ? Xh : Xt;              // the operand stored transposed
-  const int64_t other_ld = tr ? Bp : Ap;
+  uint16_t* Xh = buf.Xh[0] + static_cast<int64_t>(mat) * Ap * Bp;   // [Ap][Bp]
 #pragma unroll
   for (int k = 0; k < kPrepTile / 16; ++k) {
     const int lr = lr0 + 16 * k;
@@ -170,23 +165,27 @@ muon_operand_kernel(const MuonGroup grp, NsBuffers buf, MuonScalars s) {
       }
     }
     const uint16_t h0 = f16_bits(val[0]), h1 = f16_bits(val[1]), h2 = f16_bits(val[2]), h3 = f16_bits(val[3]);
-    tile[lr][lc + 0] = h0;
-    tile[lr][lc + 1] = h1;
-    tile[lr][lc + 2] = h2;
-    tile[lr][lc + 3] = h3;
-    const uint2 packed = make_uint2(static_cast<uint32_t>(h0) | (static_cast<uint32_t>(h1) << 16),
-                                    static_cast<uint32_t>(h2) | (static_cast<uint32_t>(h3) << 16));
-    *reinterpret_cast<uint2*>(direct + r * direct_ld + c) = packed;
+    if (tr) {
+      tile[lr][lc + 0] = h0;
+      tile[lr][lc + 1] = h1;
+      tile[lr][lc + 2] = h2;
+      tile[lr][lc + 3] = h3;
+    } else {
+      *reinterpret_cast<uint2*>(Xh + r * Bp + c) =
+          make_uint2(static_cast<uint32_t>(h0) | (static_cast<uint32_t>(h1) << 16),
+                     static_cast<uint32_t>(h2) | (static_cast<uint32_t>(h3) << 16));
+    }
   }
+  if (!tr) return;   // uniform per block
   __syncthreads();
-  // transposed side: output row i (= W column c0 + i) gets W rows r0 .. r0 + 63
+  // tall W: wide row i (= W column c0 + i) gets W rows r0 .. r0 + 63
 #pragma unroll
   for (int k = 0; k < kPrepTile / 16; ++k) {
     const int i = lr0 + 16 * k;
     const int j = lc;
     const uint2 packed = make_uint2(static_cast<uint32_t>(tile[j][i]) | (static_cast<uint32_t>(tile[j + 1][i]) << 16),
                                     static_cast<uint32_t>(tile[j + 2][i]) | (static_cast<uint32_t>(tile[j + 3][i]) << 16));
-    *reinterpret_cast<uint2*>(other + (c0 + i) * other_ld + r0 + j) = packed;
+    *reinterpret_cast<uint2*>(Xh + (c0 + i) * Bp + r0 + j) = packed;
   }
 }
 

@@ -8,7 +8,8 @@
 //   gram : A = X X^T                        -> A fp32 on and below the diagonal blocks
 //                                              (for b A), A fp16 in full (operand)
 //   poly : C = a I + b A + c (A A)          -> C fp16
-//   bx   : X' = C X                         -> X' fp16, X'^T fp16 (next operands)
+//   bx   : X' = C X                         -> X' fp16 (next iterate; C X reads X
+//                                              itself as an MN-major B operand)
 //          (last iteration: W <- W (1 - lr*lambda) - lr*0.2*sqrt(max(A,B)) * X',
 //           from the fp32 accumulator, in W's own orientation, with its bf16 copy)
 //
@@ -63,6 +64,7 @@ constexpr int kRowBytes = 128;                 // one swizzle row per k-block
 constexpr int kStageA = BM * kRowBytes;        // 16 KB: this CTA's 128 rows of A
 constexpr int kStageB = BN_HALF * kRowBytes;   // 16 KB: this CTA's 128 rows of B
 constexpr int kStageBytes = kStageA + kStageB; // per CTA; the pair's stage is twice this
+constexpr int kMnBlockBytes = 64 * kRowBytes;   // MN-major B: one 64-column block of 64 K rows
 constexpr int kEpiWarps = 8;                   // two warps per TMEM lane quarter
 constexpr int kThreads = 64 + 32 * kEpiWarps;  // TMA warp, MMA warp, epilogue warps
 constexpr int kTmemCols = 512;                 // 2 accumulators x 256 fp32 columns
@@ -82,8 +84,7 @@ struct GemmParams {
   float* Af;            // gram: out; poly: in (b A term)
   uint16_t* Ah;         // gram: out (fp16 operand of A A)
   uint16_t* Ch;         // poly: out
-  uint16_t* Xh;         // bx: fp16 iterate out
-  uint16_t* Xt_out;     // bx: fp16 transposed iterate out
+  uint16_t* Xh;         // bx: fp16 iterate out (the other buffer of the pair)
   float a, b, c;
   float decay;
   int ns_only;
@@ -145,18 +146,12 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
 // Tile load into this CTA's shared memory; completion is signalled on `bar`,
 // a shared::cluster address that may be the even CTA's barrier.
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x,
-                                            int y, int z, uint64_t policy) {
+                                            int y, int z) {
   asm volatile(
-      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
-      " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar), "l"(policy)
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
       : "memory");
-}
-
-__device__ __forceinline__ uint64_t l2_evict_last_policy() {
-  uint64_t p;
-  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
-  return p;
 }
 
 // Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of
@@ -171,20 +166,35 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr) {
   return d;
 }
 
-// Instruction descriptor for kind::f16: fp32 accumulator (bits 4-5 = 1), A and
-// B fp16 (format 0 in bits 7-9 and 10-12), both K-major, N = 256 (bits 17-22,
-// N >> 3), M = 256 across the CTA pair (bits 24-28, M >> 4).
-__host__ __device__ constexpr uint32_t instr_desc() {
-  return (1u << 4) | (0u << 7) | (0u << 10) | (static_cast<uint32_t>(BN >> 3) << 17) |
-         (static_cast<uint32_t>(BM_PAIR >> 4) << 24);
+// Shared-memory matrix descriptor: MN-major operand, 128-byte swizzle.  The
+// tile is stored as 64-element (128-byte) wide column blocks, each 64 K rows
+// of 128 bytes: 8-row groups 1024 bytes apart (stride byte offset) and column
+// blocks 8192 bytes apart (leading byte offset).
+__device__ __forceinline__ uint64_t smem_desc_mn(uint32_t addr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((addr & 0x3FFFFu) >> 4);   // start address
+  d |= static_cast<uint64_t>(kMnBlockBytes >> 4) << 16;  // leading byte offset: next 64 columns
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;           // stride byte offset: next 8 K rows
+  d |= static_cast<uint64_t>(1) << 46;                   // descriptor version
+  d |= static_cast<uint64_t>(2) << 61;                   // 128-byte swizzle
+  return d;
 }
 
-// Pair MMA, issued by the even CTA: D[256 x 256] (+)= A[256 x 16] B[256 x 16]^T
-// with A's rows 0-127 / 128-255 and B's rows 0-127 / 128-255 in the shared
+// Instruction descriptor for kind::f16: fp32 accumulator (bits 4-5 = 1), A and
+// B fp16 (format 0 in bits 7-9 and 10-12), A K-major, B K-major or MN-major
+// (bit 16), N = 256 (bits 17-22, N >> 3), M = 256 across the CTA pair
+// (bits 24-28, M >> 4).
+__host__ __device__ constexpr uint32_t instr_desc(bool b_mn_major) {
+  return (1u << 4) | (0u << 7) | (0u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
+         (static_cast<uint32_t>(BN >> 3) << 17) | (static_cast<uint32_t>(BM_PAIR >> 4) << 24);
+}
+
+// Pair MMA, issued by the even CTA: D[256 x 256] (+)= A[256 x 16] B[16 x 256]
+// with A's rows 0-127 / 128-255 and B's columns 0-127 / 128-255 in the shared
 // memory of the even / odd CTA at the descriptors' offsets; each CTA's TMEM
 // receives its own 128 rows of D.
-__device__ __forceinline__ void mma(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t accumulate) {
-  constexpr uint32_t idesc = instr_desc();
+__device__ __forceinline__ void mma(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                    uint32_t accumulate) {
   asm volatile(
       "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
       " tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(tmem_d),
@@ -364,8 +374,6 @@ __device__ __forceinline__ void epilogue_block(const GemmParams& P, const MuonGr
     }
   } else if (P.mode == kBx) {
     store_f16x32(P.Xh + static_cast<int64_t>(t.mat) * Ap * Bp + static_cast<int64_t>(row) * Bp + col0, v);
-    warp_transpose(slab, lane, v, w);
-    store_f16x32(P.Xt_out + static_cast<int64_t>(t.mat) * Ap * Bp + static_cast<int64_t>(col0 + lane) * Ap + row0, w);
   } else {
     // last iteration: O = X' in the wide orientation (rows: A index, columns: B index).
     // The warp updates 32 runs of 32 consecutive W elements: for a tall W
@@ -434,6 +442,9 @@ ns_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
   const int lane = threadIdx.x & 31;
   const uint32_t rank = cluster_rank();      // 0: even CTA (issues the MMAs), 1: odd CTA
   const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+  // C X takes X [K = Ap][N = Bp] as an MN-major B operand; the symmetric
+  // products take K-major rows for both operands
+  const bool b_mn = P.mode == kBx || P.mode == kBxFinal;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -473,11 +484,10 @@ ns_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
       uint32_t it = 0;
       bool ok = true;
       bool issued = false;
-      const uint64_t policy = l2_evict_last_policy();
       for (int tile = pair; ok && tile < P.total_tiles; tile += npairs) {
         const Tile t = decode_tile(P, tile);
         const int arow = t.tm * BM_PAIR + static_cast<int>(rank) * BM;
-        const int brow = t.tn * BN + static_cast<int>(rank) * BN_HALF;
+        const int brow = t.tn * BN + static_cast<int>(rank) * BN_HALF;   // B rows (K-major) or columns (MN-major)
         for (int kb = 0; kb < P.k_blocks; ++kb, ++it) {
           const uint32_t s = it % kStages, ph = (it / kStages) & 1u;
           if (!mbar_wait(smem_u32(&empty[s]), ph ^ 1u, abort_flag, P.status, kStatusTimeoutEmpty)) {
@@ -487,8 +497,14 @@ ns_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
           const uint32_t fb = peer_addr(smem_u32(&full[s]), 0);
           if (rank == 0) mbar_expect_tx(smem_u32(&full[s]), 2 * kStageBytes);
           const int kx = kb * kElemsPerKBlock;
-          tma_load_3d(smem_u32(stage_a + s * kStageA), &map_a, fb, kx, arow, t.mat, policy);
-          tma_load_3d(smem_u32(stage_b + s * kStageB), &map_b, fb, kx, brow, t.mat, policy);
+          tma_load_3d(smem_u32(stage_a + s * kStageA), &map_a, fb, kx, arow, t.mat);
+          if (b_mn) {
+            // MN-major B: this CTA's 128 columns as two 64-column blocks of 64 K rows
+            tma_load_3d(smem_u32(stage_b + s * kStageB), &map_b, fb, brow, kx, t.mat);
+            tma_load_3d(smem_u32(stage_b + s * kStageB + kMnBlockBytes), &map_b, fb, brow + 64, kx, t.mat);
+          } else {
+            tma_load_3d(smem_u32(stage_b + s * kStageB), &map_b, fb, kx, brow, t.mat);
+          }
           issued = true;
         }
       }
@@ -502,6 +518,7 @@ ns_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
   } else if (warp == 1) {
     if (lane == 0 && rank == 0) {
       // ------------------------------------- MMA issuer (even CTA only) --
+      const uint32_t idesc = b_mn ? instr_desc(true) : instr_desc(false);
       uint32_t it = 0;
       int lt = 0;
       bool ok = true;
@@ -523,8 +540,9 @@ ns_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
           const uint32_t a_addr = smem_u32(stage_a + s * kStageA);
           const uint32_t b_addr = smem_u32(stage_b + s * kStageB);
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {   // 4 MMAs of 32 bytes of K each
-            mma(d_tmem, smem_desc(a_addr + kk * 32), smem_desc(b_addr + kk * 32), (kb > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < 4; ++kk) {   // 4 MMAs of 16 K each: 32 bytes along a K-major row, 16 MN-major rows
+            const uint64_t bdesc = b_mn ? smem_desc_mn(b_addr + kk * 16 * kRowBytes) : smem_desc(b_addr + kk * 32);
+            mma(d_tmem, smem_desc(a_addr + kk * 32), bdesc, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
           }
           mma_commit_pair(smem_u32(&empty[s]));
         }
@@ -642,11 +660,14 @@ cudaError_t launch_ns_iteration(const MuonGroup& grp, const NsBuffers& buf, cons
   const int T = static_cast<int>(Ap / 256);
   cudaError_t e;
 
-  // gram: A = X X^T  (operands: fp16 X [Ap][Bp], K = Bp)
+  uint16_t* X = buf.Xh[it & 1];           // this iteration's iterate
+  uint16_t* X_next = buf.Xh[(it + 1) & 1];
+
+  // gram: A = X X^T  (operands: fp16 X [Ap][Bp], K = Bp, both K-major)
   {
     CUtensorMap ma, mb;
-    if ((e = make_map(&ma, buf.Xh, Bp, Ap, cnt, BM)) != cudaSuccess) return e;
-    if ((e = make_map(&mb, buf.Xh, Bp, Ap, cnt, BN_HALF)) != cudaSuccess) return e;
+    if ((e = make_map(&ma, X, Bp, Ap, cnt, BM)) != cudaSuccess) return e;
+    if ((e = make_map(&mb, X, Bp, Ap, cnt, BN_HALF)) != cudaSuccess) return e;
     GemmParams P = base;
     P.mode = kGram;
     P.k_blocks = static_cast<int>(Bp / 64);
@@ -676,19 +697,19 @@ cudaError_t launch_ns_iteration(const MuonGroup& grp, const NsBuffers& buf, cons
     prof_end(stream);
     if (e != cudaSuccess) return e;
   }
-  // bx: X' = C X  (operands: fp16 C [Ap][Ap], fp16 X^T [Bp][Ap], K = Ap)
+  // bx: X' = C X  (operands: fp16 C [Ap][Ap] K-major, fp16 X [Ap][Bp] MN-major
+  // in 64-column x 64-row boxes, K = Ap)
   {
     CUtensorMap ma, mb;
     if ((e = make_map(&ma, buf.Ch, Ap, Ap, cnt, BM)) != cudaSuccess) return e;
-    if ((e = make_map(&mb, buf.Xt[it & 1], Ap, Bp, cnt, BN_HALF)) != cudaSuccess) return e;
+    if ((e = make_map(&mb, X, Bp, Ap, cnt, 64)) != cudaSuccess) return e;
     GemmParams P = base;
     P.mode = (it == s.ns_steps - 1) ? kBxFinal : kBx;
     P.k_blocks = static_cast<int>(Ap / 64);
     P.tiles_m = static_cast<int>(Ap / BM_PAIR);
     P.tiles_per_mat = static_cast<int>((Ap / BM_PAIR) * (Bp / BN));
     P.total_tiles = P.tiles_per_mat * grp.count;
-    P.Xh = buf.Xh;
-    P.Xt_out = buf.Xt[(it + 1) & 1];
+    P.Xh = X_next;
     prof_begin(OPT_KERNEL_NS_BX, grp.count, grp.A, grp.B, stream);
     e = launch_gemm(ma, mb, P, grp, stream);
     prof_end(stream);
