@@ -263,6 +263,25 @@ def kernel_traffic(kernel_key):
     return float(m.group(1)) if m else None
 
 
+def tensor_pipe_active():
+    """ncu tensor-pipe utilisation (% of peak) of the three GEMM stages from the
+    committed full-set summary, if it was captured from the current ns_gemm.cu
+    source (else None): the algorithmic TFLOP/s count the symmetric stages' full
+    flops, and this shows what the tensor pipe actually did."""
+    path = os.path.join(ROOT, "profiles", "ns_gemm_llama_mlp_1layer.md")
+    try:
+        text = open(path, encoding="utf-8").read()
+    except OSError:
+        return None
+    src = open(os.path.join(ROOT, "mixed_precision_optimizer_gb300", "csrc", "ns_gemm.cu"), "rb").read()
+    sha = hashlib.sha256(src).hexdigest()[:16]
+    m = re.search(rf"^\| *tensor_pipe *\| *{sha} *\| *([0-9.]+) *\| *([0-9.]+) *\| *([0-9.]+) *\|", text, re.M)
+    if not m:
+        return None
+    return {"gram": float(m.group(1)), "poly": float(m.group(2)), "bx": float(m.group(3)),
+            "source": "profiles/ns_gemm_llama_mlp_1layer.md (ncu --set full, one-layer MLP case)"}
+
+
 # ------------------------------------------------------------ CPU oracle --
 
 def cpu_oracle_sample(w: S.Workload, budget_s=20.0):
@@ -416,6 +435,7 @@ def run_ours(args, dist: Dist):
                     "frac": round(achieved / peak, 4), "traffic": tr,
                     "peak_source": f"{peak_src} bf16_tflops_sustained x nominal fp16/bf16 ratio 1",
                     "executed_tflops": round(ex / (gemm_ms * 1e-3) / 1e12, 1),
+                    "tensor_pipe_active_pct": tensor_pipe_active(),
                     "per_launch_flops": round(fl / nl), "avg_launch_ms": round(gemm_ms / nl, 4)}
     else:
         k = kernels["adamw"]

@@ -96,3 +96,24 @@ def test_reference_arm_line():
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["unit"] == "params/s" and d["value"] > 0
     assert d["cpu_baseline"]["kind"] == "oracle" and d["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_profile_rows_apply_only_to_their_source(tmp_path, monkeypatch):
+    """traffic and tensor-pipe rows are used only while the kernel source has the
+    sha256 prefix they were captured from."""
+    import hashlib
+    csrc = tmp_path / "mixed_precision_optimizer_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    (tmp_path / "profiles").mkdir()
+    (csrc / "ns_gemm.cu").write_bytes(b"kernel v1")
+    (csrc / "adamw.cu").write_bytes(b"adamw v1")
+    sha = hashlib.sha256(b"kernel v1").hexdigest()[:16]
+    (tmp_path / "profiles" / "ncu_traffic.md").write_text(f"| ns_gemm | {sha} | 1.5e9 |\n| adamw | 0000000000000000 | 3e9 |\n")
+    (tmp_path / "profiles" / "ns_gemm_llama_mlp_1layer.md").write_text(f"| tensor_pipe | {sha} | 70.5 | 60.0 | 85.25 |\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.kernel_traffic("ns_gemm") == 1.5e9
+    assert bench.kernel_traffic("adamw") is None          # captured from another source
+    tp = bench.tensor_pipe_active()
+    assert (tp["gram"], tp["poly"], tp["bx"]) == (70.5, 60.0, 85.25)
+    (csrc / "ns_gemm.cu").write_bytes(b"kernel v2")       # source changed since the capture
+    assert bench.kernel_traffic("ns_gemm") is None and bench.tensor_pipe_active() is None
