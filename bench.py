@@ -53,6 +53,9 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=10,
                     help="steps of the end-to-end leg; its time includes filling and draining the copy pipeline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--compare-cublas", action="store_true",
+                    help="also time cuBLAS (torch.bmm, fp16) on the Newton-Schulz GEMM shapes of the largest "
+                         "Muon group, back to back for a few seconds each, for comparison only")
     ap.add_argument("--clip", type=float, default=0.0,
                     help="max_norm of global grad-norm clipping fused into the step (0: off)")
     return ap.parse_args()
@@ -246,6 +249,70 @@ def gemm_executed_flops(rec):
     if rec["kernel"] == "ns_poly":
         return c * T * (T + 1) * 2.0 * 128 * 256 * Ap
     return c * 2.0 * Ap * Ap * Bp
+
+
+def kernels_by_shape(recs):
+    """Per Newton-Schulz GEMM stage and Muon shape class (A x B, matrices per
+    launch): launches, ms per launch, and TFLOP/s algorithmic and executed."""
+    out = {}
+    for r in recs:
+        if not r["kernel"].startswith("ns_"):
+            continue
+        k = out.setdefault(f"{r['kernel']} {r['a']}x{r['b']} x{r['count']}", dict(launches=0, ms=0.0, flops=0.0, ex=0.0))
+        k["launches"] += 1
+        k["ms"] += r["ms"]
+        k["flops"] += gemm_flops(r)
+        k["ex"] += gemm_executed_flops(r)
+    return {name: {"launches": k["launches"], "ms_per_launch": round(k["ms"] / k["launches"], 4),
+                   "tflops_algorithmic": round(k["flops"] / (k["ms"] * 1e-3) / 1e12, 1),
+                   "tflops_executed": round(k["ex"] / (k["ms"] * 1e-3) / 1e12, 1)}
+            for name, k in sorted(out.items())}
+
+
+def cublas_same_shapes(w, seconds=3.0):
+    """cuBLAS (torch.bmm, fp16 in and out, fp32 accumulation) on the three GEMMs
+    of one Newton-Schulz iteration of the largest Muon group, each run back to
+    back for `seconds` and timed with CUDA events; the symmetric products are
+    computed in full, as a library GEMM does.  For comparison only: this is
+    not the optimizer step."""
+    import torch
+    groups = {}
+    for sp in w.tensors:
+        if is_muon(w, sp):
+            A, B = sorted(sp.shape)
+            groups[(A, B)] = groups.get((A, B), 0) + 1
+    if not groups:
+        return None
+    (A, B), n = max(groups.items(), key=lambda kv: kv[1] * kv[0][0] * kv[0][0] * kv[0][1])
+    n = min(n, 64)
+    g = torch.Generator(device="cuda")
+    g.manual_seed(0)
+    X = (torch.randn(n, A, B, device="cuda", generator=g) * 0.01).half()
+    C = (torch.randn(n, A, A, device="cuda", generator=g) * 0.01).half()
+    out_x = torch.empty(n, A, B, device="cuda", dtype=torch.half)
+    out_a = torch.empty(n, A, A, device="cuda", dtype=torch.half)
+    res = {"shape": f"{n} x ({A} x {B})", "note": "full products; fp16 operands and output"}
+    for name, fn, flops in (("C X", lambda: torch.bmm(C, X, out=out_x), 2.0 * n * A * A * B),
+                            ("X X^T", lambda: torch.bmm(X, X.transpose(1, 2), out=out_a), 2.0 * n * A * A * B),
+                            ("A A", lambda: torch.bmm(C, C, out=out_a), 2.0 * n * A * A * A)):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        k, t0 = 0, time.perf_counter()
+        e0.record()
+        while time.perf_counter() - t0 < seconds:
+            fn()
+            k += 1
+            if k % 4 == 0:
+                torch.cuda.synchronize()
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / k
+        res[name] = {"ms_per_launch": round(ms, 3), "tflops": round(flops / (ms * 1e-3) / 1e12, 1)}
+    del X, C, out_x, out_a
+    torch.cuda.empty_cache()
+    return res
 
 
 def kernel_traffic(kernel_key):
@@ -482,11 +549,17 @@ def run_ours(args, dist: Dist):
         "roofline": roofline,
         "roofline_adamw": roofline_adamw,
         "kernels": kern_out,
+        "kernels_by_shape": kernels_by_shape(recs),
         "adamw_gbs_by_size": buckets,
         "gpu_launches": launches,
         "e2e": e2e,
         "clocks": csum,
     }
+    if args.compare_cublas and dist.rank == 0:
+        with ClockSampler(smi_index(device.index), "_cublas") as cclocks:
+            line["cublas_same_shapes"] = cublas_same_shapes(w)
+        if line["cublas_same_shapes"] is not None:
+            line["cublas_same_shapes"]["clocks"] = cclocks.summary()
     if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
         t_cpu, sample = cpu_oracle_sample(w)
         line["cpu_baseline"] = {"value": round(total / t_cpu, 1), "unit": UNIT, "cores": cpu_threads(),

@@ -117,3 +117,17 @@ def test_profile_rows_apply_only_to_their_source(tmp_path, monkeypatch):
     assert (tp["gram"], tp["poly"], tp["bx"]) == (70.5, 60.0, 85.25)
     (csrc / "ns_gemm.cu").write_bytes(b"kernel v2")       # source changed since the capture
     assert bench.kernel_traffic("ns_gemm") is None and bench.tensor_pipe_active() is None
+
+
+def test_kernels_by_shape_groups_stages_and_classes():
+    recs = [dict(kernel="ns_gram", count=48, a=4096, b=14336, ms=7.5),
+            dict(kernel="ns_gram", count=48, a=4096, b=14336, ms=7.3),
+            dict(kernel="ns_bx", count=32, a=1024, b=4096, ms=0.2),
+            dict(kernel="adamw", count=2, a=1000, b=0, ms=5.0)]
+    out = bench.kernels_by_shape(recs)
+    assert set(out) == {"ns_gram 4096x14336 x48", "ns_bx 1024x4096 x32"}
+    g = out["ns_gram 4096x14336 x48"]
+    assert g["launches"] == 2 and g["ms_per_launch"] == 7.4
+    # algorithmic 2 A^2 B per matrix; executed: 136 of the 256 blocks
+    assert g["tflops_algorithmic"] == round(48 * 2.0 * 4096 ** 2 * 14336 / 7.4e-3 / 1e12, 1)
+    assert g["tflops_executed"] == round(48 * 136 * 2.0 * 256 * 256 * 14336 / 7.4e-3 / 1e12, 1)
