@@ -143,8 +143,15 @@ enum : uint32_t {
   kStatusTimeoutEmpty = 2,    // producer waited too long for a free stage
   kStatusTimeoutAcc = 3,      // epilogue waited too long for an accumulator
   kStatusTimeoutAccFree = 4,  // MMA waited too long for a free accumulator
-  kStatusTimeoutDrain = 5
+  kStatusTimeoutDrain = 5,
+  kStatusTimeoutTile = 6      // a role waited too long for the next tile index
 };
+
+// Workspace-header words (uint32 index) of the GEMM tile scheduler: the count
+// of tiles claimed after each pair's first, and the count of CTAs that have
+// finished.  The last CTA of a launch resets both, and each step clears the
+// header before its first launch.
+constexpr int kSchedWord = 32;
 
 // ------------------------------------------------------------- clipping ----
 

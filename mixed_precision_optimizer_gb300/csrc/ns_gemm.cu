@@ -72,6 +72,12 @@ constexpr int kSlabWords = 32 * 33;            // per epilogue warp: 32 x 32 fp3
 constexpr int kSlabBytes = kEpiWarps * kSlabWords * 4;
 constexpr uint32_t kSmemBytes = kStages * kStageBytes + kSlabBytes + 1024 /*align*/ + 256 /*barriers*/;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
+constexpr int kTileSlots = 6;                  // tile-index ring between the scheduler and the other roles
+// consumers of one ring slot, all arriving on the even CTA's barrier: the MMA
+// warp, the odd CTA's producer, and every epilogue warp of both CTAs
+constexpr uint32_t kTileConsumers = 1 + 1 + 2 * kEpiWarps;
+constexpr int kBarrierBytes = (2 * kStages + 5 + 2 * kTileSlots) * 8 + 8 + 4 * kTileSlots;
+static_assert(kBarrierBytes <= 256, "barrier block larger than its 256-byte reservation");
 
 struct GemmParams {
   int mode;             // NsGemmMode
@@ -89,6 +95,7 @@ struct GemmParams {
   float decay;
   int ns_only;
   uint32_t* status;
+  uint32_t* sched;      // [0]: tiles claimed after the first, [1]: CTAs finished
 };
 
 // ------------------------------------------------------------ PTX helpers --
@@ -227,6 +234,45 @@ __device__ __forceinline__ uint32_t peer_addr(uint32_t addr, uint32_t rank) {
 
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_local(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+// Store to the shared memory of a CTA of this cluster (address from mapa).
+__device__ __forceinline__ void st_cluster_u32(uint32_t cluster_addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
+}
+
+// Wait for a phase completed by an arrive.release.cluster from the other CTA,
+// so that the data it published before arriving is visible here.
+__device__ __forceinline__ bool mbar_try_acq_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ bool mbar_wait_acq_cluster(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
+                                                      uint32_t* status, uint32_t code) {
+  if (mbar_try_acq_cluster(bar, parity)) return true;
+  const unsigned long long t0 = global_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_acq_cluster(bar, parity)) return true;
+    if ((i & 255u) == 0) {
+      if (*abort_flag) return false;
+      if (global_ns() - t0 > kWaitLimitNs) {
+        *abort_flag = 1u;
+        atomicCAS(status, 0u, code);
+        return false;
+      }
+    }
+  }
 }
 
 __device__ __forceinline__ void cluster_sync() {
@@ -435,8 +481,11 @@ ns_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
   uint64_t* acc_full = bars + 2 * kStages;   // [2]        both CTAs: accumulator ready
   uint64_t* acc_empty = acc_full + 2;        // [2]        even CTA: both epilogues drained it
   uint64_t* drain = acc_empty + 2;           // [1]        even CTA: all MMAs complete
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* tile_full = drain + 1;           // [kTileSlots] both CTAs: next tile index published
+  uint64_t* tile_empty = tile_full + kTileSlots;   // [kTileSlots] even CTA: every role has read it
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tile_empty + kTileSlots);
   volatile uint32_t* abort_flag = tmem_slot + 1;
+  volatile int* tile_ring = reinterpret_cast<volatile int*>(tmem_slot + 2);   // [kTileSlots]
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -456,6 +505,10 @@ ns_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
       mbar_init(smem_u32(&acc_empty[a]), 2 * 32 * kEpiWarps);
     }
     mbar_init(smem_u32(drain), 1);
+    for (int k = 0; k < kTileSlots; ++k) {
+      mbar_init(smem_u32(&tile_full[k]), 1);
+      mbar_init(smem_u32(&tile_empty[k]), kTileConsumers);
+    }
     *abort_flag = 0u;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -479,12 +532,44 @@ ns_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------ TMA producer --
-      // Both CTAs load their own halves; completion is counted on the even
-      // CTA's full barrier, which expects both halves' bytes.
+      // The even CTA's producer also schedules.  Each pair starts with tile
+      // `pair` and then claims tiles from a launch-wide counter, so the tiles
+      // in flight are always the most recently claimed ones -- neighbours in
+      // the tile order, which share operand panels in L2 -- however unevenly
+      // the pairs progress (with a fixed stride they drift apart over a long
+      // launch and re-read their panels from DRAM).  Every index, and finally
+      // one past the end, goes to both CTAs through the tile ring; the odd
+      // CTA's producer reads it there.  Both CTAs load their own halves;
+      // completion is counted on the even CTA's full barrier, which expects
+      // both halves' bytes.
       uint32_t it = 0;
       bool ok = true;
       bool issued = false;
-      for (int tile = pair; ok && tile < P.total_tiles; tile += npairs) {
+      const uint32_t ring_odd = peer_addr(smem_u32(const_cast<int*>(tile_ring)), 1);
+      const uint32_t tfull_odd = peer_addr(smem_u32(&tile_full[0]), 1);
+      const uint32_t tempty_even = peer_addr(smem_u32(&tile_empty[0]), 0);
+      for (uint32_t seq = 0; ok; ++seq) {
+        const uint32_t slot = seq % kTileSlots, sph = (seq / kTileSlots) & 1u;
+        int tile;
+        if (rank == 0) {
+          if (!mbar_wait(smem_u32(&tile_empty[slot]), sph ^ 1u, abort_flag, P.status, kStatusTimeoutTile)) {
+            ok = false;
+            break;
+          }
+          tile = seq == 0 ? pair : npairs + static_cast<int>(atomicAdd(P.sched, 1u));
+          tile_ring[slot] = tile;
+          st_cluster_u32(ring_odd + 4 * slot, static_cast<uint32_t>(tile));
+          mbar_arrive_local(smem_u32(&tile_full[slot]));
+          mbar_arrive_remote(tfull_odd + 8 * slot);
+        } else {
+          if (!mbar_wait_acq_cluster(smem_u32(&tile_full[slot]), sph, abort_flag, P.status, kStatusTimeoutTile)) {
+            ok = false;
+            break;
+          }
+          tile = tile_ring[slot];
+          mbar_arrive_remote(tempty_even + 8 * slot);
+        }
+        if (tile >= P.total_tiles) break;
         const Tile t = decode_tile(P, tile);
         const int arow = t.tm * BM_PAIR + static_cast<int>(rank) * BM;
         const int brow = t.tn * BN + static_cast<int>(rank) * BN_HALF;   // B rows (K-major) or columns (MN-major)
@@ -520,9 +605,13 @@ ns_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
       // ------------------------------------- MMA issuer (even CTA only) --
       const uint32_t idesc = b_mn ? instr_desc(true) : instr_desc(false);
       uint32_t it = 0;
-      int lt = 0;
       bool ok = true;
-      for (int tile = pair; ok && tile < P.total_tiles; tile += npairs, ++lt) {
+      for (uint32_t lt = 0; ok; ++lt) {   // lt: this pair's tile sequence number
+        const uint32_t slot = lt % kTileSlots, sph = (lt / kTileSlots) & 1u;
+        if (!mbar_wait(smem_u32(&tile_full[slot]), sph, abort_flag, P.status, kStatusTimeoutTile)) break;
+        const int tile = tile_ring[slot];
+        mbar_arrive_local(smem_u32(&tile_empty[slot]));
+        if (tile >= P.total_tiles) break;
         const uint32_t acc = lt & 1, acc_ph = (lt >> 1) & 1u;
         if (!mbar_wait(smem_u32(&acc_empty[acc]), acc_ph ^ 1u, abort_flag, P.status, kStatusTimeoutAccFree)) {
           ok = false;
@@ -561,8 +650,25 @@ ns_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
     const int half = (warp - 2) >> 2;         // which 128 of the 256 columns
     float* slab = slabs + (warp - 2) * kSlabWords;
     const uint32_t empty_even = peer_addr(smem_u32(&acc_empty[0]), 0);
-    int lt = 0;
-    for (int tile = pair; tile < P.total_tiles; tile += npairs, ++lt) {
+    const uint32_t tempty_even = peer_addr(smem_u32(&tile_empty[0]), 0);
+    for (uint32_t lt = 0;; ++lt) {   // lt: this pair's tile sequence number
+      const uint32_t slot = lt % kTileSlots, sph = (lt / kTileSlots) & 1u;
+      int tile = 0, got = 1;
+      if (lane == 0) {
+        got = (rank == 0 ? mbar_wait(smem_u32(&tile_full[slot]), sph, abort_flag, P.status, kStatusTimeoutTile)
+                         : mbar_wait_acq_cluster(smem_u32(&tile_full[slot]), sph, abort_flag, P.status,
+                                                 kStatusTimeoutTile))
+                  ? 1
+                  : 0;
+        if (got) {
+          tile = tile_ring[slot];
+          if (rank == 0) mbar_arrive_local(smem_u32(&tile_empty[slot]));
+          else mbar_arrive_remote(tempty_even + 8 * slot);
+        }
+      }
+      got = __shfl_sync(0xffffffffu, got, 0);
+      tile = __shfl_sync(0xffffffffu, tile, 0);
+      if (!got || tile >= P.total_tiles) break;
       const uint32_t acc = lt & 1, acc_ph = (lt >> 1) & 1u;
       if (!mbar_wait(smem_u32(&acc_full[acc]), acc_ph, abort_flag, P.status, kStatusTimeoutAcc)) break;
       tc_fence_after();
@@ -583,6 +689,15 @@ ns_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
   tc_fence_before();
   __syncthreads();
   cluster_sync();            // no CTA leaves while its partner may still signal it
+  if (threadIdx.x == 0) {
+    // the last CTA to finish (every claim of the launch is made by then)
+    // resets the scheduler for the next launch on this workspace
+    __threadfence();
+    if (atomicAdd(P.sched + 1, 1u) == gridDim.x - 1) {
+      atomicExch(P.sched, 0u);
+      atomicExch(P.sched + 1, 0u);
+    }
+  }
   if (warp == 1) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(kTmemCols)
@@ -657,6 +772,7 @@ cudaError_t launch_ns_iteration(const MuonGroup& grp, const NsBuffers& buf, cons
   base.decay = s.decay;
   base.ns_only = s.ns_only;
   base.status = buf.status;
+  base.sched = buf.status + kSchedWord;
   const int T = static_cast<int>(Ap / 256);
   cudaError_t e;
 
