@@ -70,6 +70,9 @@ constexpr int kThreads = 64 + 32 * kEpiWarps;  // TMA warp, MMA warp, epilogue w
 constexpr int kTmemCols = 512;                 // 2 accumulators x 256 fp32 columns
 constexpr int kSlabWords = 32 * 33;            // per epilogue warp: 32 x 32 fp32, padded rows
 constexpr int kSlabBytes = kEpiWarps * kSlabWords * 4;
+constexpr int kOutBlockBytes = 32 * 32 * 2;    // C X output: one 32 x 32 fp16 block staged for a TMA store
+// each epilogue warp stages two output blocks; together they must fit in the slabs
+static_assert(kEpiWarps * 2 * kOutBlockBytes <= kSlabBytes, "output staging larger than the transpose slabs");
 constexpr uint32_t kSmemBytes = kStages * kStageBytes + kSlabBytes + 1024 /*align*/ + 256 /*barriers*/;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 constexpr int kTileSlots = 6;                  // tile-index ring between the scheduler and the other roles
@@ -159,6 +162,28 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
       " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
       : "memory");
+}
+
+// Tile store from this CTA's shared memory to global memory (bulk async-group
+// of the issuing thread).
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int x, int y, int z) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y), "r"(z), "r"(src)
+               : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+// Wait until at most one of this thread's bulk groups still reads shared memory.
+__device__ __forceinline__ void bulk_wait_read_1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
+
+// Wait until all of this thread's bulk groups have completed.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// Make this thread's generic-proxy shared-memory writes visible to the TMA.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 // Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of
@@ -469,7 +494,8 @@ __device__ __forceinline__ void epilogue_block(const GemmParams& P, const MuonGr
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 ns_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
-               const __grid_constant__ GemmParams P, const __grid_constant__ MuonGroup grp) {
+               const __grid_constant__ CUtensorMap map_out, const __grid_constant__ GemmParams P,
+               const __grid_constant__ MuonGroup grp) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* stage_a = smem;                                  // kStages x 16 KB
@@ -649,6 +675,10 @@ ns_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
     const int quarter = warp & 3;             // TMEM lanes this warp may access
     const int half = (warp - 2) >> 2;         // which 128 of the 256 columns
     float* slab = slabs + (warp - 2) * kSlabWords;
+    // C X: two 1024-byte-aligned output staging buffers per warp, carved from
+    // the transpose slabs (which C X does not use)
+    uint8_t* out_stage = reinterpret_cast<uint8_t*>(slabs) + (warp - 2) * 2 * kOutBlockBytes;
+    uint32_t out_blocks = 0;
     const uint32_t empty_even = peer_addr(smem_u32(&acc_empty[0]), 0);
     const uint32_t tempty_even = peer_addr(smem_u32(&tile_empty[0]), 0);
     for (uint32_t lt = 0;; ++lt) {   // lt: this pair's tile sequence number
@@ -679,11 +709,35 @@ ns_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
         float v[32];
         __syncwarp();
         tmem_ld32(taddr + c0, v);
-        epilogue_block(P, grp, t, slab, lane, row0, t.tn * BN + c0, v);
+        if (P.mode == kBx) {
+          // X' block: staged in shared memory (64-byte swizzle: 16-byte chunk
+          // q of row r sits at chunk q ^ ((r >> 1) & 3)), stored by one TMA
+          // store; two staging buffers alternate
+          uint8_t* buf = out_stage + (out_blocks & 1) * kOutBlockBytes;
+          if (out_blocks >= 2 && lane == 0) bulk_wait_read_1();   // this buffer's previous store has read it
+          __syncwarp();
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const uint32_t phys = static_cast<uint32_t>(q) ^ ((static_cast<uint32_t>(lane) >> 1) & 3u);
+            *reinterpret_cast<uint4*>(buf + lane * 64 + phys * 16) =
+                make_uint4(pack_f16(v[8 * q], v[8 * q + 1]), pack_f16(v[8 * q + 2], v[8 * q + 3]),
+                           pack_f16(v[8 * q + 4], v[8 * q + 5]), pack_f16(v[8 * q + 6], v[8 * q + 7]));
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_3d(&map_out, smem_u32(buf), t.tn * BN + c0, row0, t.mat);
+            bulk_commit();
+          }
+          ++out_blocks;
+        } else {
+          epilogue_block(P, grp, t, slab, lane, row0, t.tn * BN + c0, v);
+        }
       }
       tc_fence_before();
       mbar_arrive_remote(empty_even + acc * static_cast<uint32_t>(sizeof(uint64_t)));
     }
+    if (lane == 0 && out_blocks > 0) bulk_wait_all();   // stores complete before the CTA exits
   }
 
   tc_fence_before();
@@ -740,7 +794,24 @@ cudaError_t make_map(CUtensorMap* map, const void* base, int64_t inner, int64_t 
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-cudaError_t launch_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const GemmParams& P, const MuonGroup& grp,
+// 3-D map over `count` row-major fp16 matrices [rows][inner] for the C X output:
+// box 32 x 32 elements (64-byte rows), 64-byte swizzle.
+cudaError_t make_out_map(CUtensorMap* map, const void* base, int64_t inner, int64_t rows, int64_t count) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return cudaErrorNotSupported;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows),
+                              static_cast<cuuint64_t>(count)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(inner * 2), static_cast<cuuint64_t>(inner * rows * 2)};
+  const cuuint32_t box[3] = {32, 32, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+cudaError_t launch_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mo, const GemmParams& P,
+                        const MuonGroup& grp,
                         cudaStream_t stream) {
   static thread_local int configured_dev = -1;
   int dev = 0;
@@ -753,7 +824,7 @@ cudaError_t launch_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const Gemm
   }
   const int max_pairs = num_sms() / 2;
   const int pairs = P.total_tiles < max_pairs ? P.total_tiles : max_pairs;
-  ns_gemm_kernel<<<2 * pairs, kThreads, kSmemBytes, stream>>>(ma, mb, P, grp);
+  ns_gemm_kernel<<<2 * pairs, kThreads, kSmemBytes, stream>>>(ma, mb, mo, P, grp);
   return cudaGetLastError();
 }
 
@@ -784,6 +855,7 @@ cudaError_t launch_ns_iteration(const MuonGroup& grp, const NsBuffers& buf, cons
     CUtensorMap ma, mb;
     if ((e = make_map(&ma, X, Bp, Ap, cnt, BM)) != cudaSuccess) return e;
     if ((e = make_map(&mb, X, Bp, Ap, cnt, BN_HALF)) != cudaSuccess) return e;
+    const CUtensorMap& mo = mb;   // unused by this mode
     GemmParams P = base;
     P.mode = kGram;
     P.k_blocks = static_cast<int>(Bp / 64);
@@ -792,7 +864,7 @@ cudaError_t launch_ns_iteration(const MuonGroup& grp, const NsBuffers& buf, cons
     P.Af = buf.Af;
     P.Ah = buf.Ah;
     prof_begin(OPT_KERNEL_NS_GRAM, grp.count, grp.A, grp.B, stream);
-    e = launch_gemm(ma, mb, P, grp, stream);
+    e = launch_gemm(ma, mb, mo, P, grp, stream);
     prof_end(stream);
     if (e != cudaSuccess) return e;
   }
@@ -801,6 +873,7 @@ cudaError_t launch_ns_iteration(const MuonGroup& grp, const NsBuffers& buf, cons
     CUtensorMap ma, mb;
     if ((e = make_map(&ma, buf.Ah, Ap, Ap, cnt, BM)) != cudaSuccess) return e;
     if ((e = make_map(&mb, buf.Ah, Ap, Ap, cnt, BN_HALF)) != cudaSuccess) return e;
+    const CUtensorMap& mo = mb;   // unused by this mode
     GemmParams P = base;
     P.mode = kPoly;
     P.k_blocks = static_cast<int>(Ap / 64);
@@ -809,7 +882,7 @@ cudaError_t launch_ns_iteration(const MuonGroup& grp, const NsBuffers& buf, cons
     P.Af = buf.Af;
     P.Ch = buf.Ch;
     prof_begin(OPT_KERNEL_NS_POLY, grp.count, grp.A, grp.B, stream);
-    e = launch_gemm(ma, mb, P, grp, stream);
+    e = launch_gemm(ma, mb, mo, P, grp, stream);
     prof_end(stream);
     if (e != cudaSuccess) return e;
   }
@@ -819,6 +892,8 @@ cudaError_t launch_ns_iteration(const MuonGroup& grp, const NsBuffers& buf, cons
     CUtensorMap ma, mb;
     if ((e = make_map(&ma, buf.Ch, Ap, Ap, cnt, BM)) != cudaSuccess) return e;
     if ((e = make_map(&mb, X, Bp, Ap, cnt, 64)) != cudaSuccess) return e;
+    CUtensorMap mo = mb;   // the last iteration updates W instead
+    if (it != s.ns_steps - 1 && (e = make_out_map(&mo, X_next, Bp, Ap, cnt)) != cudaSuccess) return e;
     GemmParams P = base;
     P.mode = (it == s.ns_steps - 1) ? kBxFinal : kBx;
     P.k_blocks = static_cast<int>(Ap / 64);
@@ -827,7 +902,7 @@ cudaError_t launch_ns_iteration(const MuonGroup& grp, const NsBuffers& buf, cons
     P.total_tiles = P.tiles_per_mat * grp.count;
     P.Xh = X_next;
     prof_begin(OPT_KERNEL_NS_BX, grp.count, grp.A, grp.B, stream);
-    e = launch_gemm(ma, mb, P, grp, stream);
+    e = launch_gemm(ma, mb, mo, P, grp, stream);
     prof_end(stream);
     if (e != cudaSuccess) return e;
   }
