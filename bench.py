@@ -569,74 +569,35 @@ def run_ours(args, dist: Dist):
 
 class PinnedHostArena:
     """Page-locked host memory for every per-tensor host buffer of the e2e
-    leg: one anonymous mapping aligned to the transparent-huge-page size and
-    advised MADV_HUGEPAGE, registered once with cudaHostRegister (return code
-    checked), carved into per-tensor views at 256-byte boundaries.
+    leg: one allocation from CUDA's pinned-host allocator (cudaHostAlloc,
+    through torch's pinned memory), carved into per-tensor views at 256-byte
+    boundaries.
 
-    One registration over huge pages keeps the copy engines' translation of
-    host addresses cheap.  On a GB300 (64 KiB base pages) one registration of
-    a numpy array per tensor -- 294 for the 147-tensor model -- copied at
-    10-30 GB/s, the arena at 190-210 GB/s in each direction."""
+    On the GB300 hosts (64 KiB base pages) the copy engines are fast only on
+    memory the driver pinned itself or on transparent huge pages: one
+    cudaHostRegister of a numpy array per tensor (294 for the 147-tensor model)
+    copied at 10-30 GB/s, and a registered mapping advised MADV_HUGEPAGE copied
+    at 190-210 GB/s only while the kernel could back all of it with huge pages
+    (with 79 % backed, H2D fell to 13 GB/s).  cudaHostAlloc memory copies at
+    190-210 GB/s in both directions whatever the state of host memory."""
 
     ALIGN = 256
 
     def __init__(self, counts_dtypes):
-        import mmap
-        import numpy as np
         import torch
-        try:
-            huge = int(open("/sys/kernel/mm/transparent_hugepage/hpage_pmd_size").read())
-        except (OSError, ValueError):
-            huge = 2 << 20
         offsets, o = [], 0
         for n, dt in counts_dtypes:
             offsets.append(o)
             o += (n * torch.empty(0, dtype=dt).element_size() + self.ALIGN - 1) // self.ALIGN * self.ALIGN
         self.nbytes = max(o, self.ALIGN)
-        self._map = mmap.mmap(-1, self.nbytes + huge, flags=mmap.MAP_PRIVATE | mmap.MAP_ANONYMOUS)
-        whole = np.frombuffer(self._map, dtype=np.uint8)
-        skip = (-whole.ctypes.data) % huge
-        self.huge_pages = True
-        try:
-            self._map.madvise(mmap.MADV_HUGEPAGE, skip, self.nbytes)
-        except (AttributeError, OSError, ValueError):
-            self.huge_pages = False
-        self._bytes = whole[skip:skip + self.nbytes]
-        self._bytes[::4096] = 0                      # fault the pages in under the advice
-        self.base = self._bytes.ctypes.data
-        rc = torch.cuda.cudart().cudaHostRegister(self.base, self.nbytes, 0)
-        if int(rc) != 0:
-            raise SystemExit(f"e2e: cudaHostRegister of the {self.nbytes}-byte host arena failed: {rc}")
-        raw = torch.from_numpy(self._bytes)
-        self.views = [raw[off:off + n * torch.empty(0, dtype=dt).element_size()].view(dt)
+        self._raw = torch.empty(self.nbytes, dtype=torch.uint8, pin_memory=True)
+        if not self._raw.is_pinned():
+            raise SystemExit("e2e: the pinned host allocation is not page-locked")
+        self.views = [self._raw[off:off + n * torch.empty(0, dtype=dt).element_size()].view(dt)
                       for off, (n, dt) in zip(offsets, counts_dtypes)]
 
-    def huge_page_bytes(self):
-        """Bytes of the arena the kernel backs with transparent huge pages
-        (AnonHugePages of the mappings that overlap it), or None."""
-        lo, hi = self.base, self.base + self.nbytes
-        total, inside = 0, False
-        try:
-            with open("/proc/self/smaps") as f:
-                for line in f:
-                    head = line.split(" ", 1)[0]
-                    if "-" in head and not line.startswith(("AnonHugePages", "Size")):
-                        try:
-                            s, e = (int(x, 16) for x in head.split("-"))
-                        except ValueError:
-                            continue
-                        inside = s < hi and e > lo
-                    elif inside and line.startswith("AnonHugePages:"):
-                        total += int(line.split()[1]) * 1024
-        except OSError:
-            return None
-        return total
-
     def close(self):
-        import torch
-        if self._bytes is not None:
-            torch.cuda.cudart().cudaHostUnregister(self.base)
-            self.views, self._bytes = [], None
+        self.views, self._raw = [], None
 
 
 def adamw_buckets(params, hp, reps=5):
@@ -760,7 +721,6 @@ def run_e2e(args, step_fn, params, t, total, dist: Dist):
                                   ("d2h", d2h_begin, d2h_done))}
     h2d = sum(x.numel() * x.element_size() for x in g_host)
     d2h = sum(x.numel() * x.element_size() for x in b_host)
-    huge = arena.huge_page_bytes()
     del g_host, b_host
     arena.close()
     return {"value": round(total * K * dist.world / (ms * 1e-3), 1), "unit": UNIT,
@@ -768,8 +728,7 @@ def run_e2e(args, step_fn, params, t, total, dist: Dist):
             "steps": K, "ms_per_step": round(ms / K, 3),
             "pipelined": "main_grad and bf16 model double-buffered; H2D, step and D2H on three streams; "
                          "the first step's H2D and the last step's D2H are not overlapped and are included",
-            "host_buffers": f"one registered arena of {arena.nbytes} bytes, "
-                            f"{'transparent huge pages advised' if arena.huge_pages else 'base pages'}; "
+            "host_buffers": f"one cudaHostAlloc arena of {arena.nbytes} bytes (torch pinned memory); "
                             "copies warmed once before timing",
             "host_wall_ms_per_step": round(wall_ms / K, 3),
             "host_enqueue_ms_per_step": {"h2d": round(host_ms[0] / K, 3), "step": round(host_ms[1] / K, 3),
@@ -777,7 +736,6 @@ def run_e2e(args, step_fn, params, t, total, dist: Dist):
             "device_ms_per_step": phase,
             "h2d_gbs": round(h2d / (phase["h2d"] * 1e6), 1) if phase["h2d"] > 0 else None,
             "d2h_gbs": round(d2h / (phase["d2h"] * 1e6), 1) if phase["d2h"] > 0 else None,
-            "host_huge_page_bytes": huge,
             "clocks": clocks.summary()}
 
 
