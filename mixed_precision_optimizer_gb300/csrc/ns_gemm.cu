@@ -31,8 +31,12 @@
 //             overlap the main loop of the next
 //   warps 2-9 epilogue in both CTAs: two warps per TMEM lane quarter, each
 //             taking 128 of the 256 columns of this CTA's 128 rows, 32 at a
-//             time (tcgen05.ld), fused math, stores; each warp transposes
-//             32 x 32 blocks through its own shared-memory slab
+//             time (tcgen05.ld), fused math; each warp stages its 32 x 32
+//             output blocks (and, for the symmetric products, their mirror
+//             blocks, written column-wise) in its own 8 KB of shared memory
+//             and writes them with TMA stores; the last C X, a read-modify-
+//             write of W in W's own orientation, uses the same 8 KB as a
+//             transpose slab and plain loads and stores
 // Per MMA each SM stages 8 KB of operands (A and B halves) instead of the
 // 12 KB a single-CTA 128 x 256 tile needs.
 //
@@ -68,12 +72,15 @@ constexpr int kMnBlockBytes = 64 * kRowBytes;   // MN-major B: one 64-column blo
 constexpr int kEpiWarps = 8;                   // two warps per TMEM lane quarter
 constexpr int kThreads = 64 + 32 * kEpiWarps;  // TMA warp, MMA warp, epilogue warps
 constexpr int kTmemCols = 512;                 // 2 accumulators x 256 fp32 columns
-constexpr int kSlabWords = 32 * 33;            // per epilogue warp: 32 x 32 fp32, padded rows
-constexpr int kSlabBytes = kEpiWarps * kSlabWords * 4;
-constexpr int kOutBlockBytes = 32 * 32 * 2;    // C X output: one 32 x 32 fp16 block staged for a TMA store
-// each epilogue warp stages two output blocks; together they must fit in the slabs
-static_assert(kEpiWarps * 2 * kOutBlockBytes <= kSlabBytes, "output staging larger than the transpose slabs");
+constexpr int kSlabWords = 32 * 33;            // 32 x 32 fp32 transpose slab, padded rows
+constexpr int kWarpScratch = 8192;             // per epilogue warp: transpose slab or TMA-store staging
+constexpr int kSlabBytes = kEpiWarps * kWarpScratch;
+constexpr int kOutBlockBytes = 32 * 32 * 2;    // one 32 x 32 fp16 block staged for a TMA store
+constexpr int kOutBlockBytes32 = 32 * 32 * 4;  // one 32 x 32 fp32 block
+static_assert(kSlabWords * 4 <= kWarpScratch, "transpose slab larger than a warp's scratch");
+static_assert(kOutBlockBytes32 + 2 * kOutBlockBytes <= kWarpScratch, "gram staging larger than a warp's scratch");
 constexpr uint32_t kSmemBytes = kStages * kStageBytes + kSlabBytes + 1024 /*align*/ + 256 /*barriers*/;
+static_assert(kSmemBytes <= 232448, "dynamic shared memory above the 227 KB a CTA may use");
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 constexpr int kTileSlots = 6;                  // tile-index ring between the scheduler and the other roles
 // consumers of one ring slot, all arriving on the even CTA's barrier: the MMA
@@ -370,21 +377,40 @@ __device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
   return static_cast<uint32_t>(f16_bits(lo)) | (static_cast<uint32_t>(f16_bits(hi)) << 16);
 }
 
-// Store 32 consecutive fp16 values (64 bytes, 16-byte aligned destination).
-__device__ __forceinline__ void store_f16x32(uint16_t* dst, const float (&v)[32]) {
-  uint4* d = reinterpret_cast<uint4*>(dst);
+// Staging of 32 x 32 blocks for TMA stores.  Lane t holds row t of the block
+// (columns 0..31) in v.  fp16 blocks use the 64-byte swizzle (16-byte chunk q
+// of row r at chunk q ^ ((r >> 1) & 3)), fp32 blocks the 128-byte swizzle
+// (chunk q of row r at chunk q ^ (r & 7)); the buffers are 1024-byte aligned.
+__device__ __forceinline__ void stage_f16_rows(uint8_t* buf, int lane, const float (&v)[32]) {
 #pragma unroll
-  for (int q = 0; q < 4; ++q)
-    d[q] = make_uint4(pack_f16(v[8 * q], v[8 * q + 1]), pack_f16(v[8 * q + 2], v[8 * q + 3]),
-                      pack_f16(v[8 * q + 4], v[8 * q + 5]), pack_f16(v[8 * q + 6], v[8 * q + 7]));
+  for (int q = 0; q < 4; ++q) {
+    const uint32_t phys = static_cast<uint32_t>(q) ^ ((static_cast<uint32_t>(lane) >> 1) & 3u);
+    *reinterpret_cast<uint4*>(buf + lane * 64 + phys * 16) =
+        make_uint4(pack_f16(v[8 * q], v[8 * q + 1]), pack_f16(v[8 * q + 2], v[8 * q + 3]),
+                   pack_f16(v[8 * q + 4], v[8 * q + 5]), pack_f16(v[8 * q + 6], v[8 * q + 7]));
+  }
 }
 
-// Store 32 consecutive fp32 values (128 bytes, 16-byte aligned destination).
-__device__ __forceinline__ void store_f32x32(float* dst, const float (&v)[32]) {
+// The transposed block: lane t writes column t (element (j, t) = v[j]).
+__device__ __forceinline__ void stage_f16_cols(uint8_t* buf, int lane, const float (&v)[32]) {
+  const uint32_t chunk = static_cast<uint32_t>(lane) >> 3, within = (static_cast<uint32_t>(lane) & 7u) * 2u;
 #pragma unroll
-  for (int q = 0; q < 8; ++q)
-    reinterpret_cast<float4*>(dst)[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+  for (int j = 0; j < 32; ++j) {
+    const uint32_t phys = chunk ^ ((static_cast<uint32_t>(j) >> 1) & 3u);
+    *reinterpret_cast<uint16_t*>(buf + j * 64 + phys * 16 + within) = f16_bits(v[j]);
+  }
 }
+
+__device__ __forceinline__ void stage_f32_rows(uint8_t* buf, int lane, const float (&v)[32]) {
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const uint32_t phys = static_cast<uint32_t>(q) ^ (static_cast<uint32_t>(lane) & 7u);
+    *reinterpret_cast<float4*>(buf + lane * 128 + phys * 16) =
+        make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+  }
+}
+
+__device__ __forceinline__ void bulk_wait_read_0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 
 // Warp-level 32 x 32 transpose through the warp's shared-memory slab: on
 // entry lane t holds row t (columns 0..31) in v; on exit lane t holds column t
@@ -411,41 +437,9 @@ __device__ __forceinline__ uint16_t bf16_rne(float x) {
 // `lane` holds row row0 + lane, columns col0 .. col0 + 31, in v.
 __device__ __forceinline__ void epilogue_block(const GemmParams& P, const MuonGroup& grp, const Tile& t,
                                                float* slab, int lane, int row0, int col0, float (&v)[32]) {
-  const int64_t Ap = P.Ap, Bp = P.Bp;
   const int row = row0 + lane;
   float w[32];
-  if (P.mode == kGram) {
-    // fp32 A only on and below the diagonal blocks (the only blocks the poly
-    // stage reads for its b A term); the fp16 operand in full.
-    float* Am = P.Af + static_cast<int64_t>(t.mat) * Ap * Ap;
-    uint16_t* Ahm = P.Ah + static_cast<int64_t>(t.mat) * Ap * Ap;
-    store_f32x32(Am + static_cast<int64_t>(row) * Ap + col0, v);
-    store_f16x32(Ahm + static_cast<int64_t>(row) * Ap + col0, v);
-    if (t.mirror) {
-      warp_transpose(slab, lane, v, w);   // lane now holds column col0 + lane, rows row0..row0+31
-      store_f16x32(Ahm + static_cast<int64_t>(col0 + lane) * Ap + row0, w);
-    }
-  } else if (P.mode == kPoly) {
-    const float* Arow = P.Af + static_cast<int64_t>(t.mat) * Ap * Ap + static_cast<int64_t>(row) * Ap + col0;
-    uint16_t* Cm = P.Ch + static_cast<int64_t>(t.mat) * Ap * Ap;
-#pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      const float4 a4 = __ldcs(reinterpret_cast<const float4*>(Arow) + q);
-      v[4 * q + 0] = P.b * a4.x + P.c * v[4 * q + 0];
-      v[4 * q + 1] = P.b * a4.y + P.c * v[4 * q + 1];
-      v[4 * q + 2] = P.b * a4.z + P.c * v[4 * q + 2];
-      v[4 * q + 3] = P.b * a4.w + P.c * v[4 * q + 3];
-    }
-#pragma unroll
-    for (int j = 0; j < 32; ++j) v[j] += (row == col0 + j) ? P.a : 0.f;   // + a I
-    store_f16x32(Cm + static_cast<int64_t>(row) * Ap + col0, v);
-    if (t.mirror) {
-      warp_transpose(slab, lane, v, w);
-      store_f16x32(Cm + static_cast<int64_t>(col0 + lane) * Ap + row0, w);
-    }
-  } else if (P.mode == kBx) {
-    store_f16x32(P.Xh + static_cast<int64_t>(t.mat) * Ap * Bp + static_cast<int64_t>(row) * Bp + col0, v);
-  } else {
+  {
     // last iteration: O = X' in the wide orientation (rows: A index, columns: B index).
     // The warp updates 32 runs of 32 consecutive W elements: for a tall W
     // (stored as the transpose of the wide layout) run j is W[col0 + j][row0 ..
@@ -494,13 +488,14 @@ __device__ __forceinline__ void epilogue_block(const GemmParams& P, const MuonGr
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 ns_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
-               const __grid_constant__ CUtensorMap map_out, const __grid_constant__ GemmParams P,
+               const __grid_constant__ CUtensorMap map_out, const __grid_constant__ CUtensorMap map_out32,
+               const __grid_constant__ GemmParams P,
                const __grid_constant__ MuonGroup grp) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* stage_a = smem;                                  // kStages x 16 KB
   uint8_t* stage_b = smem + kStages * kStageA;              // kStages x 16 KB
-  float* slabs = reinterpret_cast<float*>(smem + kStages * kStageBytes);   // 4 x 32 x 33 fp32
+  uint8_t* scratch = smem + kStages * kStageBytes;         // kEpiWarps x 8 KB
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes + kSlabBytes);
   uint64_t* full = bars;                     // [kStages]  even CTA: both CTAs' copies landed
   uint64_t* empty = bars + kStages;          // [kStages]  both CTAs: stage free again
@@ -674,10 +669,10 @@ ns_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
     // ------------------------------------------------------ epilogue --
     const int quarter = warp & 3;             // TMEM lanes this warp may access
     const int half = (warp - 2) >> 2;         // which 128 of the 256 columns
-    float* slab = slabs + (warp - 2) * kSlabWords;
-    // C X: two 1024-byte-aligned output staging buffers per warp, carved from
-    // the transpose slabs (which C X does not use)
-    uint8_t* out_stage = reinterpret_cast<uint8_t*>(slabs) + (warp - 2) * 2 * kOutBlockBytes;
+    // this warp's 8 KB of scratch (1024-byte aligned): the transpose slab of
+    // the last C X, or staging for the TMA stores of the other stages
+    uint8_t* out_stage = scratch + (warp - 2) * kWarpScratch;
+    float* slab = reinterpret_cast<float*>(out_stage);
     uint32_t out_blocks = 0;
     const uint32_t empty_even = peer_addr(smem_u32(&acc_empty[0]), 0);
     const uint32_t tempty_even = peer_addr(smem_u32(&tile_empty[0]), 0);
@@ -710,23 +705,64 @@ ns_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
         __syncwarp();
         tmem_ld32(taddr + c0, v);
         if (P.mode == kBx) {
-          // X' block: staged in shared memory (64-byte swizzle: 16-byte chunk
-          // q of row r sits at chunk q ^ ((r >> 1) & 3)), stored by one TMA
-          // store; two staging buffers alternate
+          // X' block: staged in shared memory, stored by one TMA store; two
+          // staging buffers alternate
           uint8_t* buf = out_stage + (out_blocks & 1) * kOutBlockBytes;
           if (out_blocks >= 2 && lane == 0) bulk_wait_read_1();   // this buffer's previous store has read it
           __syncwarp();
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const uint32_t phys = static_cast<uint32_t>(q) ^ ((static_cast<uint32_t>(lane) >> 1) & 3u);
-            *reinterpret_cast<uint4*>(buf + lane * 64 + phys * 16) =
-                make_uint4(pack_f16(v[8 * q], v[8 * q + 1]), pack_f16(v[8 * q + 2], v[8 * q + 3]),
-                           pack_f16(v[8 * q + 4], v[8 * q + 5]), pack_f16(v[8 * q + 6], v[8 * q + 7]));
-          }
+          stage_f16_rows(buf, lane, v);
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
             tma_store_3d(&map_out, smem_u32(buf), t.tn * BN + c0, row0, t.mat);
+            bulk_commit();
+          }
+          ++out_blocks;
+        } else if (P.mode == kGram) {
+          // A in fp32 and fp16 (and the fp16 mirror block of an off-diagonal
+          // tile); one staging buffer: the previous block's stores have read it
+          const int col0 = t.tn * BN + c0;
+          if (out_blocks >= 1 && lane == 0) bulk_wait_read_0();
+          __syncwarp();
+          stage_f32_rows(out_stage, lane, v);
+          stage_f16_rows(out_stage + kOutBlockBytes32, lane, v);
+          if (t.tm != t.tn) stage_f16_cols(out_stage + kOutBlockBytes32 + kOutBlockBytes, lane, v);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_3d(&map_out32, smem_u32(out_stage), col0, row0, t.mat);
+            tma_store_3d(&map_out, smem_u32(out_stage + kOutBlockBytes32), col0, row0, t.mat);
+            if (t.tm != t.tn)
+              tma_store_3d(&map_out, smem_u32(out_stage + kOutBlockBytes32 + kOutBlockBytes), row0, col0, t.mat);
+            bulk_commit();
+          }
+          ++out_blocks;
+        } else if (P.mode == kPoly) {
+          // C = a I + b A + c (A A) in fp16 (and its mirror block); two
+          // staging buffers alternate
+          const int col0 = t.tn * BN + c0;
+          const int row = row0 + lane;
+          const float* Arow = P.Af + static_cast<int64_t>(t.mat) * P.Ap * P.Ap + static_cast<int64_t>(row) * P.Ap + col0;
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const float4 a4 = __ldcs(reinterpret_cast<const float4*>(Arow) + q);
+            v[4 * q + 0] = P.b * a4.x + P.c * v[4 * q + 0];
+            v[4 * q + 1] = P.b * a4.y + P.c * v[4 * q + 1];
+            v[4 * q + 2] = P.b * a4.z + P.c * v[4 * q + 2];
+            v[4 * q + 3] = P.b * a4.w + P.c * v[4 * q + 3];
+          }
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] += (row == col0 + j) ? P.a : 0.f;   // + a I
+          uint8_t* buf = out_stage + (out_blocks & 1) * (2 * kOutBlockBytes);
+          if (out_blocks >= 2 && lane == 0) bulk_wait_read_1();
+          __syncwarp();
+          stage_f16_rows(buf, lane, v);
+          if (t.tm != t.tn) stage_f16_cols(buf + kOutBlockBytes, lane, v);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_3d(&map_out, smem_u32(buf), col0, row0, t.mat);
+            if (t.tm != t.tn) tma_store_3d(&map_out, smem_u32(buf + kOutBlockBytes), row0, col0, t.mat);
             bulk_commit();
           }
           ++out_blocks;
@@ -810,8 +846,24 @@ cudaError_t make_out_map(CUtensorMap* map, const void* base, int64_t inner, int6
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-cudaError_t launch_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mo, const GemmParams& P,
-                        const MuonGroup& grp,
+// 3-D map over `count` row-major fp32 matrices [rows][inner] for the fp32 Gram
+// output: box 32 x 32 elements (128-byte rows), 128-byte swizzle.
+cudaError_t make_out_map32(CUtensorMap* map, const void* base, int64_t inner, int64_t rows, int64_t count) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return cudaErrorNotSupported;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows),
+                              static_cast<cuuint64_t>(count)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(inner * 4), static_cast<cuuint64_t>(inner * rows * 4)};
+  const cuuint32_t box[3] = {32, 32, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+cudaError_t launch_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mo, const CUtensorMap& mo32,
+                        const GemmParams& P, const MuonGroup& grp,
                         cudaStream_t stream) {
   static thread_local int configured_dev = -1;
   int dev = 0;
@@ -824,7 +876,7 @@ cudaError_t launch_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const CUte
   }
   const int max_pairs = num_sms() / 2;
   const int pairs = P.total_tiles < max_pairs ? P.total_tiles : max_pairs;
-  ns_gemm_kernel<<<2 * pairs, kThreads, kSmemBytes, stream>>>(ma, mb, mo, P, grp);
+  ns_gemm_kernel<<<2 * pairs, kThreads, kSmemBytes, stream>>>(ma, mb, mo, mo32, P, grp);
   return cudaGetLastError();
 }
 
@@ -855,7 +907,9 @@ cudaError_t launch_ns_iteration(const MuonGroup& grp, const NsBuffers& buf, cons
     CUtensorMap ma, mb;
     if ((e = make_map(&ma, X, Bp, Ap, cnt, BM)) != cudaSuccess) return e;
     if ((e = make_map(&mb, X, Bp, Ap, cnt, BN_HALF)) != cudaSuccess) return e;
-    const CUtensorMap& mo = mb;   // unused by this mode
+    CUtensorMap mo, mo32;
+    if ((e = make_out_map(&mo, buf.Ah, Ap, Ap, cnt)) != cudaSuccess) return e;
+    if ((e = make_out_map32(&mo32, buf.Af, Ap, Ap, cnt)) != cudaSuccess) return e;
     GemmParams P = base;
     P.mode = kGram;
     P.k_blocks = static_cast<int>(Bp / 64);
@@ -864,7 +918,7 @@ cudaError_t launch_ns_iteration(const MuonGroup& grp, const NsBuffers& buf, cons
     P.Af = buf.Af;
     P.Ah = buf.Ah;
     prof_begin(OPT_KERNEL_NS_GRAM, grp.count, grp.A, grp.B, stream);
-    e = launch_gemm(ma, mb, mo, P, grp, stream);
+    e = launch_gemm(ma, mb, mo, mo32, P, grp, stream);
     prof_end(stream);
     if (e != cudaSuccess) return e;
   }
@@ -873,7 +927,8 @@ cudaError_t launch_ns_iteration(const MuonGroup& grp, const NsBuffers& buf, cons
     CUtensorMap ma, mb;
     if ((e = make_map(&ma, buf.Ah, Ap, Ap, cnt, BM)) != cudaSuccess) return e;
     if ((e = make_map(&mb, buf.Ah, Ap, Ap, cnt, BN_HALF)) != cudaSuccess) return e;
-    const CUtensorMap& mo = mb;   // unused by this mode
+    CUtensorMap mo;
+    if ((e = make_out_map(&mo, buf.Ch, Ap, Ap, cnt)) != cudaSuccess) return e;
     GemmParams P = base;
     P.mode = kPoly;
     P.k_blocks = static_cast<int>(Ap / 64);
@@ -882,7 +937,7 @@ cudaError_t launch_ns_iteration(const MuonGroup& grp, const NsBuffers& buf, cons
     P.Af = buf.Af;
     P.Ch = buf.Ch;
     prof_begin(OPT_KERNEL_NS_POLY, grp.count, grp.A, grp.B, stream);
-    e = launch_gemm(ma, mb, mo, P, grp, stream);
+    e = launch_gemm(ma, mb, mo, mo, P, grp, stream);   // no fp32 output
     prof_end(stream);
     if (e != cudaSuccess) return e;
   }
@@ -902,7 +957,7 @@ cudaError_t launch_ns_iteration(const MuonGroup& grp, const NsBuffers& buf, cons
     P.total_tiles = P.tiles_per_mat * grp.count;
     P.Xh = X_next;
     prof_begin(OPT_KERNEL_NS_BX, grp.count, grp.A, grp.B, stream);
-    e = launch_gemm(ma, mb, mo, P, grp, stream);
+    e = launch_gemm(ma, mb, mo, mo, P, grp, stream);   // no fp32 output
     prof_end(stream);
     if (e != cudaSuccess) return e;
   }
