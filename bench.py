@@ -192,26 +192,55 @@ def is_muon(w: S.Workload, spec: S.TensorSpec) -> bool:
     return (not w.force_adamw) and len(spec.shape) == 2 and not spec.embedding_or_output
 
 
+FLAT_ALIGN = 64   # elements: every tensor of a flat buffer starts 256 B (fp32) / 128 B (bf16) aligned
+
+
+def flat_layout(numels):
+    """Element offsets of consecutive tensors in one flat buffer, each start
+    rounded up to FLAT_ALIGN elements; and the buffer's length."""
+    offs, o = [], 0
+    for n in numels:
+        offs.append(o)
+        o += -(-int(n) // FLAT_ALIGN) * FLAT_ALIGN
+    return offs, max(o, FLAT_ALIGN)
+
+
+def flat_views(flat, offs, shapes):
+    return [flat[o:o + int(math.prod(sh))].view(sh) for o, sh in zip(offs, shapes)]
+
+
 def build_device_workload(w: S.Workload, device):
+    """Parameters, optimizer state and gradients of the workload on the
+    device.  As in a mixed-precision trainer, every main_grad is a view of one
+    contiguous fp32 gradient buffer and every bf16 model copy a view of one
+    contiguous bf16 buffer (same element offsets), so the e2e leg moves each
+    direction's data with one copy."""
     import torch
     import mixed_precision_optimizer_gb300 as mp
+    shapes = [spec.shape for spec in w.tensors]
+    offs, n_flat = flat_layout(spec.numel for spec in w.tensors)
+    grad_flat = torch.empty(n_flat, dtype=torch.float32, device=device)
+    model_flat = torch.empty(n_flat, dtype=torch.bfloat16, device=device)
+    grads, models = flat_views(grad_flat, offs, shapes), flat_views(model_flat, offs, shapes)
     params, n_muon, n_adamw = [], 0, 0
     for i, spec in enumerate(w.tensors):
         p = torch.empty(spec.shape, dtype=torch.float32, device=device)
         S.torch_init_(p, spec, i)
-        g = torch.empty_like(p)
+        g = grads[i]
         S.torch_grad_(g, spec, i, 1)
         m = torch.zeros_like(p)
         muon = is_muon(w, spec)
         v = None if muon else torch.zeros_like(p)
-        model = p.to(torch.bfloat16)
+        model = models[i]
+        model.copy_(p)
         params.append(mp.Param(p, g, m, v, model, embedding_or_output=spec.embedding_or_output,
                                kind="adamw" if w.force_adamw else None))
         if muon:
             n_muon += spec.numel
         else:
             n_adamw += spec.numel
-    return params, n_muon, n_adamw
+    flat = {"offsets": offs, "shapes": shapes, "grad": grad_flat, "model": model_flat}
+    return params, n_muon, n_adamw, flat
 
 
 def hyper(w: S.Workload):
@@ -421,7 +450,7 @@ def run_ours(args, dist: Dist):
     device = torch.device("cuda", dist.local)
     torch.cuda.set_device(device)
     w = S.WORKLOADS[args.workload]()
-    params, n_muon, n_adamw = build_device_workload(w, device)
+    params, n_muon, n_adamw, flat = build_device_workload(w, device)
     total = n_muon + n_adamw
     ws = mp.alloc_workspace(mp.workspace_size(params, clip=args.clip > 0), device)
     hm, ha = hyper(w)
@@ -528,7 +557,7 @@ def run_ours(args, dist: Dist):
     t += 1 if buckets else 0
 
     # ---- end to end through the public API with host buffers
-    e2e = run_e2e(args, step, params, t, total, dist)
+    e2e = run_e2e(args, step, params, flat, t, total, dist)
     t += args.e2e_steps
 
     value = total * args.steps * dist.world / (elapsed_ms * 1e-3)
@@ -630,43 +659,46 @@ def adamw_buckets(params, hp, reps=5):
     return out
 
 
-def run_e2e(args, step_fn, params, t, total, dist: Dist):
+def run_e2e(args, step_fn, params, flat, t, total, dist: Dist):
     """The same step through the public API, with main_grad arriving from
     pinned host memory and the bf16 model parameters read back to host
-    memory, every step, inside the timed region.  The copies are pipelined
-    with the compute: main_grad and the bf16 model copy are double-buffered on
-    the device, step k uses buffer set k % 2, its gradients are copied in on
-    a host-to-device stream while step k-1 computes, and its model copy is
-    read back on a device-to-host stream while step k+1 computes; events
-    order every reuse of a buffer set."""
+    memory, every step, inside the timed region.  The gradients of all
+    tensors form one contiguous buffer, and so do the bf16 model copies
+    (build_device_workload), so each direction is one copy per step.  The
+    copies are pipelined with the compute: both buffers are double-buffered on
+    the device, step k uses buffer set k % 2, its gradients are copied in on a
+    host-to-device stream while step k-1 computes, and its model copy is read
+    back on a device-to-host stream while step k+1 computes; events order
+    every reuse of a buffer set."""
     import torch
     import mixed_precision_optimizer_gb300 as mp
     if args.e2e_steps <= 0:
         return None
     K = args.e2e_steps
-    arena = PinnedHostArena([(p.main_param.numel(), torch.float32) for p in params]
-                            + [(p.main_param.numel(), torch.bfloat16) for p in params])
-    g_host, b_host = arena.views[:len(params)], arena.views[len(params):]
-    for p, gh in zip(params, g_host):
-        gh.copy_(p.main_grad.reshape(-1))
-    if not all(x.is_pinned() for x in g_host + b_host):
+    n_flat = flat["grad"].numel()
+    arena = PinnedHostArena([(n_flat, torch.float32), (n_flat, torch.bfloat16)])
+    g_host, b_host = arena.views
+    g_host.copy_(flat["grad"])
+    if not (g_host.is_pinned() and b_host.is_pinned()):
         raise SystemExit("e2e: host buffers are not page-locked")
-    # second device set of gradients and model copies
-    sets = [params, [mp.Param(p.main_param, torch.empty_like(p.main_grad), p.exp_avg, p.exp_avg_sq,
-                              torch.empty_like(p.model), p.embedding_or_output, p.kind) for p in params]]
+    # second device set of gradients and model copies, same layout
+    grad2, model2 = torch.empty_like(flat["grad"]), torch.empty_like(flat["model"])
+    g2 = flat_views(grad2, flat["offsets"], flat["shapes"])
+    b2 = flat_views(model2, flat["offsets"], flat["shapes"])
+    sets = [params, [mp.Param(p.main_param, g, p.exp_avg, p.exp_avg_sq, b, p.embedding_or_output, p.kind)
+                     for p, g, b in zip(params, g2, b2)]]
+    flats = [(flat["grad"], flat["model"]), (grad2, model2)]
     prepared_sets = [mp.prepare(x) for x in sets]
     compute = torch.cuda.current_stream()
     s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
     # untimed: one pass of each copy direction over every host buffer
     s_in.wait_stream(compute)
     s_out.wait_stream(compute)
-    for x in sets:
+    for gd, bd in flats:
         with torch.cuda.stream(s_in):
-            for p, gh in zip(x, g_host):
-                p.main_grad.reshape(-1).copy_(gh, non_blocking=True)
+            gd.copy_(g_host, non_blocking=True)
         with torch.cuda.stream(s_out):
-            for p, bh in zip(x, b_host):
-                bh.copy_(p.model.reshape(-1), non_blocking=True)
+            b_host.copy_(bd, non_blocking=True)
     E = lambda: torch.cuda.Event(enable_timing=True)
     h2d_begin, h2d_done = [E() for _ in range(K)], [E() for _ in range(K)]
     step_begin, step_done = [E() for _ in range(K)], [E() for _ in range(K)]
@@ -683,13 +715,12 @@ def run_e2e(args, step_fn, params, t, total, dist: Dist):
     s_out.wait_event(start)
     for k in range(K):
         h0 = time.perf_counter()
-        cur = sets[k % 2]
+        gd, bd = flats[k % 2]
         with torch.cuda.stream(s_in):                  # gradients of step k
             if k >= 2:
                 s_in.wait_event(step_done[k - 2])     # step k-2 finished reading this set
             h2d_begin[k].record(s_in)
-            for p, gh in zip(cur, g_host):
-                p.main_grad.reshape(-1).copy_(gh, non_blocking=True)
+            gd.copy_(g_host, non_blocking=True)
             h2d_done[k].record(s_in)
         h1 = time.perf_counter()
         compute.wait_event(h2d_done[k])
@@ -703,8 +734,7 @@ def run_e2e(args, step_fn, params, t, total, dist: Dist):
         with torch.cuda.stream(s_out):                 # model parameters of step k
             s_out.wait_event(step_done[k])
             d2h_begin[k].record(s_out)
-            for p, bh in zip(cur, b_host):
-                bh.copy_(p.model.reshape(-1), non_blocking=True)
+            b_host.copy_(bd, non_blocking=True)
             d2h_done[k].record(s_out)
         h3 = time.perf_counter()
         host_ms[0] += (h1 - h0) * 1e3
@@ -719,15 +749,16 @@ def run_e2e(args, step_fn, params, t, total, dist: Dist):
     phase = {name: round(sum(b.elapsed_time(d) for b, d in zip(bs, ds)) / K, 3)
              for name, bs, ds in (("h2d", h2d_begin, h2d_done), ("step", step_begin, step_done),
                                   ("d2h", d2h_begin, d2h_done))}
-    h2d = sum(x.numel() * x.element_size() for x in g_host)
-    d2h = sum(x.numel() * x.element_size() for x in b_host)
+    h2d = g_host.numel() * g_host.element_size()
+    d2h = b_host.numel() * b_host.element_size()
     del g_host, b_host
     arena.close()
     return {"value": round(total * K * dist.world / (ms * 1e-3), 1), "unit": UNIT,
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
             "steps": K, "ms_per_step": round(ms / K, 3),
-            "pipelined": "main_grad and bf16 model double-buffered; H2D, step and D2H on three streams; "
-                         "the first step's H2D and the last step's D2H are not overlapped and are included",
+            "pipelined": "main_grad and bf16 model buffers (each one contiguous buffer, one copy per direction) "
+                         "double-buffered; H2D, step and D2H on three streams; the first step's H2D and the "
+                         "last step's D2H are not overlapped and are included",
             "host_buffers": f"one cudaHostAlloc arena of {arena.nbytes} bytes (torch pinned memory); "
                             "copies warmed once before timing",
             "host_wall_ms_per_step": round(wall_ms / K, 3),
