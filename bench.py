@@ -50,7 +50,7 @@ def parse():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="llama16_mixed", choices=sorted(S.WORKLOADS))
-    ap.add_argument("--e2e-steps", type=int, default=10,
+    ap.add_argument("--e2e-steps", type=int, default=20,
                     help="steps of the end-to-end leg; its time includes filling and draining the copy pipeline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--compare-cublas", action="store_true",

@@ -12,7 +12,8 @@ sampled outputs the oracle can compute one by one.
 
 Inputs are drawn on the GPU with the seeded generators of synthetic/; the
 sampled inputs are copied back before each step, so every expected value comes
-from the oracle."""
+from the oracle.  Gradients and bf16 model copies are views of flat buffers, as
+in the bench."""
 
 import math
 
@@ -20,6 +21,7 @@ import numpy as np
 import pytest
 
 from gpu_helpers import bf16_host, host, require_gpu, torch
+import bench
 import mixed_precision_optimizer_gb300 as mp
 from oracle import adamw as OA
 from oracle import muon as OM
@@ -47,15 +49,20 @@ def free_gb():
 
 
 def build(w, muon_route):
+    """The workload in the layout bench.py times: every main_grad a view of one
+    flat fp32 buffer and every bf16 model copy a view of one flat bf16 buffer."""
+    shapes = [spec.shape for spec in w.tensors]
+    offs, n_flat = bench.flat_layout(spec.numel for spec in w.tensors)
+    grads = bench.flat_views(torch.empty(n_flat, dtype=torch.float32, device="cuda"), offs, shapes)
+    models = bench.flat_views(torch.empty(n_flat, dtype=torch.bfloat16, device="cuda"), offs, shapes)
     params, specs = [], []
     for i, spec in enumerate(w.tensors):
         p = torch.empty(spec.shape, dtype=torch.float32, device="cuda")
         S.torch_init_(p, spec, i)
-        g = torch.empty_like(p)
         m = torch.zeros_like(p)
         v = None if muon_route(spec) else torch.zeros_like(p)
-        b = p.to(torch.bfloat16)
-        params.append(mp.Param(p, g, m, v, b, embedding_or_output=spec.embedding_or_output,
+        models[i].copy_(p)
+        params.append(mp.Param(p, grads[i], m, v, models[i], embedding_or_output=spec.embedding_or_output,
                                kind="adamw" if w.force_adamw else None))
         specs.append(spec)
     return params, specs
