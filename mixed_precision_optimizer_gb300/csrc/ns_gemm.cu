@@ -563,9 +563,13 @@ ns_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
       // CTA's producer reads it there.  Both CTAs load their own halves;
       // completion is counted on the even CTA's full barrier, which expects
       // both halves' bytes.
-      uint32_t it = 0;
       bool ok = true;
       bool issued = false;
+      // stage s of the ring, phase parity ph; addresses of stage 0 (a stage is a fixed offset)
+      const uint32_t full0 = smem_u32(&full[0]), empty0 = smem_u32(&empty[0]);
+      const uint32_t full0_even = peer_addr(full0, 0);   // both CTAs' loads complete on the even CTA's barrier
+      const uint32_t sa0 = smem_u32(stage_a), sb0 = smem_u32(stage_b);
+      uint32_t s = 0, ph = 0;
       const uint32_t ring_odd = peer_addr(smem_u32(const_cast<int*>(tile_ring)), 1);
       const uint32_t tfull_odd = peer_addr(smem_u32(&tile_full[0]), 1);
       const uint32_t tempty_even = peer_addr(smem_u32(&tile_empty[0]), 0);
@@ -594,24 +598,28 @@ ns_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
         const Tile t = decode_tile(P, tile);
         const int arow = t.tm * BM_PAIR + static_cast<int>(rank) * BM;
         const int brow = t.tn * BN + static_cast<int>(rank) * BN_HALF;   // B rows (K-major) or columns (MN-major)
-        for (int kb = 0; kb < P.k_blocks; ++kb, ++it) {
-          const uint32_t s = it % kStages, ph = (it / kStages) & 1u;
-          if (!mbar_wait(smem_u32(&empty[s]), ph ^ 1u, abort_flag, P.status, kStatusTimeoutEmpty)) {
+        for (int kb = 0; kb < P.k_blocks; ++kb) {
+          if (!mbar_wait(empty0 + 8 * s, ph ^ 1u, abort_flag, P.status, kStatusTimeoutEmpty)) {
             ok = false;
             break;
           }
-          const uint32_t fb = peer_addr(smem_u32(&full[s]), 0);
-          if (rank == 0) mbar_expect_tx(smem_u32(&full[s]), 2 * kStageBytes);
+          const uint32_t fb = full0_even + 8 * s;
+          if (rank == 0) mbar_expect_tx(full0 + 8 * s, 2 * kStageBytes);
           const int kx = kb * kElemsPerKBlock;
-          tma_load_3d(smem_u32(stage_a + s * kStageA), &map_a, fb, kx, arow, t.mat);
+          const uint32_t sa = sa0 + s * kStageA, sb = sb0 + s * kStageB;
+          tma_load_3d(sa, &map_a, fb, kx, arow, t.mat);
           if (b_mn) {
             // MN-major B: this CTA's 128 columns as two 64-column blocks of 64 K rows
-            tma_load_3d(smem_u32(stage_b + s * kStageB), &map_b, fb, brow, kx, t.mat);
-            tma_load_3d(smem_u32(stage_b + s * kStageB + kMnBlockBytes), &map_b, fb, brow + 64, kx, t.mat);
+            tma_load_3d(sb, &map_b, fb, brow, kx, t.mat);
+            tma_load_3d(sb + kMnBlockBytes, &map_b, fb, brow + 64, kx, t.mat);
           } else {
-            tma_load_3d(smem_u32(stage_b + s * kStageB), &map_b, fb, kx, brow, t.mat);
+            tma_load_3d(sb, &map_b, fb, kx, brow, t.mat);
           }
           issued = true;
+          if (++s == kStages) {
+            s = 0;
+            ph ^= 1u;
+          }
         }
       }
       if (!ok && issued) {
@@ -625,7 +633,13 @@ ns_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
     if (lane == 0 && rank == 0) {
       // ------------------------------------- MMA issuer (even CTA only) --
       const uint32_t idesc = b_mn ? instr_desc(true) : instr_desc(false);
-      uint32_t it = 0;
+      // operand descriptors of stage 0: a stage and a K step are offsets of the
+      // start-address field (bits 0-13, address >> 4; shared memory stays below 256 KB)
+      const uint64_t adesc0 = smem_desc(smem_u32(stage_a));
+      const uint64_t bdesc0 = b_mn ? smem_desc_mn(smem_u32(stage_b)) : smem_desc(smem_u32(stage_b));
+      const uint32_t b_kstep = b_mn ? (16 * kRowBytes) >> 4 : 32 >> 4;   // 16 MN-major rows or 32 bytes of a K-major row
+      const uint32_t full0 = smem_u32(&full[0]), empty0 = smem_u32(&empty[0]);
+      uint32_t s = 0, ph = 0;
       bool ok = true;
       for (uint32_t lt = 0; ok; ++lt) {   // lt: this pair's tile sequence number
         const uint32_t slot = lt % kTileSlots, sph = (lt / kTileSlots) & 1u;
@@ -640,21 +654,23 @@ ns_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
-        for (int kb = 0; kb < P.k_blocks; ++kb, ++it) {
-          const uint32_t s = it % kStages, ph = (it / kStages) & 1u;
-          if (!mbar_wait(smem_u32(&full[s]), ph, abort_flag, P.status, kStatusTimeoutFull)) {
+        for (int kb = 0; kb < P.k_blocks; ++kb) {
+          // the operands were written by TMA and completed on this barrier:
+          // its wait orders them before the MMAs, no tcgen05 fence needed
+          if (!mbar_wait(full0 + 8 * s, ph, abort_flag, P.status, kStatusTimeoutFull)) {
             ok = false;
             break;
           }
-          tc_fence_after();
-          const uint32_t a_addr = smem_u32(stage_a + s * kStageA);
-          const uint32_t b_addr = smem_u32(stage_b + s * kStageB);
+          const uint64_t ad = adesc0 + s * (kStageA >> 4);
+          const uint64_t bd = bdesc0 + s * (kStageB >> 4);
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {   // 4 MMAs of 16 K each: 32 bytes along a K-major row, 16 MN-major rows
-            const uint64_t bdesc = b_mn ? smem_desc_mn(b_addr + kk * 16 * kRowBytes) : smem_desc(b_addr + kk * 32);
-            mma(d_tmem, smem_desc(a_addr + kk * 32), bdesc, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < 4; ++kk)   // 4 MMAs of 16 K each
+            mma(d_tmem, ad + 2 * kk, bd + b_kstep * kk, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+          mma_commit_pair(empty0 + 8 * s);
+          if (++s == kStages) {
+            s = 0;
+            ph ^= 1u;
           }
-          mma_commit_pair(smem_u32(&empty[s]));
         }
         if (!ok) break;
         mma_commit_pair(smem_u32(&acc_full[acc]));
