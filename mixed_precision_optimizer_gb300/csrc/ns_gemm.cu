@@ -171,6 +171,16 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// The same for a 4-D tensor map (the MN-major operand: column blocks as a dimension).
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x,
+                                            int y, int z, int w) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(bar)
+      : "memory");
+}
+
 // Tile store from this CTA's shared memory to global memory (bulk async-group
 // of the issuing thread).
 __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int x, int y, int z) {
@@ -609,9 +619,9 @@ ns_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
           const uint32_t sa = sa0 + s * kStageA, sb = sb0 + s * kStageB;
           tma_load_3d(sa, &map_a, fb, kx, arow, t.mat);
           if (b_mn) {
-            // MN-major B: this CTA's 128 columns as two 64-column blocks of 64 K rows
-            tma_load_3d(sb, &map_b, fb, brow, kx, t.mat);
-            tma_load_3d(sb + kMnBlockBytes, &map_b, fb, brow + 64, kx, t.mat);
+            // MN-major B: this CTA's 128 columns as two 64-column blocks of 64 K
+            // rows, one box of the 4-D map (blocks land kMnBlockBytes apart)
+            tma_load_4d(sb, &map_b, fb, 0, kx, brow / 64, t.mat);
           } else {
             tma_load_3d(sb, &map_b, fb, kx, brow, t.mat);
           }
@@ -846,6 +856,25 @@ cudaError_t make_map(CUtensorMap* map, const void* base, int64_t inner, int64_t 
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// 4-D map over `count` row-major fp16 matrices [rows][inner] read as an MN-major
+// operand: (64 columns, rows, inner / 64 column blocks, count), box (64, 64, 2,
+// 1), 128-byte swizzle.  One box is 64 rows of two 64-column blocks, each block
+// 64 x 128 bytes and stored 8 KB apart in shared memory.
+cudaError_t make_map_mn(CUtensorMap* map, const void* base, int64_t inner, int64_t rows, int64_t count) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return cudaErrorNotSupported;
+  const cuuint64_t dims[4] = {64, static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(inner / 64),
+                              static_cast<cuuint64_t>(count)};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(inner * 2), 128,
+                                 static_cast<cuuint64_t>(inner * rows * 2)};
+  const cuuint32_t box[4] = {64, 64, 2, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 // 3-D map over `count` row-major fp16 matrices [rows][inner] for the C X output:
 // box 32 x 32 elements (64-byte rows), 64-byte swizzle.
 cudaError_t make_out_map(CUtensorMap* map, const void* base, int64_t inner, int64_t rows, int64_t count) {
@@ -957,12 +986,12 @@ cudaError_t launch_ns_iteration(const MuonGroup& grp, const NsBuffers& buf, cons
     prof_end(stream);
     if (e != cudaSuccess) return e;
   }
-  // bx: X' = C X  (operands: fp16 C [Ap][Ap] K-major, fp16 X [Ap][Bp] MN-major
-  // in 64-column x 64-row boxes, K = Ap)
+  // bx: X' = C X  (operands: fp16 C [Ap][Ap] K-major, fp16 X [Ap][Bp] MN-major,
+  // one box of 64 K rows x two 64-column blocks per stage, K = Ap)
   {
     CUtensorMap ma, mb;
     if ((e = make_map(&ma, buf.Ch, Ap, Ap, cnt, BM)) != cudaSuccess) return e;
-    if ((e = make_map(&mb, X, Bp, Ap, cnt, 64)) != cudaSuccess) return e;
+    if ((e = make_map_mn(&mb, X, Bp, Ap, cnt)) != cudaSuccess) return e;
     CUtensorMap mo = mb;   // the last iteration updates W instead
     if (it != s.ns_steps - 1 && (e = make_out_map(&mo, X_next, Bp, Ap, cnt)) != cudaSuccess) return e;
     GemmParams P = base;
