@@ -37,6 +37,9 @@
 //             and writes them with TMA stores; the last C X, a read-modify-
 //             write of W in W's own orientation, uses the same 8 KB as a
 //             transpose slab and plain loads and stores
+//   warp 10   tile scheduler in the even CTA: claims tiles from a launch-wide
+//             counter and publishes them to both CTAs through a ring of
+//             tile indices, ahead of the roles that read it
 // Per MMA each SM stages 8 KB of operands (A and B halves) instead of the
 // 12 KB a single-CTA 128 x 256 tile needs.
 //
@@ -70,7 +73,7 @@ constexpr int kStageB = BN_HALF * kRowBytes;   // 16 KB: this CTA's 128 rows of 
 constexpr int kStageBytes = kStageA + kStageB; // per CTA; the pair's stage is twice this
 constexpr int kMnBlockBytes = 64 * kRowBytes;   // MN-major B: one 64-column block of 64 K rows
 constexpr int kEpiWarps = 8;                   // two warps per TMEM lane quarter
-constexpr int kThreads = 64 + 32 * kEpiWarps;  // TMA warp, MMA warp, epilogue warps
+constexpr int kThreads = 96 + 32 * kEpiWarps;  // TMA warp, MMA warp, epilogue warps, scheduler warp
 constexpr int kTmemCols = 512;                 // 2 accumulators x 256 fp32 columns
 constexpr int kSlabWords = 32 * 33;            // 32 x 32 fp32 transpose slab, padded rows
 constexpr int kWarpScratch = 8192;             // per epilogue warp: transpose slab or TMA-store staging
@@ -82,10 +85,10 @@ static_assert(kOutBlockBytes32 + 2 * kOutBlockBytes <= kWarpScratch, "gram stagi
 constexpr uint32_t kSmemBytes = kStages * kStageBytes + kSlabBytes + 1024 /*align*/ + 256 /*barriers*/;
 static_assert(kSmemBytes <= 232448, "dynamic shared memory above the 227 KB a CTA may use");
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
-constexpr int kTileSlots = 6;                  // tile-index ring between the scheduler and the other roles
-// consumers of one ring slot, all arriving on the even CTA's barrier: the MMA
-// warp, the odd CTA's producer, and every epilogue warp of both CTAs
-constexpr uint32_t kTileConsumers = 1 + 1 + 2 * kEpiWarps;
+constexpr int kTileSlots = 3;                  // tile-index ring between the scheduler and the other roles
+// consumers of one ring slot, all arriving on the even CTA's barrier: both
+// CTAs' producers, the MMA warp, and every epilogue warp of both CTAs
+constexpr uint32_t kTileConsumers = 2 + 1 + 2 * kEpiWarps;
 constexpr int kBarrierBytes = (2 * kStages + 5 + 2 * kTileSlots) * 8 + 8 + 4 * kTileSlots;
 static_assert(kBarrierBytes <= 256, "barrier block larger than its 256-byte reservation");
 
@@ -563,16 +566,9 @@ ns_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------ TMA producer --
-      // The even CTA's producer also schedules.  Each pair starts with tile
-      // `pair` and then claims tiles from a launch-wide counter, so the tiles
-      // in flight are always the most recently claimed ones -- neighbours in
-      // the tile order, which share operand panels in L2 -- however unevenly
-      // the pairs progress (with a fixed stride they drift apart over a long
-      // launch and re-read their panels from DRAM).  Every index, and finally
-      // one past the end, goes to both CTAs through the tile ring; the odd
-      // CTA's producer reads it there.  Both CTAs load their own halves;
-      // completion is counted on the even CTA's full barrier, which expects
-      // both halves' bytes.
+      // Tiles come from the scheduler warp through the tile ring.  Both CTAs
+      // load their own halves; completion is counted on the even CTA's full
+      // barrier, which expects both halves' bytes.
       bool ok = true;
       bool issued = false;
       // stage s of the ring, phase parity ph; addresses of stage 0 (a stage is a fixed offset)
@@ -580,22 +576,17 @@ ns_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
       const uint32_t full0_even = peer_addr(full0, 0);   // both CTAs' loads complete on the even CTA's barrier
       const uint32_t sa0 = smem_u32(stage_a), sb0 = smem_u32(stage_b);
       uint32_t s = 0, ph = 0;
-      const uint32_t ring_odd = peer_addr(smem_u32(const_cast<int*>(tile_ring)), 1);
-      const uint32_t tfull_odd = peer_addr(smem_u32(&tile_full[0]), 1);
       const uint32_t tempty_even = peer_addr(smem_u32(&tile_empty[0]), 0);
       for (uint32_t seq = 0; ok; ++seq) {
         const uint32_t slot = seq % kTileSlots, sph = (seq / kTileSlots) & 1u;
         int tile;
         if (rank == 0) {
-          if (!mbar_wait(smem_u32(&tile_empty[slot]), sph ^ 1u, abort_flag, P.status, kStatusTimeoutTile)) {
+          if (!mbar_wait(smem_u32(&tile_full[slot]), sph, abort_flag, P.status, kStatusTimeoutTile)) {
             ok = false;
             break;
           }
-          tile = seq == 0 ? pair : npairs + static_cast<int>(atomicAdd(P.sched, 1u));
-          tile_ring[slot] = tile;
-          st_cluster_u32(ring_odd + 4 * slot, static_cast<uint32_t>(tile));
-          mbar_arrive_local(smem_u32(&tile_full[slot]));
-          mbar_arrive_remote(tfull_odd + 8 * slot);
+          tile = tile_ring[slot];
+          mbar_arrive_local(smem_u32(&tile_empty[slot]));
         } else {
           if (!mbar_wait_acq_cluster(smem_u32(&tile_full[slot]), sph, abort_flag, P.status, kStatusTimeoutTile)) {
             ok = false;
@@ -691,7 +682,7 @@ ns_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
       while (!mbar_try(smem_u32(drain), 0) && global_ns() - t0 < kWaitLimitNs) {
       }
     }
-  } else {
+  } else if (warp < 2 + kEpiWarps) {
     // ------------------------------------------------------ epilogue --
     const int quarter = warp & 3;             // TMEM lanes this warp may access
     const int half = (warp - 2) >> 2;         // which 128 of the 256 columns
@@ -800,6 +791,30 @@ ns_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
       mbar_arrive_remote(empty_even + acc * static_cast<uint32_t>(sizeof(uint64_t)));
     }
     if (lane == 0 && out_blocks > 0) bulk_wait_all();   // stores complete before the CTA exits
+  } else if (lane == 0 && rank == 0) {
+    // ----------------------------------------- tile scheduler (even CTA) --
+    // Each pair starts with tile `pair` and then claims tiles from a
+    // launch-wide counter, so the tiles in flight are always the most
+    // recently claimed ones -- neighbours in the tile order, which share
+    // operand panels in L2 -- however unevenly the pairs progress (with a
+    // fixed stride they drift apart over a long launch and re-read their
+    // panels from DRAM).  Every index, and finally one past the end, goes to
+    // both CTAs through the tile ring.  Running in its own warp, the scheduler
+    // fills the ring ahead of the roles that read it, so neither the
+    // counter's round trip nor the publication to the odd CTA falls between
+    // two tiles of the producers.
+    const uint32_t ring_odd = peer_addr(smem_u32(const_cast<int*>(tile_ring)), 1);
+    const uint32_t tfull_odd = peer_addr(smem_u32(&tile_full[0]), 1);
+    for (uint32_t seq = 0;; ++seq) {
+      const uint32_t slot = seq % kTileSlots, sph = (seq / kTileSlots) & 1u;
+      if (!mbar_wait(smem_u32(&tile_empty[slot]), sph ^ 1u, abort_flag, P.status, kStatusTimeoutTile)) break;
+      const int tile = seq == 0 ? pair : npairs + static_cast<int>(atomicAdd(P.sched, 1u));
+      tile_ring[slot] = tile;
+      st_cluster_u32(ring_odd + 4 * slot, static_cast<uint32_t>(tile));
+      mbar_arrive_local(smem_u32(&tile_full[slot]));
+      mbar_arrive_remote(tfull_odd + 8 * slot);
+      if (tile >= P.total_tiles) break;
+    }
   }
 
   tc_fence_before();
