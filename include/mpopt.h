@@ -298,6 +298,25 @@ MPOPT_API opt_status opt_newton_schulz_noalloc(const float* G, float* O, int64_t
 MPOPT_API opt_status opt_device_status(const void* workspace, void* stream);
 
 /*
+ * Self-test of the bounded device-side waits (for tests of the failure path).
+ * Runs opt_newton_schulz on G (rows x cols; 5 iterations with the quintic
+ * coefficients of "02 · Optimizer：算法与 infra" §5.2, eps 1e-7) with one TMA
+ * stage of the first X X^T launch withheld: the even CTA of the first CTA pair
+ * never signals it, so the MMA issuer's wait for that stage runs out after
+ * about 2 s.  The kernel then records the timeout in the workspace header,
+ * every role of the CTA pair leaves its loop (each of their waits is bounded
+ * too), and the remaining launches run to completion on whatever the buffers
+ * hold.  Nothing faults, and the CUDA context and the workspace stay usable:
+ * opt_device_status() returns OPT_ERR_DEVICE_TIMEOUT, and the next call on
+ * the same workspace clears the header and runs normally.  O receives
+ * unspecified values.  Arguments, workspace size (opt_workspace_size of one
+ * OPT_KIND_MUON tensor of this shape) and host-side errors are those of
+ * opt_newton_schulz.
+ */
+MPOPT_API opt_status opt_selftest_wait_timeout(const float* G, float* O, int64_t rows, int64_t cols,
+                                               void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Optional launch instrumentation (off by default).  After
  *   opt_profile_launches(events, info, capacity, &count)
  * every kernel this library launches from the calling thread is bracketed by

@@ -27,6 +27,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libmpopt.so")
 
 OPT_OK = 0
+OPT_ERR_DEVICE_TIMEOUT = 6
 STATUS_NAMES = {0: "OPT_OK", 1: "OPT_ERR_INVALID_ARG", 2: "OPT_ERR_UNSUPPORTED", 3: "OPT_ERR_MISALIGNED",
                 4: "OPT_ERR_WORKSPACE", 5: "OPT_ERR_CUDA", 6: "OPT_ERR_DEVICE_TIMEOUT"}
 KIND_AUTO, KIND_ADAMW, KIND_MUON = 0, 1, 2
@@ -73,7 +74,7 @@ _lib = None
 
 EXPORTED = ("opt_workspace_size", "opt_adamw_step", "opt_muon_step", "opt_mixed_step", "opt_mixed_step_clipped",
             "opt_newton_schulz", "opt_newton_schulz_noalloc", "opt_reload_model_params", "opt_device_status",
-            "opt_profile_launches",
+            "opt_selftest_wait_timeout", "opt_profile_launches",
             "opt_strerror",
             "opt_last_cuda_error", "opt_abi_version")
 
@@ -119,6 +120,8 @@ def lib():
     L.opt_reload_model_params.restype = ctypes.c_int
     L.opt_device_status.argtypes = [vp, vp]
     L.opt_device_status.restype = ctypes.c_int
+    L.opt_selftest_wait_timeout.argtypes = [vp, vp, i64, i64, vp, sz, vp]
+    L.opt_selftest_wait_timeout.restype = ctypes.c_int
     L.opt_profile_launches.argtypes = [vp, ctypes.POINTER(OptLaunchInfo), i32, ctypes.POINTER(i32)]
     L.opt_profile_launches.restype = ctypes.c_int
     L.opt_strerror.argtypes = [ctypes.c_int]
@@ -356,6 +359,21 @@ def device_status(workspace, stream=None) -> int:
     if workspace is None:
         return OPT_OK
     return int(lib().opt_device_status(ctypes.c_void_p(workspace.data_ptr()), _stream(stream)))
+
+
+def selftest_wait_timeout(G, out, workspace, stream=None):
+    """Newton-Schulz on G with one TMA stage withheld, so that a bounded
+    device-side wait runs out (about 2 s): device_status() then reports
+    OPT_ERR_DEVICE_TIMEOUT and the workspace stays usable.  For tests of the
+    failure path; `out` receives unspecified values."""
+    import torch
+    if G.dim() != 2:
+        raise ValueError("G must be 2-D")
+    rows, cols = G.shape
+    gp = _ptr(G, torch.float32, "G", rows * cols)
+    op = _ptr(out, torch.float32, "out", rows * cols)
+    w, nb = _ws(workspace)
+    _check(lib().opt_selftest_wait_timeout(gp, op, rows, cols, w, nb, _stream(stream)), "opt_selftest_wait_timeout")
 
 
 class LaunchProfiler:

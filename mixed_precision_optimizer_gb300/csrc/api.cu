@@ -317,6 +317,7 @@ struct MuonPlanHp {
   int scale_mode;            // OPT_SCALE_*
   int no_ortho;              // plain momentum SGD
   const float* schedule;     // host (a, b, c) per iteration, or nullptr: (a, b, c) every time
+  int stall;                 // self-test of the bounded waits (opt_selftest_wait_timeout)
 };
 
 // lr * update scale for a parameter of shape R x C ("02 · Optimizer：算法与
@@ -383,6 +384,7 @@ opt_status run_muon_class(const MuonPlanHp& hp, const ShapeClass& cls, uint8_t* 
       s.ns_steps = hp.ns_steps;
       s.ns_only = hp.ns_only;
       s.grad_scale = hp.grad_scale;
+      s.stall_first_stage = (hp.stall && g0 == 0) ? 1 : 0;
       prof_begin(OPT_KERNEL_MUON_PREP, grp.count, grp.A, grp.B, stream);
       cudaError_t e = launch_muon_momentum(grp, buf, s, stream);
       prof_end(stream);
@@ -632,8 +634,10 @@ opt_status opt_reload_model_params(const opt_tensor* tensors, int32_t n, void* s
   return OPT_OK;
 }
 
-opt_status opt_newton_schulz(const float* G, float* O, int64_t rows, int64_t cols, int32_t ns_steps, float a,
-                             float b, float c, float eps, void* workspace, size_t workspace_bytes, void* stream) {
+// opt_newton_schulz; `stall` is the self-test of the bounded device waits
+static opt_status newton_schulz_impl(const float* G, float* O, int64_t rows, int64_t cols, int32_t ns_steps,
+                                     float a, float b, float c, float eps, void* workspace, size_t workspace_bytes,
+                                     void* stream, int stall) {
   if (rows < 0 || cols < 0 || ns_steps < 0 || ns_steps > 16) return OPT_ERR_INVALID_ARG;
   if (!std::isfinite(a) || !std::isfinite(b) || !std::isfinite(c) || !std::isfinite(eps) || eps < 0.f)
     return OPT_ERR_INVALID_ARG;
@@ -658,9 +662,21 @@ opt_status opt_newton_schulz(const float* G, float* O, int64_t rows, int64_t col
   cudaError_t e = cudaMemsetAsync(ws, 0, kHeaderBytes, s);
   if (e != cudaSuccess) return cuda_fail(e, "workspace header");
   MuonPlanHp hp{0.f, 0.f, 0.f, eps, a, b, c, 0.f, 0, ns_steps, 1};
+  hp.stall = stall;
   float* outs[1] = {O};
   return run_muon_class(hp, classes[0], ws + kHeaderBytes, workspace_bytes - kHeaderBytes,
                         reinterpret_cast<uint32_t*>(ws), s, outs);
+}
+
+opt_status opt_newton_schulz(const float* G, float* O, int64_t rows, int64_t cols, int32_t ns_steps, float a,
+                             float b, float c, float eps, void* workspace, size_t workspace_bytes, void* stream) {
+  return newton_schulz_impl(G, O, rows, cols, ns_steps, a, b, c, eps, workspace, workspace_bytes, stream, 0);
+}
+
+opt_status opt_selftest_wait_timeout(const float* G, float* O, int64_t rows, int64_t cols, void* workspace,
+                                     size_t workspace_bytes, void* stream) {
+  return newton_schulz_impl(G, O, rows, cols, 5, 3.4445f, -4.7750f, 2.0315f, 1e-7f, workspace, workspace_bytes,
+                            stream, 1);
 }
 
 opt_status opt_device_status(const void* workspace, void* stream) {

@@ -106,6 +106,7 @@ struct MuonScalars {
   int no_normalize;   // plain momentum SGD: the direction is gtilde itself
   const float* grad_scale;  // device scalar multiplying every gradient (clipping), or nullptr
   float sched[16][3]; // (a, b, c) of each iteration
+  int stall_first_stage;    // self-test: withhold one TMA stage of the first X X^T launch
 };
 
 // Elementwise pass 1 (momentum, norm partials): fixed elements per block so the

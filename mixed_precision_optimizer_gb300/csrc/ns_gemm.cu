@@ -109,6 +109,7 @@ struct GemmParams {
   int ns_only;
   uint32_t* status;
   uint32_t* sched;      // [0]: tiles claimed after the first, [1]: CTAs finished
+  int stall;            // self-test: the even CTA of pair 0 never signals its first stage
 };
 
 // ------------------------------------------------------------ PTX helpers --
@@ -576,6 +577,9 @@ ns_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
       const uint32_t full0_even = peer_addr(full0, 0);   // both CTAs' loads complete on the even CTA's barrier
       const uint32_t sa0 = smem_u32(stage_a), sb0 = smem_u32(stage_b);
       uint32_t s = 0, ph = 0;
+      // self-test of the bounded waits: the even CTA of pair 0 withholds its
+      // first stage, so the MMA issuer's wait for it runs out
+      const bool withhold = P.stall != 0 && rank == 0 && pair == 0;
       const uint32_t tempty_even = peer_addr(smem_u32(&tile_empty[0]), 0);
       for (uint32_t seq = 0; ok; ++seq) {
         const uint32_t slot = seq % kTileSlots, sph = (seq / kTileSlots) & 1u;
@@ -604,19 +608,21 @@ ns_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
             ok = false;
             break;
           }
-          const uint32_t fb = full0_even + 8 * s;
-          if (rank == 0) mbar_expect_tx(full0 + 8 * s, 2 * kStageBytes);
-          const int kx = kb * kElemsPerKBlock;
-          const uint32_t sa = sa0 + s * kStageA, sb = sb0 + s * kStageB;
-          tma_load_3d(sa, &map_a, fb, kx, arow, t.mat);
-          if (b_mn) {
-            // MN-major B: this CTA's 128 columns as two 64-column blocks of 64 K
-            // rows, one box of the 4-D map (blocks land kMnBlockBytes apart)
-            tma_load_4d(sb, &map_b, fb, 0, kx, brow / 64, t.mat);
-          } else {
-            tma_load_3d(sb, &map_b, fb, kx, brow, t.mat);
+          if (!(withhold && seq == 0 && kb == 0)) {
+            const uint32_t fb = full0_even + 8 * s;
+            if (rank == 0) mbar_expect_tx(full0 + 8 * s, 2 * kStageBytes);
+            const int kx = kb * kElemsPerKBlock;
+            const uint32_t sa = sa0 + s * kStageA, sb = sb0 + s * kStageB;
+            tma_load_3d(sa, &map_a, fb, kx, arow, t.mat);
+            if (b_mn) {
+              // MN-major B: this CTA's 128 columns as two 64-column blocks of 64 K
+              // rows, one box of the 4-D map (blocks land kMnBlockBytes apart)
+              tma_load_4d(sb, &map_b, fb, 0, kx, brow / 64, t.mat);
+            } else {
+              tma_load_3d(sb, &map_b, fb, kx, brow, t.mat);
+            }
+            issued = true;
           }
-          issued = true;
           if (++s == kStages) {
             s = 0;
             ph ^= 1u;
@@ -977,6 +983,7 @@ cudaError_t launch_ns_iteration(const MuonGroup& grp, const NsBuffers& buf, cons
     P.total_tiles = P.tiles_per_mat * grp.count;
     P.Af = buf.Af;
     P.Ah = buf.Ah;
+    P.stall = (s.stall_first_stage && it == 0) ? 1 : 0;
     prof_begin(OPT_KERNEL_NS_GRAM, grp.count, grp.A, grp.B, stream);
     e = launch_gemm(ma, mb, mo, mo32, P, grp, stream);
     prof_end(stream);
