@@ -145,7 +145,8 @@ enum : uint32_t {
   kStatusTimeoutAcc = 3,      // epilogue waited too long for an accumulator
   kStatusTimeoutAccFree = 4,  // MMA waited too long for a free accumulator
   kStatusTimeoutDrain = 5,
-  kStatusTimeoutTile = 6      // a role waited too long for the next tile index
+  kStatusTimeoutTile = 6,     // a role waited too long for the next tile index
+  kStatusTimeoutWload = 7     // an epilogue warp waited too long for its block of W
 };
 
 // Workspace-header words (uint32 index) of the GEMM tile scheduler: the count

@@ -35,8 +35,10 @@
 //             output blocks (and, for the symmetric products, their mirror
 //             blocks, written column-wise) in its own 8 KB of shared memory
 //             and writes them with TMA stores; the last C X, a read-modify-
-//             write of W in W's own orientation, uses the same 8 KB as a
-//             transpose slab and plain loads and stores
+//             write of W in W's own orientation, loads each 32 x 32 block of
+//             W there by TMA, updates it in place and stores it and its bf16
+//             copy by TMA (plain loads and stores through a transpose slab
+//             when a matrix does not meet TMA's alignment rules)
 //   warp 10   tile scheduler in the even CTA: claims tiles from a launch-wide
 //             counter and publishes them to both CTAs through a ring of
 //             tile indices, ahead of the roles that read it
@@ -89,7 +91,7 @@ constexpr int kTileSlots = 3;                  // tile-index ring between the sc
 // consumers of one ring slot, all arriving on the even CTA's barrier: both
 // CTAs' producers, the MMA warp, and every epilogue warp of both CTAs
 constexpr uint32_t kTileConsumers = 2 + 1 + 2 * kEpiWarps;
-constexpr int kBarrierBytes = (2 * kStages + 5 + 2 * kTileSlots) * 8 + 8 + 4 * kTileSlots;
+constexpr int kBarrierBytes = (2 * kStages + 5 + 2 * kTileSlots + kEpiWarps) * 8 + 8 + 4 * kTileSlots;
 static_assert(kBarrierBytes <= 256, "barrier block larger than its 256-byte reservation");
 
 struct GemmParams {
@@ -110,7 +112,17 @@ struct GemmParams {
   uint32_t* status;
   uint32_t* sched;      // [0]: tiles claimed after the first, [1]: CTAs finished
   int stall;            // self-test: the even CTA of pair 0 never signals its first stage
+  int w_tma;            // last C X: W and its bf16 copy move through TMA, with the maps in WMaps
 };
+
+// Tensor maps of the last C X's update, one pair per matrix of the group
+// (a kernel parameter: 16 KB).  Both have a 32 x 32 box in W's own layout.
+struct WMaps {
+  CUtensorMap w[kMaxGroup];    // fp32 master W [R][C], 128-byte swizzle
+  CUtensorMap wb[kMaxGroup];   // bf16 model copy [R][C], 64-byte swizzle
+};
+static_assert(4 * sizeof(CUtensorMap) + sizeof(GemmParams) + sizeof(MuonGroup) + sizeof(WMaps) + 256 <= 32764,
+              "kernel parameters above the 32 KB parameter space");
 
 // ------------------------------------------------------------ PTX helpers --
 
@@ -183,6 +195,32 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map
       " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(bar)
       : "memory");
+}
+
+// L2 policy for data touched once (W of the last C X): evicted first, so
+// that it does not push the GEMM operands out of L2.
+__device__ __forceinline__ uint64_t l2_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+// A 2-D box into this CTA's own shared memory, completing on this CTA's
+// barrier, with an L2 policy.
+__device__ __forceinline__ void tma_load_2d_local(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y,
+                                                  uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "l"(pol)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int x, int y, uint64_t pol) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group.L2::cache_hint [%0, {%1, %2}], [%3], %4;" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y), "r"(src), "l"(pol)
+               : "memory");
 }
 
 // Tile store from this CTA's shared memory to global memory (bulk async-group
@@ -504,7 +542,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 ns_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                const __grid_constant__ CUtensorMap map_out, const __grid_constant__ CUtensorMap map_out32,
                const __grid_constant__ GemmParams P,
-               const __grid_constant__ MuonGroup grp) {
+               const __grid_constant__ MuonGroup grp, const __grid_constant__ WMaps wm) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* stage_a = smem;                                  // kStages x 16 KB
@@ -518,7 +556,8 @@ ns_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
   uint64_t* drain = acc_empty + 2;           // [1]        even CTA: all MMAs complete
   uint64_t* tile_full = drain + 1;           // [kTileSlots] both CTAs: next tile index published
   uint64_t* tile_empty = tile_full + kTileSlots;   // [kTileSlots] even CTA: every role has read it
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tile_empty + kTileSlots);
+  uint64_t* wload = tile_empty + kTileSlots; // [kEpiWarps] each epilogue warp: its block of W landed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(wload + kEpiWarps);
   volatile uint32_t* abort_flag = tmem_slot + 1;
   volatile int* tile_ring = reinterpret_cast<volatile int*>(tmem_slot + 2);   // [kTileSlots]
 
@@ -544,6 +583,7 @@ ns_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
       mbar_init(smem_u32(&tile_full[k]), 1);
       mbar_init(smem_u32(&tile_empty[k]), kTileConsumers);
     }
+    for (int w = 0; w < kEpiWarps; ++w) mbar_init(smem_u32(&wload[w]), 1);
     *abort_flag = 0u;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -692,11 +732,16 @@ ns_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
     // ------------------------------------------------------ epilogue --
     const int quarter = warp & 3;             // TMEM lanes this warp may access
     const int half = (warp - 2) >> 2;         // which 128 of the 256 columns
-    // this warp's 8 KB of scratch (1024-byte aligned): the transpose slab of
-    // the last C X, or staging for the TMA stores of the other stages
+    // this warp's 8 KB of scratch (1024-byte aligned): staging for the TMA
+    // loads and stores of its blocks, or the transpose slab of the last C X
+    // when W cannot move through TMA
     uint8_t* out_stage = scratch + (warp - 2) * kWarpScratch;
     float* slab = reinterpret_cast<float*>(out_stage);
     uint32_t out_blocks = 0;
+    const bool w_tma = P.mode == kBxFinal && P.w_tma != 0;
+    const uint32_t wbar = smem_u32(&wload[warp - 2]);
+    uint32_t wphase = 0;
+    bool wait_failed = false;
     const uint32_t empty_even = peer_addr(smem_u32(&acc_empty[0]), 0);
     const uint32_t tempty_even = peer_addr(smem_u32(&tile_empty[0]), 0);
     for (uint32_t lt = 0;; ++lt) {   // lt: this pair's tile sequence number
@@ -725,6 +770,15 @@ ns_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * BN;
       for (int c0 = half * (BN / 2); c0 < (half + 1) * (BN / 2); c0 += 32) {
         float v[32];
+        // last C X through TMA: this block of W, in W's own layout (W rows are
+        // the iterate's rows, or its columns for a tall W)
+        const bool tall = w_tma && grp.mats[t.mat].transposed != 0;
+        const int wx = tall ? row0 : t.tn * BN + c0, wy = tall ? t.tn * BN + c0 : row0;
+        if (w_tma && lane == 0) {
+          if (out_blocks > 0) bulk_wait_read_0();   // the previous block's stores have read the staging area
+          mbar_expect_tx(wbar, kOutBlockBytes32);
+          tma_load_2d_local(smem_u32(out_stage), &wm.w[t.mat], wbar, wx, wy, l2_evict_first());
+        }
         __syncwarp();
         tmem_ld32(taddr + c0, v);
         if (P.mode == kBx) {
@@ -789,12 +843,79 @@ ns_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
             bulk_commit();
           }
           ++out_blocks;
+        } else if (w_tma) {
+          // W <- W (1 - lr wd) - lr scale X', updated in place in the staging
+          // area (128-byte swizzle: 16-byte chunk q of row r at q ^ (r & 7)),
+          // its bf16 copy staged 4 KB further (64-byte swizzle); both leave by
+          // TMA stores, which clip at the matrix edge
+          if (!mbar_wait(wbar, wphase, abort_flag, P.status, kStatusTimeoutWload)) {
+            wait_failed = true;
+            break;
+          }
+          wphase ^= 1u;
+          const MuonMat& M = grp.mats[t.mat];
+          const float decay = P.decay, scale = M.step_scale;
+          uint8_t* wbf = out_stage + kOutBlockBytes32;
+          if (tall) {
+            // lane t holds W column t of the block: element (j, t) for row j
+            const uint32_t q32 = static_cast<uint32_t>(lane) >> 2, w32 = (static_cast<uint32_t>(lane) & 3u) * 4u;
+            const uint32_t q16 = static_cast<uint32_t>(lane) >> 3, w16 = (static_cast<uint32_t>(lane) & 7u) * 2u;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              float* e = reinterpret_cast<float*>(out_stage + j * 128 + ((q32 ^ (static_cast<uint32_t>(j) & 7u)) * 16) + w32);
+              const float wv = *e * decay - scale * v[j];
+              *e = wv;
+              *reinterpret_cast<uint16_t*>(wbf + j * 64 + ((q16 ^ ((static_cast<uint32_t>(j) >> 1) & 3u)) * 16) + w16) =
+                  bf16_rne(wv);
+            }
+          } else {
+            // lane t holds W row t of the block
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              float4* e = reinterpret_cast<float4*>(out_stage + lane * 128 + ((static_cast<uint32_t>(q) ^ (static_cast<uint32_t>(lane) & 7u)) * 16));
+              float4 o = *e;
+              o.x = o.x * decay - scale * v[4 * q + 0];
+              o.y = o.y * decay - scale * v[4 * q + 1];
+              o.z = o.z * decay - scale * v[4 * q + 2];
+              o.w = o.w * decay - scale * v[4 * q + 3];
+              *e = o;
+              v[4 * q + 0] = o.x;
+              v[4 * q + 1] = o.y;
+              v[4 * q + 2] = o.z;
+              v[4 * q + 3] = o.w;
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const uint32_t phys = static_cast<uint32_t>(q) ^ ((static_cast<uint32_t>(lane) >> 1) & 3u);
+              *reinterpret_cast<uint4*>(wbf + lane * 64 + phys * 16) = make_uint4(
+                  static_cast<uint32_t>(bf16_rne(v[8 * q + 0])) | (static_cast<uint32_t>(bf16_rne(v[8 * q + 1])) << 16),
+                  static_cast<uint32_t>(bf16_rne(v[8 * q + 2])) | (static_cast<uint32_t>(bf16_rne(v[8 * q + 3])) << 16),
+                  static_cast<uint32_t>(bf16_rne(v[8 * q + 4])) | (static_cast<uint32_t>(bf16_rne(v[8 * q + 5])) << 16),
+                  static_cast<uint32_t>(bf16_rne(v[8 * q + 6])) | (static_cast<uint32_t>(bf16_rne(v[8 * q + 7])) << 16));
+            }
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            const uint64_t pol = l2_evict_first();
+            tma_store_2d(&wm.w[t.mat], smem_u32(out_stage), wx, wy, pol);
+            if (M.Wb) tma_store_2d(&wm.wb[t.mat], smem_u32(wbf), wx, wy, pol);
+            bulk_commit();
+          }
+          ++out_blocks;
         } else {
           epilogue_block(P, grp, t, slab, lane, row0, t.tn * BN + c0, v);
         }
       }
+      if (wait_failed) break;
       tc_fence_before();
       mbar_arrive_remote(empty_even + acc * static_cast<uint32_t>(sizeof(uint64_t)));
+    }
+    if (wait_failed) {
+      // a W block may still be on its way into the staging area: give it time to land
+      const unsigned long long t0 = global_ns();
+      while (global_ns() - t0 < 10000000ull) {
+      }
     }
     if (lane == 0 && out_blocks > 0) bulk_wait_all();   // stores complete before the CTA exits
   } else if (lane == 0 && rank == 0) {
@@ -928,8 +1049,38 @@ cudaError_t make_out_map32(CUtensorMap* map, const void* base, int64_t inner, in
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// 2-D map over one row-major matrix [rows][cols] of W (fp32, 128-byte swizzle)
+// or of its bf16 copy (64-byte swizzle), box 32 x 32.
+cudaError_t make_w_map(CUtensorMap* map, const void* base, int64_t cols, int64_t rows, bool bf16) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return cudaErrorNotSupported;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols * (bf16 ? 2 : 4))};
+  const cuuint32_t box[2] = {32, 32};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
+                        const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        bf16 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+// Maps of every matrix of the group for the last C X; false when a matrix
+// does not meet TMA's rules (16-byte aligned bases, row pitches a multiple of
+// 16 bytes), and the update then takes plain loads and stores.
+bool make_w_maps(const MuonGroup& grp, WMaps* wm) {
+  for (int m = 0; m < grp.count; ++m) {
+    const MuonMat& M = grp.mats[m];
+    if ((reinterpret_cast<uintptr_t>(M.W) & 15u) != 0 || M.C % 4 != 0) return false;
+    if (M.Wb && ((reinterpret_cast<uintptr_t>(M.Wb) & 15u) != 0 || M.C % 8 != 0)) return false;
+    if (make_w_map(&wm->w[m], M.W, M.C, M.R, false) != cudaSuccess) return false;
+    if (M.Wb && make_w_map(&wm->wb[m], M.Wb, M.C, M.R, true) != cudaSuccess) return false;
+  }
+  return true;
+}
+
 cudaError_t launch_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mo, const CUtensorMap& mo32,
-                        const GemmParams& P, const MuonGroup& grp,
+                        const GemmParams& P, const MuonGroup& grp, const WMaps& wm,
                         cudaStream_t stream) {
   static thread_local int configured_dev = -1;
   int dev = 0;
@@ -942,8 +1093,14 @@ cudaError_t launch_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const CUte
   }
   const int max_pairs = num_sms() / 2;
   const int pairs = P.total_tiles < max_pairs ? P.total_tiles : max_pairs;
-  ns_gemm_kernel<<<2 * pairs, kThreads, kSmemBytes, stream>>>(ma, mb, mo, mo32, P, grp);
+  ns_gemm_kernel<<<2 * pairs, kThreads, kSmemBytes, stream>>>(ma, mb, mo, mo32, P, grp, wm);
   return cudaGetLastError();
+}
+
+// The maps argument of the launches that do not use it.
+const WMaps& no_maps() {
+  static const WMaps none{};
+  return none;
 }
 
 }  // namespace
@@ -985,7 +1142,7 @@ cudaError_t launch_ns_iteration(const MuonGroup& grp, const NsBuffers& buf, cons
     P.Ah = buf.Ah;
     P.stall = (s.stall_first_stage && it == 0) ? 1 : 0;
     prof_begin(OPT_KERNEL_NS_GRAM, grp.count, grp.A, grp.B, stream);
-    e = launch_gemm(ma, mb, mo, mo32, P, grp, stream);
+    e = launch_gemm(ma, mb, mo, mo32, P, grp, no_maps(), stream);
     prof_end(stream);
     if (e != cudaSuccess) return e;
   }
@@ -1004,7 +1161,7 @@ cudaError_t launch_ns_iteration(const MuonGroup& grp, const NsBuffers& buf, cons
     P.Af = buf.Af;
     P.Ch = buf.Ch;
     prof_begin(OPT_KERNEL_NS_POLY, grp.count, grp.A, grp.B, stream);
-    e = launch_gemm(ma, mb, mo, mo, P, grp, stream);   // no fp32 output
+    e = launch_gemm(ma, mb, mo, mo, P, grp, no_maps(), stream);   // no fp32 output
     prof_end(stream);
     if (e != cudaSuccess) return e;
   }
@@ -1023,8 +1180,11 @@ cudaError_t launch_ns_iteration(const MuonGroup& grp, const NsBuffers& buf, cons
     P.tiles_per_mat = static_cast<int>((Ap / BM_PAIR) * (Bp / BN));
     P.total_tiles = P.tiles_per_mat * grp.count;
     P.Xh = X_next;
+    // the last iteration's update of W moves through TMA when every matrix allows it
+    static thread_local WMaps wm;
+    P.w_tma = (P.mode == kBxFinal && !s.ns_only && make_w_maps(grp, &wm)) ? 1 : 0;
     prof_begin(OPT_KERNEL_NS_BX, grp.count, grp.A, grp.B, stream);
-    e = launch_gemm(ma, mb, mo, mo, P, grp, stream);   // no fp32 output
+    e = launch_gemm(ma, mb, mo, mo, P, grp, P.w_tma ? wm : no_maps(), stream);   // no fp32 output
     prof_end(stream);
     if (e != cudaSuccess) return e;
   }

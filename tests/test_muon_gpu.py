@@ -148,6 +148,45 @@ def test_muon_step_options(kw):
     muon_case((200, 328), np.random.default_rng(11), **kw)
 
 
+@pytest.mark.parametrize("case", ["aligned_wide", "aligned_tall", "unaligned_wide", "unaligned_tall",
+                                  "bf16_pitch_8_bytes_off", "pitch_100_floats_no_model"])
+def test_muon_update_memory_layouts(case):
+    """The last Newton-Schulz GEMM updates W and its bf16 copy through TMA when
+    the bases are 16-byte aligned and the row pitches multiples of 16 bytes,
+    and through plain loads and stores otherwise (a view one element into its
+    buffer; 100 columns, whose bf16 rows are 200 bytes apart).  Both give the
+    oracle's update and a bf16 copy equal to the rounding of the new master."""
+    shape = {"aligned_wide": (96, 160), "aligned_tall": (160, 96), "unaligned_wide": (96, 160),
+             "unaligned_tall": (160, 96), "bf16_pitch_8_bytes_off": (64, 100),
+             "pitch_100_floats_no_model": (64, 100)}[case]
+    model = case != "pitch_100_floats_no_model"
+    rng = np.random.default_rng(23)
+    R, C = shape
+    W = (rng.standard_normal(shape) * 0.02).astype(np.float32)
+    m = (rng.standard_normal(shape) * 1e-2).astype(np.float32)
+    g = (rng.standard_normal(shape) * 1e-2).astype(np.float32)
+    if case.startswith("unaligned"):
+        Wd = torch.zeros(R * C + 1, dtype=torch.float32, device="cuda")[1:].view(R, C)
+        Wd.copy_(torch.from_numpy(W).cuda())
+        Wb = torch.zeros(R * C + 1, dtype=torch.bfloat16, device="cuda")[1:].view(R, C)
+    else:
+        Wd = dev(W)
+        Wb = torch.zeros(shape, dtype=torch.bfloat16, device="cuda") if model else None
+    md, gd = dev(m), dev(g)
+    lr, mu = 0.02, 0.95
+    hp = mp.muon_hp(lr=lr, momentum=mu)
+    p = mp.Param(Wd, gd, md, None, Wb)
+    ws = mp.alloc_workspace(mp.workspace_size([p], "muon"))
+    mp.muon_step(p, hp, ws)
+    assert mp.device_status(ws) == mp.OPT_OK
+    W1 = host(Wd)
+    Wn, mn, _ = OM.muon_step(W, g, m, lr=lr, momentum=mu, weight_decay=0.0, nesterov=True, ns_steps=5)
+    assert rel(W.astype(np.float64) - W1, W.astype(np.float64) - Wn) < NS_TOL
+    assert np.allclose(host(md), mn, rtol=1e-5, atol=1e-9)
+    if Wb is not None:
+        assert np.array_equal(bf16_host(Wb), OA.bf16_rne(W1))
+
+
 @pytest.mark.parametrize("scale", [1e-6, 1e-3, 1e3])
 def test_newton_schulz_scale_invariance(scale):
     """The normalisation makes the iteration independent of the gradient's
