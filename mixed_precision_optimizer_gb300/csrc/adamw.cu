@@ -17,11 +17,14 @@
 // launch and finds each chunk's tensor by binary search in the descriptor
 // table, which is passed in the kernel's parameter space (up to 400 tensors
 // per launch; longer lists take several launches).  Inside
-// a chunk each thread moves 8 consecutive elements per iteration: 2 x 16-byte
-// loads of p, g, m, v, 2 x 16-byte streaming stores of p, m, v and one
-// 16-byte streaming store of 8 bf16.  Elements before the first 16-byte-aligned group (views with an
-// offset) and after the last full group take the same arithmetic one at a
-// time.
+// a chunk each warp takes 256 consecutive elements at a time: lane l the
+// float4s l and 32 + l of every array, so that each of the warp's loads of
+// p, g, m, v and streaming stores of p, m, v covers 512 contiguous bytes (two
+// adjacent float4s a lane left every 32-byte sector half used by each
+// instruction), and each 8-byte store of the bf16 copy 256.  Groups of 8
+// after the last whole warp block take 8 consecutive elements a thread;
+// elements before the first 16-byte-aligned group (views with an offset) and
+// after the last full group take the same arithmetic one at a time.
 
 #include "internal.h"
 
@@ -68,9 +71,8 @@ __device__ __forceinline__ void st_v4(float* ptr, const float4& v) {
                : "memory");
 }
 
-__device__ __forceinline__ void st_u4(void* ptr, const uint4& v) {
-  asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(ptr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
-               : "memory");
+__device__ __forceinline__ void st_u2(void* ptr, uint32_t x, uint32_t y) {
+  asm volatile("st.global.cs.v2.u32 [%0], {%1,%2};" ::"l"(ptr), "r"(x), "r"(y) : "memory");
 }
 
 __device__ __forceinline__ int find_tensor(const AdamwTensorDesc* t, int n, int64_t chunk) {
@@ -113,7 +115,42 @@ adamw_mta_kernel(const __grid_constant__ AdamwBatch batch) {
     const int64_t end = min(begin + kAdamwChunk, d.numel);
     if (c == 0) scalar_range(d, 0, head, s, gs);
     const int64_t ngroups = (end > begin) ? (end - begin) / 8 : 0;
-    for (int64_t j = threadIdx.x; j < ngroups; j += blockDim.x) {
+    // A warp takes 256 consecutive elements (32 groups of 8): lane l the
+    // float4s l and 32 + l, so that every load and store instruction of the
+    // warp covers 512 contiguous bytes (256 for the bf16 copy).
+    const int lane = threadIdx.x & 31;
+    const int64_t nwarp_blocks = ngroups / 32;
+    for (int64_t wb = threadIdx.x >> 5; wb < nwarp_blocks; wb += blockDim.x >> 5) {
+      const int64_t e = begin + 256 * wb + 4 * lane, e1 = e + 128;
+      float4 p0 = ld_v4(d.p + e), p1 = ld_v4(d.p + e1);
+      float4 g0 = ld_stream(d.g + e), g1 = ld_stream(d.g + e1);
+      g0.x = __fmul_rn(g0.x, gs); g0.y = __fmul_rn(g0.y, gs); g0.z = __fmul_rn(g0.z, gs); g0.w = __fmul_rn(g0.w, gs);
+      g1.x = __fmul_rn(g1.x, gs); g1.y = __fmul_rn(g1.y, gs); g1.z = __fmul_rn(g1.z, gs); g1.w = __fmul_rn(g1.w, gs);
+      float4 m0 = ld_v4(d.m + e), m1 = ld_v4(d.m + e1);
+      float4 v0 = ld_v4(d.v + e), v1 = ld_v4(d.v + e1);
+      adamw_elem(p0.x, g0.x, m0.x, v0.x, s);
+      adamw_elem(p0.y, g0.y, m0.y, v0.y, s);
+      adamw_elem(p0.z, g0.z, m0.z, v0.z, s);
+      adamw_elem(p0.w, g0.w, m0.w, v0.w, s);
+      adamw_elem(p1.x, g1.x, m1.x, v1.x, s);
+      adamw_elem(p1.y, g1.y, m1.y, v1.y, s);
+      adamw_elem(p1.z, g1.z, m1.z, v1.z, s);
+      adamw_elem(p1.w, g1.w, m1.w, v1.w, s);
+      st_v4(d.p + e, p0);
+      st_v4(d.p + e1, p1);
+      st_v4(d.m + e, m0);
+      st_v4(d.m + e1, m1);
+      st_v4(d.v + e, v0);
+      st_v4(d.v + e1, v1);
+      if (d.model) {
+        st_u2(d.model + e, bf16_bits_rne(p0.x) | (bf16_bits_rne(p0.y) << 16),
+              bf16_bits_rne(p0.z) | (bf16_bits_rne(p0.w) << 16));
+        st_u2(d.model + e1, bf16_bits_rne(p1.x) | (bf16_bits_rne(p1.y) << 16),
+              bf16_bits_rne(p1.z) | (bf16_bits_rne(p1.w) << 16));
+      }
+    }
+    // groups after the last whole warp block: 8 consecutive elements a thread
+    for (int64_t j = 32 * nwarp_blocks + threadIdx.x; j < ngroups; j += blockDim.x) {
       const int64_t e = begin + 8 * j;
       float4 p0 = ld_v4(d.p + e), p1 = ld_v4(d.p + e + 4);
       float4 g0 = ld_stream(d.g + e), g1 = ld_stream(d.g + e + 4);
@@ -136,12 +173,10 @@ adamw_mta_kernel(const __grid_constant__ AdamwBatch batch) {
       st_v4(d.v + e, v0);
       st_v4(d.v + e + 4, v1);
       if (d.model) {
-        uint4 b;
-        b.x = bf16_bits_rne(p0.x) | (bf16_bits_rne(p0.y) << 16);
-        b.y = bf16_bits_rne(p0.z) | (bf16_bits_rne(p0.w) << 16);
-        b.z = bf16_bits_rne(p1.x) | (bf16_bits_rne(p1.y) << 16);
-        b.w = bf16_bits_rne(p1.z) | (bf16_bits_rne(p1.w) << 16);
-        st_u4(d.model + e, b);
+        st_u2(d.model + e, bf16_bits_rne(p0.x) | (bf16_bits_rne(p0.y) << 16),
+              bf16_bits_rne(p0.z) | (bf16_bits_rne(p0.w) << 16));
+        st_u2(d.model + e + 4, bf16_bits_rne(p1.x) | (bf16_bits_rne(p1.y) << 16),
+              bf16_bits_rne(p1.z) | (bf16_bits_rne(p1.w) << 16));
       }
     }
     // ragged tail of the tensor (only the last chunk has one)
