@@ -691,20 +691,33 @@ def run_e2e(args, step_fn, params, flat, t, total, dist: Dist):
     prepared_sets = [mp.prepare(x) for x in sets]
     compute = torch.cuda.current_stream()
     s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
-    # untimed: one pass of each copy direction over every host buffer
+    # untimed: one pass of each copy direction over every host buffer; the
+    # first pass is timed on its own to show the copy bandwidth of this host
+    # with no compute running (the two directions overlap each other)
+    E = lambda: torch.cuda.Event(enable_timing=True)
+    warm = [E() for _ in range(4)]
     s_in.wait_stream(compute)
     s_out.wait_stream(compute)
-    for gd, bd in flats:
+    for i, (gd, bd) in enumerate(flats):
         with torch.cuda.stream(s_in):
+            if i == 0:
+                warm[0].record(s_in)
             gd.copy_(g_host, non_blocking=True)
+            if i == 0:
+                warm[1].record(s_in)
         with torch.cuda.stream(s_out):
+            if i == 0:
+                warm[2].record(s_out)
             b_host.copy_(bd, non_blocking=True)
-    E = lambda: torch.cuda.Event(enable_timing=True)
+            if i == 0:
+                warm[3].record(s_out)
     h2d_begin, h2d_done = [E() for _ in range(K)], [E() for _ in range(K)]
     step_begin, step_done = [E() for _ in range(K)], [E() for _ in range(K)]
     d2h_begin, d2h_done = [E() for _ in range(K)], [E() for _ in range(K)]
     start = E()
     torch.cuda.synchronize()
+    idle_gbs = {"h2d": round(g_host.numel() * g_host.element_size() / (warm[0].elapsed_time(warm[1]) * 1e6), 1),
+                "d2h": round(b_host.numel() * b_host.element_size() / (warm[2].elapsed_time(warm[3]) * 1e6), 1)}
     clocks = ClockSampler(smi_index(torch.cuda.current_device()), "_e2e").__enter__()
     dist.barrier()
     torch.cuda.synchronize()
@@ -767,6 +780,7 @@ def run_e2e(args, step_fn, params, flat, t, total, dist: Dist):
             "device_ms_per_step": phase,
             "h2d_gbs": round(h2d / (phase["h2d"] * 1e6), 1) if phase["h2d"] > 0 else None,
             "d2h_gbs": round(d2h / (phase["d2h"] * 1e6), 1) if phase["d2h"] > 0 else None,
+            "copy_gbs_before_timing": idle_gbs,
             "clocks": clocks.summary()}
 
 
