@@ -347,7 +347,7 @@ def cublas_same_shapes(w, seconds=3.0):
 def kernel_traffic(kernel_key):
     """DRAM bytes per launch from the committed ncu summary of this kernel,
     if it was captured from the current source (else None)."""
-    path = os.path.join(ROOT, "profiles", "ncu_traffic.md")
+    path = os.path.join(ROOT, "profiles", "dram_traffic_llama16_mixed.md")
     try:
         text = open(path, encoding="utf-8").read()
     except OSError:

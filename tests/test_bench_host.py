@@ -108,7 +108,7 @@ def test_profile_rows_apply_only_to_their_source(tmp_path, monkeypatch):
     (csrc / "ns_gemm.cu").write_bytes(b"kernel v1")
     (csrc / "adamw.cu").write_bytes(b"adamw v1")
     sha = hashlib.sha256(b"kernel v1").hexdigest()[:16]
-    (tmp_path / "profiles" / "ncu_traffic.md").write_text(f"| ns_gemm | {sha} | 1.5e9 |\n| adamw | 0000000000000000 | 3e9 |\n")
+    (tmp_path / "profiles" / "dram_traffic_llama16_mixed.md").write_text(f"| ns_gemm | {sha} | 1.5e9 |\n| adamw | 0000000000000000 | 3e9 |\n")
     (tmp_path / "profiles" / "ns_gemm_llama_mlp_1layer.md").write_text(f"| tensor_pipe | {sha} | 70.5 | 60.0 | 85.25 |\n")
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     assert bench.kernel_traffic("ns_gemm") == 1.5e9
