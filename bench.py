@@ -30,6 +30,7 @@ import re
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -41,6 +42,7 @@ METRIC = "optimizer-step params/s; AdamW HBM GB/s; Muon Newton-Schulz TFLOPS"
 UNIT = "params/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 ADAMW_BYTES_PER_PARAM = 30     # read p, g, m, v (16 B); write p, m, v (12 B) and bf16 (2 B)
+NOMINAL_HBM_GBS = 8000.0       # GB300 HBM3e, nominal (the measured copy bandwidth is the roofline's peak)
 
 
 def parse():
@@ -58,6 +60,9 @@ def parse():
                          "Muon group, back to back for a few seconds each, for comparison only")
     ap.add_argument("--clip", type=float, default=0.0,
                     help="max_norm of global grad-norm clipping fused into the step (0: off)")
+    ap.add_argument("--no-sweep", action="store_true",
+                    help="skip the AdamW size sweep (10,000 tensors, GB/s per size decade) after the main workload")
+    ap.add_argument("--clock-log", default=None, help="directory for the nvidia-smi clock samples (default: temp)")
     return ap.parse_args()
 
 
@@ -83,14 +88,21 @@ class ClockSampler:
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap,"
              "clocks.mem,temperature.gpu")
 
+    log_dir = None   # --clock-log DIR keeps the samples there; otherwise a temporary file
+
     def __init__(self, index, tag=""):
         self.index = index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks{tag}_gpu{index}.csv")
+        self.tag = tag
 
     def __enter__(self):
         try:
-            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            if ClockSampler.log_dir:
+                os.makedirs(ClockSampler.log_dir, exist_ok=True)
+                self.path = os.path.join(ClockSampler.log_dir, f"clocks{self.tag}_gpu{self.index}.csv")
+            else:
+                fd, self.path = tempfile.mkstemp(prefix=f"mpopt_clocks{self.tag}_", suffix=".csv")
+                os.close(fd)
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
                                           "--format=csv,noheader,nounits", "-lms", "200"],
@@ -125,6 +137,11 @@ class ClockSampler:
                     rows.append((float(parts[1]), float(parts[2]), float(parts[3]), parts[5:9], *extra))
                 except ValueError:
                     continue
+        if not ClockSampler.log_dir:
+            try:
+                os.unlink(self.path)
+            except OSError:
+                pass
         if not rows:
             return None
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
@@ -259,11 +276,25 @@ def hyper(w: S.Workload):
 
 
 def gemm_flops(rec):
-    """Algorithmic flops of one Newton-Schulz GEMM launch: 2 A^2 B for X X^T
-    and for B X, 2 A^3 for A A (so one iteration is 2 (2 A^2 B + A^3), the
-    pages' 4 m^2 n + 2 m^3)."""
+    """Flops of one Newton-Schulz GEMM launch as the pages count them (dense
+    products): 2 A^2 B for X X^T and for C X, 2 A^3 for A A, so one iteration
+    is 2 (2 A^2 B + A^3), the pages' 4 m^2 n + 2 m^3."""
     A, B, c = rec["a"], rec["b"], rec["count"]
     return c * (2.0 * A * A * A if rec["kernel"] == "ns_poly" else 2.0 * A * A * B)
+
+
+def gemm_method_flops(rec):
+    """Flops of the method's own work in one launch: the symmetric products
+    X X^T and A A counted at their triangle (A^2 B and A^3), C X in full
+    (2 A^2 B), so one iteration is 3 A^2 B + A^3.  This is the roofline's
+    algorithmic count: a symmetric product needs only half its dense flops."""
+    A, B, c = rec["a"], rec["b"], rec["count"]
+    k = rec["kernel"]
+    if k == "ns_gram":
+        return c * 1.0 * A * A * B
+    if k == "ns_poly":
+        return c * 1.0 * A * A * A
+    return c * 2.0 * A * A * B
 
 
 def gemm_executed_flops(rec):
@@ -280,22 +311,31 @@ def gemm_executed_flops(rec):
     return c * 2.0 * Ap * Ap * Bp
 
 
-def kernels_by_shape(recs):
+def kernels_by_shape(recs, peak):
     """Per Newton-Schulz GEMM stage and Muon shape class (A x B, matrices per
-    launch): launches, ms per launch, and TFLOP/s algorithmic and executed."""
+    launch): launches, ms per launch, TFLOP/s by the method's count (the
+    roofline's), as executed by the tensor cores, and by the pages' dense
+    count; the executed rate as a fraction of `peak`."""
     out = {}
     for r in recs:
         if not r["kernel"].startswith("ns_"):
             continue
-        k = out.setdefault(f"{r['kernel']} {r['a']}x{r['b']} x{r['count']}", dict(launches=0, ms=0.0, flops=0.0, ex=0.0))
+        k = out.setdefault(f"{r['kernel']} {r['a']}x{r['b']} x{r['count']}",
+                           dict(launches=0, ms=0.0, flops=0.0, method=0.0, ex=0.0))
         k["launches"] += 1
         k["ms"] += r["ms"]
         k["flops"] += gemm_flops(r)
+        k["method"] += gemm_method_flops(r)
         k["ex"] += gemm_executed_flops(r)
-    return {name: {"launches": k["launches"], "ms_per_launch": round(k["ms"] / k["launches"], 4),
-                   "tflops_algorithmic": round(k["flops"] / (k["ms"] * 1e-3) / 1e12, 1),
-                   "tflops_executed": round(k["ex"] / (k["ms"] * 1e-3) / 1e12, 1)}
-            for name, k in sorted(out.items())}
+    res = {}
+    for name, k in sorted(out.items()):
+        sec = k["ms"] * 1e-3
+        res[name] = {"launches": k["launches"], "ms_per_launch": round(k["ms"] / k["launches"], 4),
+                     "tflops_method": round(k["method"] / sec / 1e12, 1),
+                     "tflops_executed": round(k["ex"] / sec / 1e12, 1),
+                     "tflops_pages_count": round(k["flops"] / sec / 1e12, 1),
+                     "executed_frac": round(k["ex"] / sec / 1e12 / peak, 3)}
+    return res
 
 
 def cublas_same_shapes(w, seconds=3.0):
@@ -344,53 +384,60 @@ def cublas_same_shapes(w, seconds=3.0):
     return res
 
 
-def kernel_traffic(kernel_key):
-    """DRAM bytes per launch from the committed ncu summary of this kernel,
-    if it was captured from the current source (else None)."""
-    path = os.path.join(ROOT, "profiles", "dram_traffic_llama16_mixed.md")
-    try:
-        text = open(path, encoding="utf-8").read()
-    except OSError:
-        return None
-    src = open(os.path.join(ROOT, "mixed_precision_optimizer_gb300", "csrc", "ns_gemm.cu" if kernel_key.startswith("ns")
-                            else "adamw.cu"), "rb").read()
-    sha = hashlib.sha256(src).hexdigest()[:16]
-    m = re.search(rf"^\| *{re.escape(kernel_key)} *\| *{sha} *\| *([0-9.eE+]+) *\|", text, re.M)
-    return float(m.group(1)) if m else None
+def source_sha(name):
+    """sha256 prefix of a kernel source file: a profile row applies only while
+    the source it was captured from is unchanged."""
+    path = os.path.join(ROOT, "mixed_precision_optimizer_gb300", "csrc", name)
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
 
 
-def tensor_pipe_active():
-    """ncu tensor-pipe utilisation (% of peak) of the three GEMM stages from the
-    committed full-set summary, if it was captured from the current ns_gemm.cu
-    source (else None): the algorithmic TFLOP/s count the symmetric stages' full
-    flops, and this shows what the tensor pipe actually did."""
-    path = os.path.join(ROOT, "profiles", "ns_gemm_llama_mlp_1layer.md")
+def profile_row(key):
+    """The row `key` of profiles/rows.json (figures taken from committed ncu
+    captures) if the kernel source it names still has the sha256 prefix it was
+    captured from; else None."""
     try:
-        text = open(path, encoding="utf-8").read()
-    except OSError:
+        with open(os.path.join(ROOT, "profiles", "rows.json"), encoding="utf-8") as f:
+            rows = json.load(f)
+    except (OSError, ValueError):
         return None
-    src = open(os.path.join(ROOT, "mixed_precision_optimizer_gb300", "csrc", "ns_gemm.cu"), "rb").read()
-    sha = hashlib.sha256(src).hexdigest()[:16]
-    m = re.search(rf"^\| *tensor_pipe *\| *{sha} *\| *([0-9.]+) *\| *([0-9.]+) *\| *([0-9.]+) *\|", text, re.M)
-    if not m:
+    row = rows.get(key)
+    if not isinstance(row, dict):
         return None
-    return {"gram": float(m.group(1)), "poly": float(m.group(2)), "bx": float(m.group(3)),
-            "source": "profiles/ns_gemm_llama_mlp_1layer.md (ncu --set full, one-layer MLP case)"}
+    try:
+        if source_sha(row["source"]) != row["sha256_16"]:
+            return None
+    except (OSError, KeyError):
+        return None
+    return row
 
 
 # ------------------------------------------------------------ CPU oracle --
 
-def cpu_oracle_sample(w: S.Workload, budget_s=20.0):
-    """Time the oracle (as it stands) on a bounded sample of the workload and
-    extrapolate to the whole step: AdamW per element from an fp32 oracle run
-    over a slice, Muon per matrix from fp64 oracle steps on one matrix of the
-    smaller shapes, the larger shapes scaled by Newton-Schulz flop count."""
+MUON_SAMPLE_FLOPS = 1.5e11   # a shape class is run through the oracle when one matrix's NS is at most this
+
+
+def cpu_oracle_sample(w: S.Workload):
+    """Time the oracle (as it stands) on a fixed sample of one step of the
+    workload and extrapolate to the whole step.  The same sample serves the
+    cpu_baseline of our arm and every step of --impl reference, so the two
+    report one measurement:
+
+      AdamW  the fp32 oracle over min(AdamW elements, 2^24) elements, scaled
+             per element to every AdamW parameter;
+      Muon   one fp64 oracle step on one matrix of every shape class whose
+             Newton-Schulz is at most MUON_SAMPLE_FLOPS (at least the
+             smallest class), scaled by the count of its class; larger classes
+             extrapolated by Newton-Schulz flop count at the best fp64 rate
+             the sampled classes reached.
+
+    Returns (seconds per step, description dict)."""
     import numpy as np
     from oracle import adamw as OA
     from oracle import muon as OM
     rng = np.random.default_rng(0)
     t_total = 0.0
-    notes = []
+    sampled, extrapolated = [], []
     adamw_n = sum(s.numel for s in w.tensors if not is_muon(w, s))
     if adamw_n:
         n = min(adamw_n, 1 << 24)
@@ -402,32 +449,56 @@ def cpu_oracle_sample(w: S.Workload, budget_s=20.0):
         OA.adamw_step_fp32(p, g, m, v, lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.1, t=1)
         dt = time.perf_counter() - t0
         t_total += dt / n * adamw_n
-        notes.append(f"AdamW fp32 oracle on {n} elements")
+        sampled.append(f"AdamW fp32 oracle on {n} elements")
+        if n < adamw_n:
+            extrapolated.append(f"AdamW scaled per element to {adamw_n}")
     shapes = {}
-    for s in w.tensors:
-        if is_muon(w, s):
-            key = tuple(sorted(s.shape))
+    for sp in w.tensors:
+        if is_muon(w, sp):
+            key = tuple(sorted(sp.shape))
             shapes[key] = shapes.get(key, 0) + 1
     if shapes:
         measured = {}
         for key in sorted(shapes, key=lambda k: OM.ns_flops(*k)):
-            if measured and OM.ns_flops(*key) * (measured[min(measured)][0] / measured[min(measured)][1]) > budget_s:
+            if measured and OM.ns_flops(*key) > MUON_SAMPLE_FLOPS:
                 break
             A, B = key
-            W = (rng.standard_normal((A, B)) * 0.02)
-            g = rng.standard_normal((A, B)) * 1e-3
+            W = rng.standard_normal((A, B)) * 0.02
+            gg = rng.standard_normal((A, B)) * 1e-3
             t0 = time.perf_counter()
-            OM.muon_step(W, g, np.zeros_like(W), lr=0.02, momentum=0.95)
+            OM.muon_step(W, gg, np.zeros_like(W), lr=0.02, momentum=0.95)
             measured[key] = (time.perf_counter() - t0, OM.ns_flops(*key))
+            sampled.append(f"Muon fp64 oracle step on one {A}x{B} matrix")
         rate = max(f / t for t, f in measured.values())     # fp64 flop/s of the best-measured shape
         for key, cnt in shapes.items():
-            t = measured[key][0] if key in measured else OM.ns_flops(*key) / rate
-            t_total += cnt * t
-        notes.append("Muon fp64 oracle on one " + ", one ".join(f"{a}x{b}" for a, b in measured)
-                     + (" matrix; larger shapes extrapolated by Newton-Schulz flop count"
-                        if len(measured) < len(shapes) else " matrix"))
-    notes.append(f"numpy elementwise on 1 thread, BLAS matmul on up to {cpu_threads()} threads")
-    return t_total, "; ".join(notes)
+            if key in measured:
+                t_total += cnt * measured[key][0]
+                if cnt > 1:
+                    extrapolated.append(f"{key[0]}x{key[1]} x{cnt} from one matrix")
+            else:
+                t_total += cnt * OM.ns_flops(*key) / rate
+                extrapolated.append(f"{key[0]}x{key[1]} x{cnt} by Newton-Schulz flops at {rate / 1e9:.1f} GFLOP/s")
+    desc = {"sampled": sampled, "extrapolated": bool(extrapolated), "extrapolation": extrapolated,
+            "threads": f"Newton-Schulz matmuls: BLAS on up to {cpu_threads()} threads; AdamW and the Muon "
+                       "elementwise steps: numpy on 1 thread"}
+    return t_total, desc
+
+
+def cpu_baseline_entry(w, t_step, desc, total):
+    return {"value": round(total / t_step, 1), "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
+            "sample": "; ".join(desc["sampled"]) + " (one step of the workload, extrapolated to all of it)",
+            "extrapolated": desc["extrapolated"], "extrapolation": desc["extrapolation"],
+            "cores_detail": desc["threads"], "seconds_per_step": round(t_step, 3)}
+
+
+def workload_config(w: S.Workload, clip: float):
+    """The workload as both arms name it (identical dicts)."""
+    n_muon = sum(s.numel for s in w.tensors if is_muon(w, s))
+    total = w.numel
+    return {"workload": w.name, "params": total, "muon_params": n_muon, "adamw_params": total - n_muon,
+            "tensors": len(w.tensors), "grad_clip_max_norm": clip if clip > 0 else None,
+            "l2": "inputs larger than L2 (all state resident, ~18 B/param touched per step)"
+            if total * 14 > 4 * 129e6 else "L2 not flushed: workload smaller than L2"}
 
 
 def cpu_threads():
@@ -492,24 +563,56 @@ def run_ours(args, dist: Dist):
     launches = prof.count
 
     # ---- per-kernel breakdown from the events around each launch
+    peaks, peak_src = load_peaks()
+    line = measured_line(args, w, recs, launches, elapsed_ms, total, dist, peaks, peak_src)
+
+    # ---- end to end through the public API with host buffers
+    line["e2e"] = run_e2e(args, step, params, flat, t, total, dist)
+    t += args.e2e_steps
+    line["clocks"] = clocks.summary()
+    if args.compare_cublas and dist.rank == 0:
+        with ClockSampler(smi_index(device.index), "_cublas") as cclocks:
+            line["cublas_same_shapes"] = cublas_same_shapes(w)
+        if line["cublas_same_shapes"] is not None:
+            line["cublas_same_shapes"]["clocks"] = cclocks.summary()
+
+    # ---- AdamW GB/s by size decade: the 10,000-tensor sweep, on the device
+    # once this workload's buffers are released
+    del step, params, flat, prepared, ws
+    import gc
+    gc.collect()
+    torch.cuda.empty_cache()
+    if w.name == "adamw_sweep_10k" or not args.no_sweep:
+        line["adamw_gbs_by_size"] = run_sweep(device, peaks)
+    if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
+        t_cpu, desc = cpu_oracle_sample(w)
+        line["cpu_baseline"] = cpu_baseline_entry(w, t_cpu, desc, total)
+    return line
+
+
+def measured_line(args, w, recs, launches, elapsed_ms, total, dist, peaks, peak_src):
+    """The JSON line's measured part: value, per-kernel times, the roofline of
+    the dominant kernel and AdamW's bandwidth."""
     kernels = {}
     for r in recs:
-        k = kernels.setdefault(r["kernel"], dict(launches=0, ms=0.0, flops=0.0, executed=0.0, elems=0))
+        k = kernels.setdefault(r["kernel"], dict(launches=0, ms=0.0, flops=0.0, method=0.0, executed=0.0, elems=0))
         k["launches"] += 1
         k["ms"] += r["ms"]
         if r["kernel"].startswith("ns_"):
             k["flops"] += gemm_flops(r)
+            k["method"] += gemm_method_flops(r)
             k["executed"] += gemm_executed_flops(r)
         if r["kernel"] == "adamw":
             k["elems"] += r["a"]
     busy = sum(k["ms"] for k in kernels.values()) or 1.0
-    peaks, peak_src = load_peaks()
     kern_out = {}
     for name, k in kernels.items():
         e = dict(launches=k["launches"], ms_total=round(k["ms"], 3), share=round(k["ms"] / busy, 4))
         if k["flops"]:
-            e["tflops_algorithmic"] = round(k["flops"] / (k["ms"] * 1e-3) / 1e12, 1)
-            e["tflops_executed"] = round(k["executed"] / (k["ms"] * 1e-3) / 1e12, 1)
+            sec = k["ms"] * 1e-3
+            e["tflops_method"] = round(k["method"] / sec / 1e12, 1)
+            e["tflops_executed"] = round(k["executed"] / sec / 1e12, 1)
+            e["tflops_pages_count"] = round(k["flops"] / sec / 1e12, 1)
         if k["elems"]:
             e["gbs"] = round(k["elems"] * ADAMW_BYTES_PER_PARAM / (k["ms"] * 1e-3) / 1e9, 1)
         kern_out[name] = e
@@ -517,83 +620,131 @@ def run_ours(args, dist: Dist):
     ns = ("ns_gram", "ns_poly", "ns_bx")
     gemm_ms = sum(kernels.get(n, {}).get("ms", 0.0) for n in ns)
     adamw_ms = kernels.get("adamw", {}).get("ms", 0.0)
+    sustained = peaks["bf16_tflops_sustained"]
     if gemm_ms >= adamw_ms and gemm_ms > 0:
+        sec = gemm_ms * 1e-3
         fl = sum(kernels.get(n, {}).get("flops", 0.0) for n in ns)
+        me = sum(kernels.get(n, {}).get("method", 0.0) for n in ns)
         ex = sum(kernels.get(n, {}).get("executed", 0.0) for n in ns)
         nl = sum(kernels.get(n, {}).get("launches", 0) for n in ns)
-        achieved = fl / nl / ((gemm_ms / nl) * 1e-3) / 1e12
+        achieved = me / sec / 1e12
         # fp16 and bf16 share the dense tensor rate (nominal ratio 1), so the
         # measured bf16 figure is the fp16 peak
-        peak = peaks["bf16_tflops_sustained"]
-        tr = kernel_traffic("ns_gemm")   # mean DRAM bytes per GEMM launch of one step
+        row = profile_row("ns_gemm_traffic") or {}
+        pipe = profile_row("ns_gemm_tensor_pipe")
         roofline = {"bound": "tensor", "kernel": "ns_gemm_kernel (fp16 x fp16 -> fp32: X X^T, A A, C X)",
-                    "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
-                    "frac": round(achieved / peak, 4), "traffic": tr,
-                    "peak_source": f"{peak_src} bf16_tflops_sustained x nominal fp16/bf16 ratio 1",
-                    "executed_tflops": round(ex / (gemm_ms * 1e-3) / 1e12, 1),
-                    "tensor_pipe_active_pct": tensor_pipe_active(),
-                    "per_launch_flops": round(fl / nl), "avg_launch_ms": round(gemm_ms / nl, 4)}
+                    "achieved": round(achieved, 1), "peak": sustained, "unit": "TFLOP/s",
+                    "frac": round(achieved / sustained, 4), "traffic": row.get("bytes_per_launch"),
+                    "count": "method: X X^T and A A at their triangle (A^2 B, A^3), C X in full (2 A^2 B); "
+                             "3 A^2 B + A^3 per iteration and matrix",
+                    "peak_source": f"{peak_src} bf16_tflops_sustained (of measured) x nominal fp16/bf16 ratio 1",
+                    "per_launch_flops": round(me / nl), "avg_launch_ms": round(gemm_ms / nl, 4),
+                    "executed_tflops": round(ex / sec / 1e12, 1),
+                    "executed_frac": round(ex / sec / 1e12 / sustained, 4),
+                    "executed_count": "padded to 256, every 256 x 256 block on or below the diagonal in full",
+                    "pages_count_tflops": round(fl / sec / 1e12, 1),
+                    "pages_count_frac": round(fl / sec / 1e12 / sustained, 4),
+                    "pages_count": "2 (2 A^2 B + A^3) per iteration (dense products, the pages' 4 m^2 n + 2 m^3)",
+                    "burst_frac": round(achieved / peaks["bf16_tflops"], 4),
+                    "traffic_source": row.get("how"),
+                    "tensor_pipe_active_pct": pipe.get("pct") if pipe else None}
     else:
         k = kernels["adamw"]
         achieved = k["elems"] * ADAMW_BYTES_PER_PARAM / (k["ms"] * 1e-3) / 1e9
         peak = peaks["hbm_gbs"]
+        row = profile_row("adamw_traffic") or {}
         roofline = {"bound": "hbm", "kernel": "adamw_mta_kernel", "achieved": round(achieved, 1), "peak": peak,
-                    "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": kernel_traffic("adamw"),
-                    "peak_source": f"{peak_src} hbm_gbs",
+                    "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": row.get("bytes_per_launch"),
+                    "peak_source": f"{peak_src} hbm_gbs (of measured)",
+                    "frac_of_nominal_8tbs": round(achieved / NOMINAL_HBM_GBS, 4),
                     "per_launch_bytes": round(k["elems"] * ADAMW_BYTES_PER_PARAM / k["launches"]),
                     "avg_launch_ms": round(k["ms"] / k["launches"], 4)}
+    roofline_adamw = None
     if "adamw" in kernels:
         k = kernels["adamw"]
-        roofline_adamw = {"bound": "hbm", "kernel": "adamw_mta_kernel", "achieved": kern_out["adamw"]["gbs"],
-                          "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                          "frac": round(kern_out["adamw"]["gbs"] / peaks["hbm_gbs"], 4),
-                          "traffic": kernel_traffic("adamw"), "peak_source": f"{peak_src} hbm_gbs",
+        gbs = kern_out["adamw"]["gbs"]
+        row = profile_row("adamw_traffic") or {}
+        roofline_adamw = {"bound": "hbm", "kernel": "adamw_mta_kernel", "achieved": gbs,
+                          "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4),
+                          "frac_of_nominal_8tbs": round(gbs / NOMINAL_HBM_GBS, 4),
+                          "traffic": row.get("bytes_per_launch"), "peak_source": f"{peak_src} hbm_gbs (of measured)",
                           "per_launch_bytes": round(k["elems"] * ADAMW_BYTES_PER_PARAM / k["launches"])}
-    else:
-        roofline_adamw = None
-
-    # ---- AdamW GB/s per size decade (the sweep workload reports it per bucket)
-    buckets = adamw_buckets(params, ha(t)) if w.name == "adamw_sweep_10k" else None
-    t += 1 if buckets else 0
-
-    # ---- end to end through the public API with host buffers
-    e2e = run_e2e(args, step, params, flat, t, total, dist)
-    t += args.e2e_steps
-
     value = total * args.steps * dist.world / (elapsed_ms * 1e-3)
-    csum = clocks.summary()
-    line = {
+    cfg = workload_config(w, args.clip)
+    return {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": dist.world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(elapsed_ms / args.steps, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "dtype_detail": "fp32 master weights, gradients, state and AdamW arithmetic; Newton-Schulz GEMMs take fp16 "
                         "operands with fp32 accumulation on the tensor cores; bf16 model writeback",
         "data": "synthetic (seeded, drawn on the GPU)",
-        "config": {"workload": w.name, "params": total, "grad_clip_max_norm": args.clip if args.clip > 0 else None, "muon_params": n_muon, "adamw_params": n_adamw,
-                   "tensors": len(w.tensors), "parallelism": f"replicas x{dist.world}" if dist.world > 1 else "1 GPU",
-                   "l2": "inputs larger than L2 (all state resident, ~18 B/param touched per step)"
-                   if total * 14 > 4 * 129e6 else "L2 not flushed: workload smaller than L2",
-                   "adamw_gbs": kern_out.get("adamw", {}).get("gbs"),
-                   "ns_tflops_algorithmic": roofline.get("achieved") if roofline["bound"] == "tensor" else None},
+        "config": cfg,
+        "parallelism": f"replicas x{dist.world}" if dist.world > 1 else "1 GPU",
+        "adamw_gbs": kern_out.get("adamw", {}).get("gbs"),
+        "ns_tflops_method": roofline.get("achieved") if roofline["bound"] == "tensor" else None,
         "roofline": roofline,
         "roofline_adamw": roofline_adamw,
         "kernels": kern_out,
-        "kernels_by_shape": kernels_by_shape(recs),
-        "adamw_gbs_by_size": buckets,
+        "kernels_by_shape": kernels_by_shape(recs, sustained),
         "gpu_launches": launches,
-        "e2e": e2e,
-        "clocks": csum,
     }
-    if args.compare_cublas and dist.rank == 0:
-        with ClockSampler(smi_index(device.index), "_cublas") as cclocks:
-            line["cublas_same_shapes"] = cublas_same_shapes(w)
-        if line["cublas_same_shapes"] is not None:
-            line["cublas_same_shapes"]["clocks"] = cclocks.summary()
-    if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
-        t_cpu, sample = cpu_oracle_sample(w)
-        line["cpu_baseline"] = {"value": round(total / t_cpu, 1), "unit": UNIT, "cores": cpu_threads(),
-                                "kind": "oracle", "sample": sample}
-    return line
+
+
+def run_sweep(device, peaks):
+    """AdamW GB/s by size decade on the 10,000-tensor sweep (sizes log-uniform
+    in [1, 2^24), ~1.0e10 parameters, 18 B/param resident).  All tensors at
+    once when the device has room; otherwise five seeded groups of 2,000
+    tensors, one after another, their per-decade times added.  Every array is
+    a view of one flat buffer per kind (p, g, m, v, bf16 copy)."""
+    import torch
+    import mixed_precision_optimizer_gb300 as mp
+    w = S.adamw_sweep_10k()
+    specs = list(w.tensors)
+    need = w.numel * 18 * 1.03 + 4e9
+    free, _ = torch.cuda.mem_get_info()
+    if free >= need:
+        groups, mode = [list(range(len(specs)))], "all 10,000 tensors resident"
+    else:
+        import numpy as np
+        perm = np.random.default_rng([S.INIT_SEED, 5]).permutation(len(specs))
+        groups, mode = [sorted(perm[k::5].tolist()) for k in range(5)], "5 seeded groups of 2,000 tensors"
+    hp = mp.adamw_hp(lr=w.adamw.lr, beta1=w.adamw.beta1, beta2=w.adamw.beta2, eps=w.adamw.eps,
+                     weight_decay=w.adamw.weight_decay, step=1)
+    acc = {}
+    for ids in groups:
+        numels = [specs[i].numel for i in ids]
+        offs, n_flat = flat_layout(numels)
+        flats = [torch.empty(n_flat, dtype=torch.float32, device=device) for _ in range(4)]
+        model = torch.empty(n_flat, dtype=torch.bfloat16, device=device)
+        shp = [specs[i].shape for i in ids]
+        P, G, M, V = (flat_views(f, offs, shp) for f in flats)
+        Bv = flat_views(model, offs, shp)
+        M_flat, V_flat = flats[2], flats[3]
+        M_flat.zero_()
+        V_flat.zero_()
+        params = []
+        for k, i in enumerate(ids):
+            S.torch_init_(P[k], specs[i], i)
+            S.torch_grad_(G[k], specs[i], i, 1)
+            params.append(mp.Param(P[k], G[k], M[k], V[k], Bv[k], kind="adamw"))
+        for key, rec in adamw_buckets(params, hp).items():
+            a = acc.setdefault(key, dict(tensors=0, params=0, launches=0, ms=0.0))
+            for f in ("tensors", "params", "launches"):
+                a[f] += rec[f]
+            a["ms"] += rec["kernel_ms"]
+        del params, P, G, M, V, Bv, flats, model, M_flat, V_flat
+        torch.cuda.empty_cache()
+    out = {"mode": mode, "bytes_per_param": ADAMW_BYTES_PER_PARAM, "peak_gbs": peaks["hbm_gbs"], "buckets": {}}
+    for key, a in sorted(acc.items(), key=lambda kv: float(kv[0].split("-")[0])):
+        gbs = a["params"] * ADAMW_BYTES_PER_PARAM / (a["ms"] * 1e-3) / 1e9
+        out["buckets"][key] = {"tensors": a["tensors"], "params": a["params"], "launches": a["launches"],
+                               "kernel_ms": round(a["ms"], 4), "gbs": round(gbs, 1),
+                               "frac": round(gbs / peaks["hbm_gbs"], 4)}
+    tp = sum(a["params"] for a in acc.values())
+    tm = sum(a["ms"] for a in acc.values())
+    out["all"] = {"params": tp, "kernel_ms": round(tm, 3),
+                  "gbs": round(tp * ADAMW_BYTES_PER_PARAM / (tm * 1e-3) / 1e9, 1)}
+    return out
 
 
 class PinnedHostArena:
@@ -787,24 +938,27 @@ def run_e2e(args, step_fn, params, flat, t, total, dist: Dist):
 # --------------------------------------------------------- reference arm --
 
 def run_reference(args, dist: Dist):
+    """The oracle, as it stands, on this host's cores: every step is one run of
+    the fixed sample of cpu_oracle_sample (the same sample as our arm's
+    cpu_baseline), extrapolated to the whole workload."""
     w = S.WORKLOADS[args.workload]()
     total = w.numel
     for _ in range(args.warmup):
-        cpu_oracle_sample(w, budget_s=2.0)
-    times, sample = [], ""
+        cpu_oracle_sample(w)
+    times, desc = [], None
     for _ in range(args.steps):
-        t, sample = cpu_oracle_sample(w, budget_s=2.0)
+        t, desc = cpu_oracle_sample(w)
         times.append(t)
     t_step = statistics.mean(times)
     value = total / t_step
+    base = cpu_baseline_entry(w, t_step, desc, total)
     return {"metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": dist.world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(t_step * 1e3, 1), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "dtype_detail": "CPU oracle: fp32 AdamW in literal operation order, fp64 Muon and Newton-Schulz",
             "data": "synthetic (seeded)", "impl": "reference",
-            "config": {"workload": w.name, "params": total, "grad_clip_max_norm": args.clip if args.clip > 0 else None, "parallelism": "CPU oracle on rank 0"},
-            "cpu_baseline": {"value": round(value, 1), "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
-                             "sample": sample + " (per step; step time extrapolated from the sample)"},
+            "config": workload_config(w, args.clip), "parallelism": "CPU oracle on rank 0",
+            "cpu_baseline": base,
             "e2e": {"value": round(value, 1), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
@@ -812,6 +966,7 @@ def main():
     args = parse()
     if args.steps < 1 or args.warmup < 0:
         raise SystemExit("--steps >= 1, --warmup >= 0")
+    ClockSampler.log_dir = args.clock_log
     dist = Dist()
     try:
         if args.impl == "reference":

@@ -255,6 +255,51 @@ MPOPT_API opt_status opt_mixed_step_clipped(const opt_muon_hp* hp_muon, const op
 MPOPT_API opt_status opt_reload_model_params(const opt_tensor* tensors, int32_t n, void* stream);
 
 /*
+ * Data-parallel sharding of one optimizer step over `world_size` ranks
+ * ("02 · Optimizer：算法与 infra" §12.1-§12.2 and §14.3; "优化器：AdamW、Muon 与
+ * 分布式优化器", distributed Muon, scheme ③).  Host-only: no device work, no
+ * CUDA call; every rank computes the same plan from the same tensor list.
+ *
+ *   - AdamW tensors (the routing of opt_mixed_step, with `routing` as in
+ *     opt_workspace_size) are laid end to end, in list order, in one index
+ *     space of N elements, which is cut into world_size contiguous ranges,
+ *     ZeRO-1 style: rank r owns [rank_bounds[r], rank_bounds[r+1]).  The cuts
+ *     ignore tensor boundaries (a tensor may span ranks); every inner cut is a
+ *     multiple of `align_elems` (>= 1) and the ranges are as equal as that
+ *     allows: rank_bounds[r] = min(N, round_up(r * N / world_size, align_elems)).
+ *     Rank r steps only the elements it owns, with fp32 master, m and v of
+ *     that size, and then every rank receives the bf16 values of the rest.
+ *   - Muon tensors stay whole (Newton-Schulz needs the whole matrix): each has
+ *     one owner rank, assigned by LPT bin-packing on its Newton-Schulz work
+ *     2 (2 A^2 B + A^3) per iteration (largest first; each goes to the rank
+ *     with the least work so far, the lowest rank on ties; equal sizes keep
+ *     list order), so the plan is deterministic.
+ *
+ * Output, caller-owned host memory:
+ *   entries[n]            per tensor: owner = the owning rank (Muon) or -1
+ *                         (AdamW; and for empty tensors); flat_begin = the
+ *                         tensor's first index in the AdamW index space
+ *                         (AdamW) or -1 (Muon)
+ *   rank_bounds[world_size + 1]   the AdamW ranges (rank_bounds[0] = 0,
+ *                         rank_bounds[world_size] = N)
+ *   rank_muon_work[world_size]    optional (NULL: not written): the
+ *                         Newton-Schulz flops per iteration each rank owns
+ * Only shapes, kinds and flags are read: the tensors' pointers may be null
+ * (on a sharded rank the master and state of what it does not own need not
+ * exist).  Errors: OPT_ERR_INVALID_ARG for world_size < 1, align_elems < 1,
+ * null outputs, or a shape or kind opt_mixed_step would reject.
+ */
+typedef struct {
+  int32_t owner;
+  int32_t reserved;
+  int64_t flat_begin;
+} opt_shard_entry;
+
+MPOPT_API opt_status opt_shard_plan(const opt_tensor* tensors, int32_t n, int32_t routing, int32_t world_size,
+                                    int64_t align_elems, opt_shard_entry* entries, int64_t* rank_bounds,
+                                    double* rank_muon_work);
+
+/*
  * Newton-Schulz orthogonalisation alone ("02 · Optimizer：算法与 infra" §5.2):
  * O = NS_steps(G) for one fp32 rows x cols matrix G, same fp16 tensor-core
  * path as opt_muon_step.  G and O are device fp32 [rows*cols]; O may alias G.
@@ -277,18 +322,29 @@ MPOPT_API opt_status opt_newton_schulz(const float* G, float* O, int64_t rows, i
  *   - Size limit: min(rows, cols) <= 1024 and max(rows, cols) <= 4096; larger
  *     matrices return OPT_ERR_UNSUPPORTED (text in opt_last_cuda_error()).
  *   - The first call on each device looks up the array's device address there
- *     (cudaGetSymbolAddress with that device current); make that first call
- *     before any stream capture.
+ *     (cudaGetSymbolAddress with that device current), and so does the first
+ *     call after the device's CUDA context was destroyed and created again
+ *     (cudaDeviceReset): the library remembers the context's id with the
+ *     address.  Make such a first call before any stream capture.
  *   - Every call on a device shares the one array, and the array keeps the last
  *     call's contents (the status word is cleared at the start of each call).
  *     Calls whose work overlaps on the GPU -- on different streams, or from
  *     different threads -- race on it: serialise them on one stream.
- *   - A device-side timeout is recorded in the array's header, which callers
- *     cannot read; use opt_newton_schulz when that status is needed.
+ *   - A device-side timeout is recorded in the array's header: read it with
+ *     opt_noalloc_device_status() after the call.
  */
 MPOPT_API opt_status opt_newton_schulz_noalloc(const float* G, float* O, int64_t rows, int64_t cols,
                                                int32_t ns_steps, float a, float b, float c, float eps,
                                                void* stream);
+
+/*
+ * Status of the last opt_newton_schulz_noalloc call on the current device:
+ * synchronises `stream` and returns OPT_ERR_DEVICE_TIMEOUT if a kernel of
+ * that call recorded a device-side timeout in the built-in array's header,
+ * else OPT_OK (OPT_ERR_CUDA if the copy or the synchronisation fails).  Like
+ * the call itself, no counterpart on the pages.
+ */
+MPOPT_API opt_status opt_noalloc_device_status(void* stream);
 
 /*
  * Synchronises `stream` and reports whether a kernel of the last step on this

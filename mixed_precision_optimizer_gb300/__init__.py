@@ -14,6 +14,8 @@ Entry points (same names as the C ABI, without the ``opt_`` prefix):
 * ``newton_schulz``   -- Newton-Schulz orthogonalisation alone
 * ``workspace_size``  -- device scratch bytes a call needs
 * ``device_status``   -- reads the device-side status word of a workspace
+* ``sharded.shard_plan`` -- opt_shard_plan: the data-parallel sharding plan
+  (``sharded`` also holds the per-rank views and the bf16 exchange)
 """
 
 from __future__ import annotations
@@ -73,7 +75,8 @@ class OptMuonHP(ctypes.Structure):
 _lib = None
 
 EXPORTED = ("opt_workspace_size", "opt_adamw_step", "opt_muon_step", "opt_mixed_step", "opt_mixed_step_clipped",
-            "opt_newton_schulz", "opt_newton_schulz_noalloc", "opt_reload_model_params", "opt_device_status",
+            "opt_newton_schulz", "opt_newton_schulz_noalloc", "opt_noalloc_device_status",
+            "opt_reload_model_params", "opt_device_status", "opt_shard_plan",
             "opt_selftest_wait_timeout", "opt_profile_launches",
             "opt_strerror",
             "opt_last_cuda_error", "opt_abi_version")
@@ -81,6 +84,10 @@ EXPORTED = ("opt_workspace_size", "opt_adamw_step", "opt_muon_step", "opt_mixed_
 KERNEL_NAMES = {0: "ns_gram", 1: "ns_poly", 2: "ns_bx", 3: "adamw", 4: "muon_momentum", 5: "muon_norm",
                 6: "muon_apply", 7: "muon_operands", 8: "grad_norm", 9: "clip_finalize"}
 WORKSPACE_CLIP = 0x10
+
+
+class OptShardEntry(ctypes.Structure):
+    _fields_ = [("owner", ctypes.c_int32), ("reserved", ctypes.c_int32), ("flat_begin", ctypes.c_int64)]
 
 
 class OptLaunchInfo(ctypes.Structure):
@@ -116,6 +123,11 @@ def lib():
     L.opt_newton_schulz.restype = ctypes.c_int
     L.opt_newton_schulz_noalloc.argtypes = [vp, vp, i64, i64, i32, f32, f32, f32, f32, vp]
     L.opt_newton_schulz_noalloc.restype = ctypes.c_int
+    L.opt_shard_plan.argtypes = [T, i32, i32, i32, i64, ctypes.POINTER(OptShardEntry), ctypes.POINTER(i64),
+                                 ctypes.POINTER(ctypes.c_double)]
+    L.opt_shard_plan.restype = ctypes.c_int
+    L.opt_noalloc_device_status.argtypes = [vp]
+    L.opt_noalloc_device_status.restype = ctypes.c_int
     L.opt_reload_model_params.argtypes = [T, i32, vp]
     L.opt_reload_model_params.restype = ctypes.c_int
     L.opt_device_status.argtypes = [vp, vp]

@@ -2,9 +2,12 @@
 // the launch sequence of one optimizer step.  See include/mpopt.h for the
 // contract of every entry point.
 
+#include <cuda.h>
+
 #include <cmath>
 #include <cstdio>
 #include <cstring>
+#include <algorithm>
 #include <map>
 #include <mutex>
 #include <utility>
@@ -79,18 +82,25 @@ opt_status check_fp32_ptr(const void* p) {
   return (reinterpret_cast<uintptr_t>(p) & 3u) ? OPT_ERR_MISALIGNED : OPT_OK;
 }
 
-// Per-tensor checks shared by both kinds.
-opt_status check_tensor(const opt_tensor& t, bool muon) {
+// Shape checks shared by both kinds (no pointer is read).
+opt_status check_shape(const opt_tensor& t, bool muon) {
   if (t.rows < 0 || t.cols < 0) return OPT_ERR_INVALID_ARG;
   if (t.ndim < 0) return OPT_ERR_INVALID_ARG;
   if (t.rows > 0 && t.cols > (INT64_MAX / t.rows)) return OPT_ERR_INVALID_ARG;
-  const int64_t n = t.rows * t.cols;
   if (muon) {
     if (t.ndim != 2) return OPT_ERR_INVALID_ARG;
     if (t.rows > (int64_t(1) << 30) || t.cols > (int64_t(1) << 30)) return OPT_ERR_UNSUPPORTED;
     if (t.scale_rows < 0 || t.scale_cols < 0 || ((t.scale_rows == 0) != (t.scale_cols == 0)))
       return OPT_ERR_INVALID_ARG;
   }
+  return OPT_OK;
+}
+
+// Per-tensor checks shared by both kinds.
+opt_status check_tensor(const opt_tensor& t, bool muon) {
+  const opt_status sh = check_shape(t, muon);
+  if (sh != OPT_OK) return sh;
+  const int64_t n = t.rows * t.cols;
   if (n == 0) return OPT_OK;
   if (!t.main_param || !t.main_grad || !t.exp_avg) return OPT_ERR_INVALID_ARG;
   if (!muon && !t.exp_avg_sq) return OPT_ERR_INVALID_ARG;
@@ -600,6 +610,64 @@ opt_status opt_mixed_step_clipped(const opt_muon_hp* hp_muon, const opt_adamw_hp
   return mixed_impl(hp_muon, hp_adamw, tensors, n, OPT_KIND_AUTO, workspace, workspace_bytes, stream, &clip);
 }
 
+opt_status opt_shard_plan(const opt_tensor* tensors, int32_t n, int32_t routing, int32_t world_size,
+                          int64_t align_elems, opt_shard_entry* entries, int64_t* rank_bounds,
+                          double* rank_muon_work) {
+  if (world_size < 1 || align_elems < 1 || (n > 0 && !entries) || !rank_bounds) return OPT_ERR_INVALID_ARG;
+  if (routing != OPT_KIND_AUTO && routing != OPT_KIND_ADAMW && routing != OPT_KIND_MUON) return OPT_ERR_INVALID_ARG;
+  if (n < 0 || (n > 0 && !tensors)) return OPT_ERR_INVALID_ARG;
+  for (int32_t i = 0; i < n; ++i) {
+    const opt_tensor& t = tensors[i];
+    if (t.kind != OPT_KIND_AUTO && t.kind != OPT_KIND_ADAMW && t.kind != OPT_KIND_MUON) return OPT_ERR_INVALID_ARG;
+    const opt_status st = check_shape(t, routes_to_muon(t, routing));   // shapes only: pointers may be null
+    if (st != OPT_OK) return st;
+  }
+  // AdamW: one index space in list order, cut into aligned, near-equal ranges
+  int64_t N = 0;
+  std::vector<double> work(static_cast<size_t>(world_size), 0.0);
+  std::vector<int32_t> muon_ids;
+  for (int32_t i = 0; i < n; ++i) {
+    const opt_tensor& t = tensors[i];
+    entries[i] = opt_shard_entry{-1, 0, -1};
+    const int64_t numel = t.rows * t.cols;
+    if (routes_to_muon(t, routing)) {
+      if (numel > 0) muon_ids.push_back(i);
+    } else {
+      entries[i].flat_begin = N;
+      N += numel;
+    }
+  }
+  rank_bounds[0] = 0;
+  for (int32_t r = 1; r < world_size; ++r) {
+    // r * N / world_size without overflow, then rounded up to the alignment
+    const int64_t q = N / world_size, rem = N % world_size;
+    const int64_t even = q * r + (rem * r) / world_size;
+    int64_t b = (even + align_elems - 1) / align_elems * align_elems;
+    if (b > N) b = N;
+    if (b < rank_bounds[r - 1]) b = rank_bounds[r - 1];
+    rank_bounds[r] = b;
+  }
+  rank_bounds[world_size] = N;
+  // Muon: LPT on the Newton-Schulz work of one iteration, 2 (2 A^2 B + A^3)
+  auto ns_work = [&](int32_t i) {
+    const double R = static_cast<double>(tensors[i].rows), C = static_cast<double>(tensors[i].cols);
+    const double A = R < C ? R : C, B = R < C ? C : R;
+    return 2.0 * (2.0 * A * A * B + A * A * A);
+  };
+  std::stable_sort(muon_ids.begin(), muon_ids.end(),
+                   [&](int32_t a, int32_t b) { return ns_work(a) > ns_work(b); });
+  for (int32_t i : muon_ids) {
+    int32_t best = 0;
+    for (int32_t r = 1; r < world_size; ++r)
+      if (work[static_cast<size_t>(r)] < work[static_cast<size_t>(best)]) best = r;
+    entries[i].owner = best;
+    work[static_cast<size_t>(best)] += ns_work(i);
+  }
+  if (rank_muon_work)
+    for (int32_t r = 0; r < world_size; ++r) rank_muon_work[r] = work[static_cast<size_t>(r)];
+  return OPT_OK;
+}
+
 opt_status opt_reload_model_params(const opt_tensor* tensors, int32_t n, void* stream) {
   if (n < 0 || (n > 0 && !tensors)) return OPT_ERR_INVALID_ARG;
   for (int32_t i = 0; i < n; ++i) {
@@ -762,24 +830,65 @@ namespace {
 
 constexpr int kNoallocMaxDevices = 64;
 std::mutex g_noalloc_mu;
-uint8_t* g_noalloc_base[kNoallocMaxDevices] = {};
+// Per device: the array's address and the id of the CUDA context it belongs
+// to.  A context that is torn down (cudaDeviceReset) and created again gets a
+// new id, and with it a new copy of the array at a possibly different address.
+struct NoallocSlot {
+  uint8_t* base;
+  unsigned long long ctx_id;
+};
+NoallocSlot g_noalloc[kNoallocMaxDevices] = {};
 
-// Device address of the scratch array on the current device; the first call on
-// each device looks it up (once, under a lock).
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+// Unique id of the context current on this thread (driver entry points, so the
+// library keeps linking only the runtime); 0 if there is none or the driver
+// cannot tell.
+unsigned long long current_context_id() {
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<CtxGetIdFn>(p);
+  });
+  if (!get_current || !get_id) return 0;
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_current(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
+// Device address of the scratch array on the current device.  The address is
+// looked up (under a lock) on the first call on each device, and again whenever
+// the device's context has changed since -- after a cudaDeviceReset the old
+// address is stale.  Without a context id from the driver it is looked up on
+// every call.
 opt_status noalloc_scratch(uint8_t** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "noalloc: current device");
   if (dev < 0 || dev >= kNoallocMaxDevices) return OPT_ERR_UNSUPPORTED;
   std::lock_guard<std::mutex> lock(g_noalloc_mu);
-  if (!g_noalloc_base[dev]) {
+  NoallocSlot& slot = g_noalloc[dev];
+  const unsigned long long id = current_context_id();
+  if (!slot.base || id == 0 || id != slot.ctx_id) {
     void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);   // creates the context if there is none yet
     if (e != cudaSuccess) return cuda_fail(e, "noalloc: scratch symbol address");
     if (reinterpret_cast<uintptr_t>(p) & 255u) return OPT_ERR_WORKSPACE;
-    g_noalloc_base[dev] = static_cast<uint8_t*>(p);
+    slot.base = static_cast<uint8_t*>(p);
+    slot.ctx_id = id ? id : current_context_id();
   }
-  *out = g_noalloc_base[dev];
+  *out = slot.base;
   return OPT_OK;
 }
 
@@ -826,4 +935,12 @@ extern "C" opt_status opt_newton_schulz_noalloc(const float* G, float* O, int64_
   float* outs[1] = {O};
   return run_muon_class(hp, classes[0], base + kHeaderBytes, kNoallocScratchBytes - kHeaderBytes,
                         reinterpret_cast<uint32_t*>(base), s, outs);
+}
+
+extern "C" opt_status opt_noalloc_device_status(void* stream) {
+  using namespace mpopt;
+  uint8_t* base = nullptr;
+  const opt_status st = noalloc_scratch(&base);
+  if (st != OPT_OK) return st;
+  return opt_device_status(base, stream);
 }

@@ -121,8 +121,25 @@ struct WMaps {
   CUtensorMap w[kMaxGroup];    // fp32 master W [R][C], 128-byte swizzle
   CUtensorMap wb[kMaxGroup];   // bf16 model copy [R][C], 64-byte swizzle
 };
-static_assert(4 * sizeof(CUtensorMap) + sizeof(GemmParams) + sizeof(MuonGroup) + sizeof(WMaps) + 256 <= 32764,
+
+// Arguments only the last C X reads: the group's matrices (W, its bf16 copy,
+// the update scale) and their tensor maps.  The other launches take the empty
+// form, so that their parameter blocks stay under 1 KB: launches whose
+// parameters are tens of KB fill the driver's launch queue after about 180
+// pending launches and then block the host thread until earlier ones finish.
+template <bool kFinal>
+struct FinalArgs {
+  int32_t unused;
+};
+template <>
+struct FinalArgs<true> {
+  MuonGroup grp;
+  WMaps wm;
+};
+static_assert(4 * sizeof(CUtensorMap) + sizeof(GemmParams) + sizeof(FinalArgs<true>) + 256 <= 32764,
               "kernel parameters above the 32 KB parameter space");
+static_assert(4 * sizeof(CUtensorMap) + sizeof(GemmParams) + sizeof(FinalArgs<false>) <= 1024,
+              "parameters of the non-final GEMM launches above 1 KB");
 
 // ------------------------------------------------------------ PTX helpers --
 
@@ -538,11 +555,13 @@ __device__ __forceinline__ void epilogue_block(const GemmParams& P, const MuonGr
 
 // ------------------------------------------------------------------ kernel --
 
+// kFinal: the last C X of the iteration (mode kBxFinal), which reads the
+// group's matrices and W maps from `fa`; every other launch has kFinal false.
+template <bool kFinal>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 ns_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                const __grid_constant__ CUtensorMap map_out, const __grid_constant__ CUtensorMap map_out32,
-               const __grid_constant__ GemmParams P,
-               const __grid_constant__ MuonGroup grp, const __grid_constant__ WMaps wm) {
+               const __grid_constant__ GemmParams P, const __grid_constant__ FinalArgs<kFinal> fa) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* stage_a = smem;                                  // kStages x 16 KB
@@ -722,10 +741,16 @@ ns_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
         if (!ok) break;
         mma_commit_pair(smem_u32(&acc_full[acc]));
       }
-      // drain: every MMA issued by this thread has completed before TMEM goes
+      // drain: every MMA issued by this thread has completed before TMEM goes;
+      // a drain that runs out is recorded like any other timed-out wait
       mma_commit_local(smem_u32(drain));
       const unsigned long long t0 = global_ns();
-      while (!mbar_try(smem_u32(drain), 0) && global_ns() - t0 < kWaitLimitNs) {
+      while (!mbar_try(smem_u32(drain), 0)) {
+        if (global_ns() - t0 > kWaitLimitNs) {
+          *abort_flag = 1u;
+          atomicCAS(P.status, 0u, static_cast<uint32_t>(kStatusTimeoutDrain));
+          break;
+        }
       }
     }
   } else if (warp < 2 + kEpiWarps) {
@@ -738,7 +763,7 @@ ns_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
     uint8_t* out_stage = scratch + (warp - 2) * kWarpScratch;
     float* slab = reinterpret_cast<float*>(out_stage);
     uint32_t out_blocks = 0;
-    const bool w_tma = P.mode == kBxFinal && P.w_tma != 0;
+    const bool w_tma = kFinal && P.w_tma != 0;
     const uint32_t wbar = smem_u32(&wload[warp - 2]);
     uint32_t wphase = 0;
     bool wait_failed = false;
@@ -772,12 +797,17 @@ ns_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
         float v[32];
         // last C X through TMA: this block of W, in W's own layout (W rows are
         // the iterate's rows, or its columns for a tall W)
-        const bool tall = w_tma && grp.mats[t.mat].transposed != 0;
-        const int wx = tall ? row0 : t.tn * BN + c0, wy = tall ? t.tn * BN + c0 : row0;
-        if (w_tma && lane == 0) {
-          if (out_blocks > 0) bulk_wait_read_0();   // the previous block's stores have read the staging area
-          mbar_expect_tx(wbar, kOutBlockBytes32);
-          tma_load_2d_local(smem_u32(out_stage), &wm.w[t.mat], wbar, wx, wy, l2_evict_first());
+        bool tall = false;
+        int wx = 0, wy = 0;
+        if constexpr (kFinal) {
+          tall = w_tma && fa.grp.mats[t.mat].transposed != 0;
+          wx = tall ? row0 : t.tn * BN + c0;
+          wy = tall ? t.tn * BN + c0 : row0;
+          if (w_tma && lane == 0) {
+            if (out_blocks > 0) bulk_wait_read_0();   // the previous block's stores have read the staging area
+            mbar_expect_tx(wbar, kOutBlockBytes32);
+            tma_load_2d_local(smem_u32(out_stage), &fa.wm.w[t.mat], wbar, wx, wy, l2_evict_first());
+          }
         }
         __syncwarp();
         tmem_ld32(taddr + c0, v);
@@ -843,68 +873,70 @@ ns_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
             bulk_commit();
           }
           ++out_blocks;
-        } else if (w_tma) {
-          // W <- W (1 - lr wd) - lr scale X', updated in place in the staging
-          // area (128-byte swizzle: 16-byte chunk q of row r at q ^ (r & 7)),
-          // its bf16 copy staged 4 KB further (64-byte swizzle); both leave by
-          // TMA stores, which clip at the matrix edge
-          if (!mbar_wait(wbar, wphase, abort_flag, P.status, kStatusTimeoutWload)) {
-            wait_failed = true;
-            break;
-          }
-          wphase ^= 1u;
-          const MuonMat& M = grp.mats[t.mat];
-          const float decay = P.decay, scale = M.step_scale;
-          uint8_t* wbf = out_stage + kOutBlockBytes32;
-          if (tall) {
-            // lane t holds W column t of the block: element (j, t) for row j
-            const uint32_t q32 = static_cast<uint32_t>(lane) >> 2, w32 = (static_cast<uint32_t>(lane) & 3u) * 4u;
-            const uint32_t q16 = static_cast<uint32_t>(lane) >> 3, w16 = (static_cast<uint32_t>(lane) & 7u) * 2u;
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              float* e = reinterpret_cast<float*>(out_stage + j * 128 + ((q32 ^ (static_cast<uint32_t>(j) & 7u)) * 16) + w32);
-              const float wv = *e * decay - scale * v[j];
-              *e = wv;
-              *reinterpret_cast<uint16_t*>(wbf + j * 64 + ((q16 ^ ((static_cast<uint32_t>(j) >> 1) & 3u)) * 16) + w16) =
-                  bf16_rne(wv);
+        } else if constexpr (kFinal) {
+          if (w_tma) {
+            // W <- W (1 - lr wd) - lr scale X', updated in place in the staging
+            // area (128-byte swizzle: 16-byte chunk q of row r at q ^ (r & 7)),
+            // its bf16 copy staged 4 KB further (64-byte swizzle); both leave by
+            // TMA stores, which clip at the matrix edge
+            if (!mbar_wait(wbar, wphase, abort_flag, P.status, kStatusTimeoutWload)) {
+              wait_failed = true;
+              break;
             }
+            wphase ^= 1u;
+            const MuonMat& M = fa.grp.mats[t.mat];
+            const float decay = P.decay, scale = M.step_scale;
+            uint8_t* wbf = out_stage + kOutBlockBytes32;
+            if (tall) {
+              // lane t holds W column t of the block: element (j, t) for row j
+              const uint32_t q32 = static_cast<uint32_t>(lane) >> 2, w32 = (static_cast<uint32_t>(lane) & 3u) * 4u;
+              const uint32_t q16 = static_cast<uint32_t>(lane) >> 3, w16 = (static_cast<uint32_t>(lane) & 7u) * 2u;
+#pragma unroll
+              for (int j = 0; j < 32; ++j) {
+                float* e = reinterpret_cast<float*>(out_stage + j * 128 + ((q32 ^ (static_cast<uint32_t>(j) & 7u)) * 16) + w32);
+                const float wv = *e * decay - scale * v[j];
+                *e = wv;
+                *reinterpret_cast<uint16_t*>(wbf + j * 64 + ((q16 ^ ((static_cast<uint32_t>(j) >> 1) & 3u)) * 16) + w16) =
+                    bf16_rne(wv);
+              }
+            } else {
+              // lane t holds W row t of the block
+#pragma unroll
+              for (int q = 0; q < 8; ++q) {
+                float4* e = reinterpret_cast<float4*>(out_stage + lane * 128 + ((static_cast<uint32_t>(q) ^ (static_cast<uint32_t>(lane) & 7u)) * 16));
+                float4 o = *e;
+                o.x = o.x * decay - scale * v[4 * q + 0];
+                o.y = o.y * decay - scale * v[4 * q + 1];
+                o.z = o.z * decay - scale * v[4 * q + 2];
+                o.w = o.w * decay - scale * v[4 * q + 3];
+                *e = o;
+                v[4 * q + 0] = o.x;
+                v[4 * q + 1] = o.y;
+                v[4 * q + 2] = o.z;
+                v[4 * q + 3] = o.w;
+              }
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                const uint32_t phys = static_cast<uint32_t>(q) ^ ((static_cast<uint32_t>(lane) >> 1) & 3u);
+                *reinterpret_cast<uint4*>(wbf + lane * 64 + phys * 16) = make_uint4(
+                    static_cast<uint32_t>(bf16_rne(v[8 * q + 0])) | (static_cast<uint32_t>(bf16_rne(v[8 * q + 1])) << 16),
+                    static_cast<uint32_t>(bf16_rne(v[8 * q + 2])) | (static_cast<uint32_t>(bf16_rne(v[8 * q + 3])) << 16),
+                    static_cast<uint32_t>(bf16_rne(v[8 * q + 4])) | (static_cast<uint32_t>(bf16_rne(v[8 * q + 5])) << 16),
+                    static_cast<uint32_t>(bf16_rne(v[8 * q + 6])) | (static_cast<uint32_t>(bf16_rne(v[8 * q + 7])) << 16));
+              }
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              const uint64_t pol = l2_evict_first();
+              tma_store_2d(&fa.wm.w[t.mat], smem_u32(out_stage), wx, wy, pol);
+              if (M.Wb) tma_store_2d(&fa.wm.wb[t.mat], smem_u32(wbf), wx, wy, pol);
+              bulk_commit();
+            }
+            ++out_blocks;
           } else {
-            // lane t holds W row t of the block
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-              float4* e = reinterpret_cast<float4*>(out_stage + lane * 128 + ((static_cast<uint32_t>(q) ^ (static_cast<uint32_t>(lane) & 7u)) * 16));
-              float4 o = *e;
-              o.x = o.x * decay - scale * v[4 * q + 0];
-              o.y = o.y * decay - scale * v[4 * q + 1];
-              o.z = o.z * decay - scale * v[4 * q + 2];
-              o.w = o.w * decay - scale * v[4 * q + 3];
-              *e = o;
-              v[4 * q + 0] = o.x;
-              v[4 * q + 1] = o.y;
-              v[4 * q + 2] = o.z;
-              v[4 * q + 3] = o.w;
-            }
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              const uint32_t phys = static_cast<uint32_t>(q) ^ ((static_cast<uint32_t>(lane) >> 1) & 3u);
-              *reinterpret_cast<uint4*>(wbf + lane * 64 + phys * 16) = make_uint4(
-                  static_cast<uint32_t>(bf16_rne(v[8 * q + 0])) | (static_cast<uint32_t>(bf16_rne(v[8 * q + 1])) << 16),
-                  static_cast<uint32_t>(bf16_rne(v[8 * q + 2])) | (static_cast<uint32_t>(bf16_rne(v[8 * q + 3])) << 16),
-                  static_cast<uint32_t>(bf16_rne(v[8 * q + 4])) | (static_cast<uint32_t>(bf16_rne(v[8 * q + 5])) << 16),
-                  static_cast<uint32_t>(bf16_rne(v[8 * q + 6])) | (static_cast<uint32_t>(bf16_rne(v[8 * q + 7])) << 16));
-            }
+            epilogue_block(P, fa.grp, t, slab, lane, row0, t.tn * BN + c0, v);
           }
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            const uint64_t pol = l2_evict_first();
-            tma_store_2d(&wm.w[t.mat], smem_u32(out_stage), wx, wy, pol);
-            if (M.Wb) tma_store_2d(&wm.wb[t.mat], smem_u32(wbf), wx, wy, pol);
-            bulk_commit();
-          }
-          ++out_blocks;
-        } else {
-          epilogue_block(P, grp, t, slab, lane, row0, t.tn * BN + c0, v);
         }
       }
       if (wait_failed) break;
@@ -1079,28 +1111,43 @@ bool make_w_maps(const MuonGroup& grp, WMaps* wm) {
   return true;
 }
 
-cudaError_t launch_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mo, const CUtensorMap& mo32,
-                        const GemmParams& P, const MuonGroup& grp, const WMaps& wm,
-                        cudaStream_t stream) {
+cudaError_t configure_gemm() {
   static thread_local int configured_dev = -1;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (configured_dev != dev) {
-    e = cudaFuncSetAttribute(ns_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    e = cudaFuncSetAttribute(ns_gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(ns_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
     configured_dev = dev;
   }
+  return cudaSuccess;
+}
+
+int gemm_grid(const GemmParams& P) {
   const int max_pairs = num_sms() / 2;
-  const int pairs = P.total_tiles < max_pairs ? P.total_tiles : max_pairs;
-  ns_gemm_kernel<<<2 * pairs, kThreads, kSmemBytes, stream>>>(ma, mb, mo, mo32, P, grp, wm);
+  return 2 * (P.total_tiles < max_pairs ? P.total_tiles : max_pairs);
+}
+
+// X X^T, A A and every C X but the last
+cudaError_t launch_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mo, const CUtensorMap& mo32,
+                        const GemmParams& P, cudaStream_t stream) {
+  cudaError_t e = configure_gemm();
+  if (e != cudaSuccess) return e;
+  const FinalArgs<false> none{};
+  ns_gemm_kernel<false><<<gemm_grid(P), kThreads, kSmemBytes, stream>>>(ma, mb, mo, mo32, P, none);
   return cudaGetLastError();
 }
 
-// The maps argument of the launches that do not use it.
-const WMaps& no_maps() {
-  static const WMaps none{};
-  return none;
+// the last C X, which updates W (or writes the Newton-Schulz output)
+cudaError_t launch_gemm_final(const CUtensorMap& ma, const CUtensorMap& mb, const GemmParams& P,
+                              const FinalArgs<true>& fa, cudaStream_t stream) {
+  cudaError_t e = configure_gemm();
+  if (e != cudaSuccess) return e;
+  ns_gemm_kernel<true><<<gemm_grid(P), kThreads, kSmemBytes, stream>>>(ma, mb, mb, mb, P, fa);
+  return cudaGetLastError();
 }
 
 }  // namespace
@@ -1142,7 +1189,7 @@ cudaError_t launch_ns_iteration(const MuonGroup& grp, const NsBuffers& buf, cons
     P.Ah = buf.Ah;
     P.stall = (s.stall_first_stage && it == 0) ? 1 : 0;
     prof_begin(OPT_KERNEL_NS_GRAM, grp.count, grp.A, grp.B, stream);
-    e = launch_gemm(ma, mb, mo, mo32, P, grp, no_maps(), stream);
+    e = launch_gemm(ma, mb, mo, mo32, P, stream);
     prof_end(stream);
     if (e != cudaSuccess) return e;
   }
@@ -1161,7 +1208,7 @@ cudaError_t launch_ns_iteration(const MuonGroup& grp, const NsBuffers& buf, cons
     P.Af = buf.Af;
     P.Ch = buf.Ch;
     prof_begin(OPT_KERNEL_NS_POLY, grp.count, grp.A, grp.B, stream);
-    e = launch_gemm(ma, mb, mo, mo, P, grp, no_maps(), stream);   // no fp32 output
+    e = launch_gemm(ma, mb, mo, mo, P, stream);   // no fp32 output
     prof_end(stream);
     if (e != cudaSuccess) return e;
   }
@@ -1171,20 +1218,27 @@ cudaError_t launch_ns_iteration(const MuonGroup& grp, const NsBuffers& buf, cons
     CUtensorMap ma, mb;
     if ((e = make_map(&ma, buf.Ch, Ap, Ap, cnt, BM)) != cudaSuccess) return e;
     if ((e = make_map_mn(&mb, X, Bp, Ap, cnt)) != cudaSuccess) return e;
-    CUtensorMap mo = mb;   // the last iteration updates W instead
-    if (it != s.ns_steps - 1 && (e = make_out_map(&mo, X_next, Bp, Ap, cnt)) != cudaSuccess) return e;
+    const bool last = it == s.ns_steps - 1;
     GemmParams P = base;
-    P.mode = (it == s.ns_steps - 1) ? kBxFinal : kBx;
+    P.mode = last ? kBxFinal : kBx;
     P.k_blocks = static_cast<int>(Ap / 64);
     P.tiles_m = static_cast<int>(Ap / BM_PAIR);
     P.tiles_per_mat = static_cast<int>((Ap / BM_PAIR) * (Bp / BN));
     P.total_tiles = P.tiles_per_mat * grp.count;
     P.Xh = X_next;
-    // the last iteration's update of W moves through TMA when every matrix allows it
-    static thread_local WMaps wm;
-    P.w_tma = (P.mode == kBxFinal && !s.ns_only && make_w_maps(grp, &wm)) ? 1 : 0;
     prof_begin(OPT_KERNEL_NS_BX, grp.count, grp.A, grp.B, stream);
-    e = launch_gemm(ma, mb, mo, mo, P, grp, P.w_tma ? wm : no_maps(), stream);   // no fp32 output
+    if (last) {
+      // the last iteration's update of W moves through TMA when every matrix allows it
+      static thread_local FinalArgs<true> fa;
+      fa.grp = grp;
+      P.w_tma = (!s.ns_only && make_w_maps(grp, &fa.wm)) ? 1 : 0;
+      if (!P.w_tma) fa.wm = WMaps{};
+      e = launch_gemm_final(ma, mb, P, fa, stream);
+    } else {
+      CUtensorMap mo;
+      if ((e = make_out_map(&mo, X_next, Bp, Ap, cnt)) != cudaSuccess) return e;
+      e = launch_gemm(ma, mb, mo, mo, P, stream);   // no fp32 output
+    }
     prof_end(stream);
     if (e != cudaSuccess) return e;
   }

@@ -144,6 +144,21 @@ def llama_mlp_1layer():
     return Workload("llama_mlp_1layer", ts, steps=10, adamw=None, muon=MuonHP(weight_decay=0.0))
 
 
+def attn_qo8():
+    """Eight 4096 x 4096 matrices (the q/o shape class of the 16-layer set) under
+    Muon: 256 MB of fp16 iterate, larger than L2, a few GB in all; the small
+    case for profiling that class."""
+    ts = tuple(TensorSpec(f"qo{i}", (4096, 4096), "normal", 0.02) for i in range(8))
+    return Workload("attn_qo8", ts, steps=10, adamw=None, muon=MuonHP(weight_decay=0.0))
+
+
+def attn_kv32():
+    """The 32 k/v matrices (1024 x 4096) of the 16-layer set under Muon: that
+    shape class's group exactly as the full step batches it."""
+    ts = tuple(TensorSpec(f"kv{i}", (1024, 4096), "normal", 0.02) for i in range(32))
+    return Workload("attn_kv32", ts, steps=10, adamw=None, muon=MuonHP(weight_decay=0.0))
+
+
 WORKLOADS = {
     "tiny_mixed": tiny_mixed,
     "adamw_8m": adamw_8m,
@@ -151,6 +166,8 @@ WORKLOADS = {
     "adamw_sweep_10k": adamw_sweep_10k,
     "llama16_mixed": llama16_mixed,
     "llama_mlp_1layer": llama_mlp_1layer,
+    "attn_qo8": attn_qo8,
+    "attn_kv32": attn_kv32,
 }
 
 

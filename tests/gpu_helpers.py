@@ -58,3 +58,37 @@ class AdamwState:
 
     def param(self):
         return mp.Param(self.d["p"], self.d["g"], self.d["m"], self.d["v"], self.model)
+
+
+def singular_values(O) -> np.ndarray:
+    """Singular values of a matrix, ascending: square roots of the
+    eigenvalues of the Gram matrix of its wide orientation (fp64; clipped at
+    zero, so near-zero singular values are exact to about 1e-7)."""
+    O = np.asarray(O, dtype=np.float64)
+    X = O if O.shape[0] <= O.shape[1] else O.T
+    ev = np.linalg.eigvalsh(X @ X.T)
+    return np.sqrt(np.clip(ev, 0.0, None))
+
+
+# Square matrices: a noise-dominated square gradient has singular values near
+# zero that five quintic steps do not lift into [0.6, 1.3], even in exact
+# arithmetic, so the bound on the update's spectrum becomes: the sorted
+# singular values of the output match those of the fp64 oracle's output, each
+# within SQUARE_SV_TOL (the distance between the two spectra as
+# distributions; it also bounds any histogram of them: counts differ only by
+# values within SQUARE_SV_TOL of a bin edge), and none exceeds SQUARE_SV_MAX.
+SQUARE_SV_TOL = 0.05
+SQUARE_SV_MAX = 1.3
+
+
+def assert_square_spectrum(got, want, what=""):
+    sg, sw = singular_values(got), singular_values(want)
+    dev_max = float(np.max(np.abs(sg - sw)))
+    assert dev_max <= SQUARE_SV_TOL, f"{what}: sorted singular values differ by up to {dev_max:.3g}"
+    assert sg.max() <= SQUARE_SV_MAX, f"{what}: largest singular value {sg.max():.4f}"
+    edges = np.linspace(0.0, 1.4, 15)
+    hg, _ = np.histogram(sg, edges)
+    hw, _ = np.histogram(sw, edges)
+    near = sum(int(np.sum(np.abs(sw - e) <= SQUARE_SV_TOL)) for e in edges)
+    assert int(np.abs(hg - hw).sum()) <= 2 * near, f"{what}: histograms {hg} vs {hw}"
+    return dev_max

@@ -78,24 +78,47 @@ def test_smi_index(monkeypatch):
 
 def test_gemm_flop_accounting_matches_pages_formula():
     """One Newton-Schulz iteration's three launches add up to the pages'
-    4 m^2 n + 2 m^3 (per matrix)."""
+    4 m^2 n + 2 m^3 per matrix (dense count); the method's count (the
+    roofline's) takes the symmetric products at their triangle, 3 m^2 n + m^3;
+    the executed count lies between the two for large shapes."""
     for A, B in ((1024, 4096), (4096, 14336), (256, 512)):
         recs = [dict(kernel=k, count=3, a=A, b=B) for k in ("ns_gram", "ns_poly", "ns_bx")]
         assert sum(bench.gemm_flops(r) for r in recs) == 3 * OM.ns_flops(A, B, 1)
+        assert sum(bench.gemm_method_flops(r) for r in recs) == 3 * (3 * A * A * B + A ** 3)
+        ex = sum(bench.gemm_executed_flops(r) for r in recs)
+        assert sum(bench.gemm_method_flops(r) for r in recs) <= ex <= sum(bench.gemm_flops(r) for r in recs)
         # executed <= algorithmic for the symmetric stages
         assert bench.gemm_executed_flops(recs[0]) < bench.gemm_flops(recs[0]) or A == 256
 
 
-def test_reference_arm_line():
-    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload",
-                        "tiny_mixed", "--steps", "1", "--warmup", "0"], capture_output=True, text=True,
+def _run_bench(*args):
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), *args], capture_output=True, text=True,
                        timeout=600, env=dict(os.environ, WORLD_SIZE="1"))
     assert r.returncode == 0, r.stderr
     lines = [l for l in r.stdout.splitlines() if l.strip()]
     assert len(lines) == 1
-    d = json.loads(lines[0])
+    return json.loads(lines[0])
+
+
+def test_reference_arm_line():
+    d = _run_bench("--impl", "reference", "--workload", "tiny_mixed", "--steps", "1", "--warmup", "0")
     assert d["impl"] == "reference" and d["unit"] == "params/s" and d["value"] > 0
     assert d["cpu_baseline"]["kind"] == "oracle" and d["e2e"]["h2d_bytes_per_step"] == 0
+    assert d["cpu_baseline"]["value"] == d["value"] and d["cpu_baseline"]["extrapolated"] is False
+    # the same config dict as our arm builds for the workload
+    assert d["config"] == bench.workload_config(bench.S.tiny_mixed(), 0.0)
+
+
+def test_cpu_sample_is_shared_and_fixed():
+    """Both arms time one fixed sample: the Muon classes whose Newton-Schulz
+    is small enough run through the oracle, larger ones are extrapolated and
+    say so."""
+    w = bench.S.llama16_mixed()
+    t, desc = bench.cpu_oracle_sample(bench.S.scaled_copy(bench.S.muon_8m_skewed(), "two", [(64, 128), (128, 64)]))
+    assert t > 0 and desc["extrapolated"] is True        # two matrices of one class, timed on one
+    classes = {tuple(sorted(sp.shape)) for sp in w.tensors if bench.is_muon(w, sp)}
+    runs = sorted(c for c in classes if OM.ns_flops(*c) <= bench.MUON_SAMPLE_FLOPS)
+    assert runs == [(1024, 4096)]
 
 
 def test_profile_rows_apply_only_to_their_source(tmp_path, monkeypatch):
@@ -108,15 +131,17 @@ def test_profile_rows_apply_only_to_their_source(tmp_path, monkeypatch):
     (csrc / "ns_gemm.cu").write_bytes(b"kernel v1")
     (csrc / "adamw.cu").write_bytes(b"adamw v1")
     sha = hashlib.sha256(b"kernel v1").hexdigest()[:16]
-    (tmp_path / "profiles" / "dram_traffic_llama16_mixed.md").write_text(f"| ns_gemm | {sha} | 1.5e9 |\n| adamw | 0000000000000000 | 3e9 |\n")
-    (tmp_path / "profiles" / "ns_gemm_llama_mlp_1layer.md").write_text(f"| tensor_pipe | {sha} | 70.5 | 60.0 | 85.25 |\n")
+    rows = {"ns_gemm_traffic": {"source": "ns_gemm.cu", "sha256_16": sha, "bytes_per_launch": 1.5e9},
+            "adamw_traffic": {"source": "adamw.cu", "sha256_16": "0000000000000000", "bytes_per_launch": 3e9},
+            "ns_gemm_tensor_pipe": {"source": "ns_gemm.cu", "sha256_16": sha,
+                                    "pct": {"gram": 70.5, "poly": 60.0, "bx": 85.25}}}
+    (tmp_path / "profiles" / "rows.json").write_text(json.dumps(rows))
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
-    assert bench.kernel_traffic("ns_gemm") == 1.5e9
-    assert bench.kernel_traffic("adamw") is None          # captured from another source
-    tp = bench.tensor_pipe_active()
-    assert (tp["gram"], tp["poly"], tp["bx"]) == (70.5, 60.0, 85.25)
+    assert bench.profile_row("ns_gemm_traffic")["bytes_per_launch"] == 1.5e9
+    assert bench.profile_row("adamw_traffic") is None          # captured from another source
+    assert bench.profile_row("ns_gemm_tensor_pipe")["pct"]["bx"] == 85.25
     (csrc / "ns_gemm.cu").write_bytes(b"kernel v2")       # source changed since the capture
-    assert bench.kernel_traffic("ns_gemm") is None and bench.tensor_pipe_active() is None
+    assert bench.profile_row("ns_gemm_traffic") is None and bench.profile_row("ns_gemm_tensor_pipe") is None
 
 
 def test_kernels_by_shape_groups_stages_and_classes():
@@ -124,10 +149,37 @@ def test_kernels_by_shape_groups_stages_and_classes():
             dict(kernel="ns_gram", count=48, a=4096, b=14336, ms=7.3),
             dict(kernel="ns_bx", count=32, a=1024, b=4096, ms=0.2),
             dict(kernel="adamw", count=2, a=1000, b=0, ms=5.0)]
-    out = bench.kernels_by_shape(recs)
+    out = bench.kernels_by_shape(recs, 1700.0)
     assert set(out) == {"ns_gram 4096x14336 x48", "ns_bx 1024x4096 x32"}
     g = out["ns_gram 4096x14336 x48"]
     assert g["launches"] == 2 and g["ms_per_launch"] == 7.4
-    # algorithmic 2 A^2 B per matrix; executed: 136 of the 256 blocks
-    assert g["tflops_algorithmic"] == round(48 * 2.0 * 4096 ** 2 * 14336 / 7.4e-3 / 1e12, 1)
-    assert g["tflops_executed"] == round(48 * 136 * 2.0 * 256 * 256 * 14336 / 7.4e-3 / 1e12, 1)
+    # pages' count 2 A^2 B per matrix; the method's A^2 B; executed: 136 of the 256 blocks
+    assert g["tflops_pages_count"] == round(48 * 2.0 * 4096 ** 2 * 14336 / 7.4e-3 / 1e12, 1)
+    assert g["tflops_method"] == round(48 * 1.0 * 4096 ** 2 * 14336 / 7.4e-3 / 1e12, 1)
+    ex = 48 * 136 * 2.0 * 256 * 256 * 14336 / 7.4e-3 / 1e12
+    assert g["tflops_executed"] == round(ex, 1) and g["executed_frac"] == round(ex / 1700.0, 3)
+
+
+def test_measured_line_roofline_follows_from_the_kernels():
+    """frac = the method's flops of the GEMM launches / their event time / the
+    sustained peak; the executed and the pages' counts beside it."""
+    class A:
+        steps, clip, warmup = 2, 0.0, 1
+    class D:
+        world = 1
+    recs = []
+    for _ in range(2):
+        for k, ms in (("ns_gram", 7.0), ("ns_poly", 2.0), ("ns_bx", 14.0)):
+            recs.append(dict(kernel=k, count=48, a=4096, b=14336, ms=ms))
+        recs.append(dict(kernel="adamw", count=35, a=1_000_000, b=0, ms=0.01))
+    peaks = {"hbm_gbs": 6787.2, "bf16_tflops": 1875.3, "bf16_tflops_sustained": 1708.2}
+    w = bench.S.llama_mlp_1layer()
+    line = bench.measured_line(A, w, recs, len(recs), 50.0, w.numel, D, peaks, "measured")
+    r = line["roofline"]
+    me = sum(bench.gemm_method_flops(x) for x in recs if x["kernel"] != "adamw")
+    ms = sum(x["ms"] for x in recs if x["kernel"] != "adamw")
+    assert r["achieved"] == round(me / (ms * 1e-3) / 1e12, 1)
+    assert r["frac"] == round(me / (ms * 1e-3) / 1e12 / 1708.2, 4)
+    assert r["executed_frac"] > r["frac"] and r["pages_count_frac"] > r["executed_frac"]
+    a = line["roofline_adamw"]
+    assert a["frac_of_nominal_8tbs"] == round(a["achieved"] / 8000.0, 4)

@@ -5,7 +5,10 @@ sampled outputs the oracle can compute one by one.
   two steps; AdamW checked bit-exact on sampled elements of the embedding, the
   LM head and norm vectors; Muon checked against the fp64 oracle on one matrix
   of each shape class (4096 x 4096, 1024 x 4096, 14336 x 4096 -- transposed --
-  and 4096 x 14336).
+  and 4096 x 14336): the update within 2e-2 relative Frobenius error, the
+  direction's singular values in [0.6, 1.3] on the rectangular classes and,
+  on the square class, within 0.05 of the oracle's sorted singular values
+  with none above 1.3.
 * adamw_sweep_10k (10,000 tensors, ~1.0e10 parameters, log-uniform sizes in
   [1, 2^24)): all 20 steps; bit-exact on sampled elements of every size
   decade.
@@ -20,7 +23,7 @@ import math
 import numpy as np
 import pytest
 
-from gpu_helpers import bf16_host, host, require_gpu, torch
+from gpu_helpers import assert_square_spectrum, bf16_host, host, require_gpu, singular_values, torch
 import bench
 import mixed_precision_optimizer_gb300 as mp
 from oracle import adamw as OA
@@ -114,6 +117,16 @@ def test_llama16_mixed_full_size_sampled():
             W1 = host(params[i].main_param).astype(np.float64)
             rel = np.linalg.norm((W0 - W1) - (W0 - Wn)) / np.linalg.norm(W0 - Wn)
             assert rel < 2e-2, (shape, rel)
+            # the update's direction O: singular values in [0.6, 1.3] on the
+            # rectangular classes; on the square q/o class the spectrum of the
+            # fp64 oracle's O (sorted values within 0.05, none above 1.3)
+            s = w.muon.lr * OM.update_scale(*shape)
+            O_gpu, O_want = (W0 - W1) / s, (W0 - Wn) / s
+            if shape[0] == shape[1]:
+                assert_square_spectrum(O_gpu, O_want, f"{shape}")
+            else:
+                sv = singular_values(O_gpu)
+                assert 0.6 <= sv.min() and sv.max() <= 1.3, (shape, sv.min(), sv.max())
             assert np.allclose(host(params[i].exp_avg), mn, rtol=1e-5, atol=1e-10)
             b = bf16_host(params[i].model)
             assert np.array_equal(b, OA.bf16_rne(host(params[i].main_param))), shape

@@ -3,7 +3,8 @@
 Tolerance (the bar for the Muon update): the update, and the Newton-Schulz
 output, within 2e-2 relative Frobenius error of the oracle's fp64
 Newton-Schulz; on rectangular matrices every singular value of the output
-in [0.6, 1.3].  The momentum buffer is fp32 arithmetic on the same inputs:
+in [0.6, 1.3]; on square matrices the sorted singular values of the output
+within 0.05 of the oracle's and none above 1.3 (gpu_helpers).  The momentum buffer is fp32 arithmetic on the same inputs:
 within 1e-5 relative per element (a few fp32 roundings).  The bf16 model copy
 is bit-exact against round-to-nearest-even of the GPU's own master weights.
 """
@@ -13,7 +14,7 @@ import math
 import numpy as np
 import pytest
 
-from gpu_helpers import bf16_host, dev, host, require_gpu, torch
+from gpu_helpers import assert_square_spectrum, bf16_host, dev, host, require_gpu, singular_values, torch
 import mixed_precision_optimizer_gb300 as mp
 from oracle import adamw as OA
 from oracle import muon as OM
@@ -105,6 +106,27 @@ def test_newton_schulz_diagonal_special_case():
     assert rel(got, want) < NS_TOL
 
 
+@pytest.mark.parametrize("shape,kind", [((96, 96), "gaussian"), ((512, 512), "gaussian"),
+                                        ((1024, 1024), "gaussian"), ((512, 512), "skewed"),
+                                        ((257, 257), "gaussian")])
+def test_newton_schulz_square_spectrum(shape, kind):
+    """Square matrices are not transposed, and their near-zero singular values
+    stay small after five steps: the output's sorted singular values match the
+    fp64 oracle's (each within 0.05) and none exceeds 1.3 ("02 · Optimizer：
+    算法与 infra" §5.2: the iteration acts on each singular value with the
+    quintic)."""
+    rng = np.random.default_rng(shape[0] * 3 + (kind == "skewed"))
+    if kind == "gaussian":
+        G = rng.standard_normal(shape).astype(np.float32)
+    else:
+        spec = S.TensorSpec("w", shape, "normal", 0.02, 1e-3, lowrank=8, lowrank_rms=1e-2)
+        G = S.grad_value(spec, 0, 1)
+    want = OM.newton_schulz(G.astype(np.float64))
+    got = ns_gpu(G)
+    assert rel(got, want) < NS_TOL
+    assert_square_spectrum(got, want, f"{shape} {kind}")
+
+
 # -------------------------------------------------------------- Muon step --
 
 def muon_case(shape, rng, *, weight_decay=0.0, nesterov=True, ns_steps=5, lr=0.02, mu=0.95, model=True,
@@ -131,15 +153,17 @@ def muon_case(shape, rng, *, weight_decay=0.0, nesterov=True, ns_steps=5, lr=0.0
         assert np.allclose(m1, mn, rtol=1e-5, atol=1e-9)
         if model:
             assert np.array_equal(bf16_host(Wb), OA.bf16_rne(W1))
-    return upd_gpu, lr * OM.update_scale(*shape)
+    return upd_gpu, upd_want, lr * OM.update_scale(*shape)
 
 
-@pytest.mark.parametrize("shape", [(256, 512), (512, 256), (300, 200), (96, 96), (1, 40), (40, 1)])
+@pytest.mark.parametrize("shape", [(256, 512), (512, 256), (300, 200), (96, 96), (512, 512), (1, 40), (40, 1)])
 def test_muon_step_shapes(shape):
-    upd, s = muon_case(shape, np.random.default_rng(shape[0] * 7 + shape[1]), steps=2)
+    upd, want, s = muon_case(shape, np.random.default_rng(shape[0] * 7 + shape[1]), steps=2)
     if 1 < shape[0] != shape[1] > 1:
-        sv = np.linalg.svd(upd / s, compute_uv=False)
+        sv = singular_values(upd / s)
         assert 0.6 <= sv.min() and sv.max() <= 1.3
+    elif shape[0] == shape[1] > 1:
+        assert_square_spectrum(upd / s, want / s, f"update {shape}")
 
 
 @pytest.mark.parametrize("kw", [dict(weight_decay=0.1), dict(nesterov=False), dict(ns_steps=1),

@@ -44,6 +44,8 @@ def without_allocation(Gd, steps):
                                             Gd.shape[0], Gd.shape[1], steps, a, b, c, 1e-7,
                                             ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
     assert st == mp.OPT_OK, mp.lib().opt_last_cuda_error()
+    # no device-side wait of the call ran out (status word of the built-in array)
+    assert mp.lib().opt_noalloc_device_status(ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)) == mp.OPT_OK
     return out
 
 
