@@ -3,6 +3,7 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload llama16_mixed|tiny_mixed|adamw_8m|muon_8m_skewed|adamw_sweep_10k]
+                    [--shard] [--clip MAX_NORM] [--no-sweep] [--clock-log DIR]
 
 A step is one full optimizer step over the workload: AdamW over every
 AdamW-routed tensor, Muon (momentum, Nesterov, five Newton-Schulz iterations,
@@ -13,10 +14,14 @@ whole path at scale.  Inputs are seeded synthetic tensors drawn on the GPU;
 the per-step inputs (~100 GB resident) are far larger than L2.
 
 Prints ONE JSON line on rank 0.  With --impl reference the line times the
-CPU oracle (numpy, fp64 Newton-Schulz) on a bounded sample of the same
-workload instead.  Under torchrun (N > 1) every rank runs an independent
-replica of the whole step on its own GPU (the step has no exchange); the
-process group is used only for barriers and the max-over-ranks time.
+CPU oracle (numpy, fp64 Newton-Schulz) on a fixed sample of one step of the
+same workload instead.  Under torchrun (N > 1) every rank by default runs an
+independent replica of the whole step on its own GPU, and the process group
+carries only barriers and the max-over-ranks time (weak scaling).  With
+--shard the ranks share one step (ZeRO-1 AdamW ranges, one owner per Muon
+matrix, the bf16 pieces exchanged by broadcasts; strong scaling).  After the
+main line's measurements the 10,000-tensor AdamW sweep reports GB/s per size
+decade (--no-sweep skips it).
 """
 
 from __future__ import annotations
@@ -60,6 +65,9 @@ def parse():
                          "Muon group, back to back for a few seconds each, for comparison only")
     ap.add_argument("--clip", type=float, default=0.0,
                     help="max_norm of global grad-norm clipping fused into the step (0: off)")
+    ap.add_argument("--shard", action="store_true",
+                    help="data-parallel sharded step over the ranks (ZeRO-1 AdamW ranges, one owner per Muon "
+                         "matrix, bf16 exchange by broadcasts); total work fixed as N grows (strong scaling)")
     ap.add_argument("--no-sweep", action="store_true",
                     help="skip the AdamW size sweep (10,000 tensors, GB/s per size decade) after the main workload")
     ap.add_argument("--clock-log", default=None, help="directory for the nvidia-smi clock samples (default: temp)")
@@ -523,15 +531,39 @@ def run_ours(args, dist: Dist):
     w = S.WORKLOADS[args.workload]()
     params, n_muon, n_adamw, flat = build_device_workload(w, device)
     total = n_muon + n_adamw
-    ws = mp.alloc_workspace(mp.workspace_size(params, clip=args.clip > 0), device)
     hm, ha = hyper(w)
-    prepared = mp.prepare(params)
-
-    def step(t, plist=prepared):
+    if args.shard:
+        # this rank keeps the replicated main_grad and bf16 model of every
+        # tensor, and master/state only for what the plan gives it
+        from mixed_precision_optimizer_gb300 import sharded as sh
         if args.clip > 0:
-            mp.mixed_step_clipped(plist, hm, ha(t), args.clip, ws)
-        else:
-            mp.mixed_step(plist, hm, ha(t), ws)
+            raise SystemExit("--shard with --clip is not supported (the norm would need a cross-rank sum)")
+        plan = sh.shard_plan(params, dist.world)
+        state = sh.RankState.empty(plan, dist.rank, device)
+        state.load(plan, params)
+        params = [mp.Param(None, p.main_grad, None, None, p.model, p.embedding_or_output, p.kind) for p in params]
+        torch.cuda.empty_cache()
+
+        def prepare_set(plist):
+            return plist, mp.prepare(sh.rank_params(plist, plan, state))
+
+        prepared = prepare_set(params)
+        ws = mp.alloc_workspace(mp.workspace_size(prepared[1].params), device)
+
+        def step(t, pset=None):
+            pset = prepared if pset is None else pset
+            sh.sharded_step(pset[0], plan, state, hm, ha(t), ws, prepared=pset[1])
+    else:
+        prepare_set = mp.prepare
+        ws = mp.alloc_workspace(mp.workspace_size(params, clip=args.clip > 0), device)
+        prepared = mp.prepare(params)
+
+        def step(t, plist=None):
+            plist = prepared if plist is None else plist
+            if args.clip > 0:
+                mp.mixed_step_clipped(plist, hm, ha(t), args.clip, ws)
+            else:
+                mp.mixed_step(plist, hm, ha(t), ws)
 
     stream = torch.cuda.current_stream()
     t = 1
@@ -549,9 +581,12 @@ def run_ours(args, dist: Dist):
         dist.barrier()
         torch.cuda.synchronize()
         start.record(stream)
+        host_ms = []
         with prof:
             for _ in range(args.steps):
+                h0 = time.perf_counter()
                 step(t)
+                host_ms.append((time.perf_counter() - h0) * 1e3)
                 t += 1
         end.record(stream)
         torch.cuda.synchronize()
@@ -565,9 +600,13 @@ def run_ours(args, dist: Dist):
     # ---- per-kernel breakdown from the events around each launch
     peaks, peak_src = load_peaks()
     line = measured_line(args, w, recs, launches, elapsed_ms, total, dist, peaks, peak_src)
+    # host time of each step call: the first starts on an empty launch queue;
+    # later ones block only once the queue holds more launches than it takes
+    line["host_enqueue_ms"] = {"first_step": round(host_ms[0], 3), "median": round(statistics.median(host_ms), 3),
+                               "max": round(max(host_ms), 3), "launches_per_step": launches // args.steps}
 
     # ---- end to end through the public API with host buffers
-    line["e2e"] = run_e2e(args, step, params, flat, t, total, dist)
+    line["e2e"] = run_e2e(args, step, prepare_set, params, flat, t, total, dist)
     t += args.e2e_steps
     line["clocks"] = clocks.summary()
     if args.compare_cublas and dist.rank == 0:
@@ -669,17 +708,21 @@ def measured_line(args, w, recs, launches, elapsed_ms, total, dist, peaks, peak_
                           "frac_of_nominal_8tbs": round(gbs / NOMINAL_HBM_GBS, 4),
                           "traffic": row.get("bytes_per_launch"), "peak_source": f"{peak_src} hbm_gbs (of measured)",
                           "per_launch_bytes": round(k["elems"] * ADAMW_BYTES_PER_PARAM / k["launches"])}
-    value = total * args.steps * dist.world / (elapsed_ms * 1e-3)
+    shard = getattr(args, "shard", False)
+    # replicas: every rank steps the whole workload; sharded: the ranks
+    # together step it once per step
+    value = total * args.steps * (1 if shard else dist.world) / (elapsed_ms * 1e-3)
     cfg = workload_config(w, args.clip)
     return {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": dist.world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(elapsed_ms / args.steps, 3), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "scaling": "strong" if shard else "weak", "vs_baseline": None, "dtype": "f32",
         "dtype_detail": "fp32 master weights, gradients, state and AdamW arithmetic; Newton-Schulz GEMMs take fp16 "
                         "operands with fp32 accumulation on the tensor cores; bf16 model writeback",
         "data": "synthetic (seeded, drawn on the GPU)",
         "config": cfg,
-        "parallelism": f"replicas x{dist.world}" if dist.world > 1 else "1 GPU",
+        "parallelism": (f"sharded x{dist.world} (ZeRO-1 AdamW, one owner per Muon matrix)" if shard
+                        else f"replicas x{dist.world}" if dist.world > 1 else "1 GPU"),
         "adamw_gbs": kern_out.get("adamw", {}).get("gbs"),
         "ns_tflops_method": roofline.get("achieved") if roofline["bound"] == "tensor" else None,
         "roofline": roofline,
@@ -810,7 +853,7 @@ def adamw_buckets(params, hp, reps=5):
     return out
 
 
-def run_e2e(args, step_fn, params, flat, t, total, dist: Dist):
+def run_e2e(args, step_fn, prepare_set, params, flat, t, total, dist: Dist):
     """The same step through the public API, with main_grad arriving from
     pinned host memory and the bf16 model parameters read back to host
     memory, every step, inside the timed region.  The gradients of all
@@ -839,7 +882,7 @@ def run_e2e(args, step_fn, params, flat, t, total, dist: Dist):
     sets = [params, [mp.Param(p.main_param, g, p.exp_avg, p.exp_avg_sq, b, p.embedding_or_output, p.kind)
                      for p, g, b in zip(params, g2, b2)]]
     flats = [(flat["grad"], flat["model"]), (grad2, model2)]
-    prepared_sets = [mp.prepare(x) for x in sets]
+    prepared_sets = [prepare_set(x) for x in sets]
     compute = torch.cuda.current_stream()
     s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
     # untimed: one pass of each copy direction over every host buffer; the
@@ -917,7 +960,8 @@ def run_e2e(args, step_fn, params, flat, t, total, dist: Dist):
     d2h = b_host.numel() * b_host.element_size()
     del g_host, b_host
     arena.close()
-    return {"value": round(total * K * dist.world / (ms * 1e-3), 1), "unit": UNIT,
+    per_step = total * (1 if getattr(args, "shard", False) else dist.world)
+    return {"value": round(per_step * K / (ms * 1e-3), 1), "unit": UNIT,
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
             "steps": K, "ms_per_step": round(ms / K, 3),
             "pipelined": "main_grad and bf16 model buffers (each one contiguous buffer, one copy per direction) "

@@ -262,11 +262,14 @@ MPOPT_API opt_status opt_reload_model_params(const opt_tensor* tensors, int32_t 
  *
  *   - AdamW tensors (the routing of opt_mixed_step, with `routing` as in
  *     opt_workspace_size) are laid end to end, in list order, in one index
- *     space of N elements, which is cut into world_size contiguous ranges,
- *     ZeRO-1 style: rank r owns [rank_bounds[r], rank_bounds[r+1]).  The cuts
- *     ignore tensor boundaries (a tensor may span ranks); every inner cut is a
- *     multiple of `align_elems` (>= 1) and the ranges are as equal as that
- *     allows: rank_bounds[r] = min(N, round_up(r * N / world_size, align_elems)).
+ *     space of N elements, each starting at a multiple of `align_elems` (>= 1;
+ *     the gaps belong to no tensor), which is cut into world_size contiguous
+ *     ranges, ZeRO-1 style: rank r owns [rank_bounds[r], rank_bounds[r+1]).
+ *     The cuts ignore tensor boundaries (a tensor may span ranks); every inner
+ *     cut is a multiple of `align_elems`, so it falls at a multiple of
+ *     `align_elems` of the tensor's own elements, and the ranges are as equal
+ *     as that allows: rank_bounds[r] = min(N, round_up(r * N / world_size,
+ *     align_elems)).
  *     Rank r steps only the elements it owns, with fp32 master, m and v of
  *     that size, and then every rank receives the bf16 values of the rest.
  *   - Muon tensors stay whole (Newton-Schulz needs the whole matrix): each has

@@ -633,6 +633,9 @@ opt_status opt_shard_plan(const opt_tensor* tensors, int32_t n, int32_t routing,
     if (routes_to_muon(t, routing)) {
       if (numel > 0) muon_ids.push_back(i);
     } else {
+      // each tensor starts on an alignment boundary, so that every cut inside
+      // it falls at a multiple of align_elems of its own elements
+      N = (N + align_elems - 1) / align_elems * align_elems;
       entries[i].flat_begin = N;
       N += numel;
     }
