@@ -318,7 +318,7 @@ MPOPT_API opt_status opt_newton_schulz(const float* G, float* O, int64_t rows, i
  * and gives extensions no allocator, or a path whose memory budget is fixed in
  * advance.  No counterpart on the pages: this is an interface convenience, the
  * arithmetic is exactly opt_newton_schulz's.
- *   - Scratch is a 24 MiB array of device memory built into the library (a
+ *   - Scratch is a 20 MiB array of device memory built into the library (a
  *     static __device__ array).  Every GPU that loads the library holds it until
  *     the process exits.  This entry point calls no cudaMalloc, cudaFree or
  *     other allocating routine.

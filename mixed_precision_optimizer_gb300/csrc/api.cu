@@ -243,10 +243,10 @@ void shape_of(int64_t R, int64_t C, int64_t& A, int64_t& B, int64_t& Ap, int64_t
 }
 
 // Workspace of one group of `count` matrices with (min, max) = (A, B):
-//   X x2 [Ap][Bp] fp16 (ping-pong), A [Ap][Ap] fp32 and fp16,
-//   C [Ap][Ap] fp16, norm partials, inverse norms.
+//   X x2 [Ap][Bp] fp16 (ping-pong), A [Ap][Ap] fp16, C [Ap][Ap] fp16,
+//   norm partials, inverse norms.
 struct GroupLayout {
-  size_t xh0, xh1, af, ah, ch, partial, inv, total;
+  size_t xh0, xh1, ah, ch, partial, inv, total;
 };
 
 GroupLayout group_layout(int64_t count, int64_t R, int64_t C) {
@@ -264,7 +264,6 @@ GroupLayout group_layout(int64_t count, int64_t R, int64_t C) {
   };
   L.xh0 = take(count * ab * 2);
   L.xh1 = take(count * ab * 2);
-  L.af = take(count * aa * 4);
   L.ah = take(count * aa * 2);
   L.ch = take(count * aa * 2);
   L.partial = take(count * blocks * 4);
@@ -280,7 +279,6 @@ NsBuffers carve(uint8_t* base, int64_t count, int64_t R, int64_t C, uint32_t* st
   NsBuffers b{};
   b.Xh[0] = reinterpret_cast<uint16_t*>(base + L.xh0);
   b.Xh[1] = reinterpret_cast<uint16_t*>(base + L.xh1);
-  b.Af = reinterpret_cast<float*>(base + L.af);
   b.Ah = reinterpret_cast<uint16_t*>(base + L.ah);
   b.Ch = reinterpret_cast<uint16_t*>(base + L.ch);
   b.partial = reinterpret_cast<float*>(base + L.partial);
@@ -801,7 +799,7 @@ int32_t opt_abi_version(void) { return (2 << 16) | 0; }
 // no allocator, or a path with a fixed memory budget where an allocation would
 // fail or stall.  Its scratch is the file-scope device array below, sized for
 // one matrix with min(rows, cols) <= 1024 and max(rows, cols) <= 4096 (padded
-// Newton-Schulz buffers of 1024 x 4096 plus the 256-byte status header, 24 MiB).
+// Newton-Schulz buffers of 1024 x 4096 plus the 256-byte status header, 20 MiB).
 // The array exists on every GPU that loads this library, from module load until
 // the process exits.  In host code its name is a host-side stand-in, not a
 // device address, so each device's address is taken once with
@@ -820,7 +818,6 @@ constexpr size_t noalloc_align(size_t x) { return (x + kAlign - 1) / kAlign * kA
 // status header.
 constexpr size_t kNoallocScratchBytes =
     kHeaderBytes + 2 * noalloc_align(kNoallocMaxMin * kNoallocMaxMax * 2) +   // X x2 (ping-pong)
-    noalloc_align(kNoallocMaxMin * kNoallocMaxMin * 4) +                      // A fp32
     2 * noalloc_align(kNoallocMaxMin * kNoallocMaxMin * 2) +                  // A fp16, C fp16
     noalloc_align((kNoallocMaxMin * kNoallocMaxMax + kNormElemsPerBlock - 1) / kNormElemsPerBlock * 4) +
     noalloc_align(4);

@@ -87,8 +87,7 @@ struct MuonGroup {
 // Newton-Schulz operands are fp16 (kind::f16 tensor cores); accumulation fp32.
 struct NsBuffers {
   uint16_t* Xh[2];   // fp16 iterate            [count][Ap][Bp], ping-pong
-  float* Af;         // fp32 Gram matrix        [count][Ap][Ap]
-  uint16_t* Ah;      // fp16 Gram matrix        [count][Ap][Ap]
+  uint16_t* Ah;      // fp16 Gram matrix        [count][Ap][Ap] (operand of A A and the b A term)
   uint16_t* Ch;      // fp16 a I + b A + c A A  [count][Ap][Ap]
   float* partial;    // per-block sums of squares [count][norm_blocks]
   float* inv_norm;   // 1 / (||G||_F + eps)     [count]

@@ -5,9 +5,11 @@
 // X (A x B, A <= B), X' = a X + (b A + c A A) X with A = X X^T, is computed as
 // three GEMMs with fused epilogues, all fp16 x fp16 -> fp32 (TMEM):
 //
-//   gram : A = X X^T                        -> A fp32 on and below the diagonal blocks
-//                                              (for b A), A fp16 in full (operand)
-//   poly : C = a I + b A + c (A A)          -> C fp16
+//   gram : A = X X^T                        -> A fp16 in full (each block below the
+//                                              diagonal also stored as its mirror)
+//   poly : C = a I + b A + c (A A)          -> C fp16 (b A from the same fp16 A that
+//                                              feeds A A, so the polynomial is
+//                                              evaluated at one rounded matrix)
 //   bx   : X' = C X                         -> X' fp16 (next iterate; C X reads X
 //                                              itself as an MN-major B operand)
 //          (last iteration: W <- W (1 - lr*lambda) - lr*0.2*sqrt(max(A,B)) * X',
@@ -83,7 +85,8 @@ constexpr int kSlabBytes = kEpiWarps * kWarpScratch;
 constexpr int kOutBlockBytes = 32 * 32 * 2;    // one 32 x 32 fp16 block staged for a TMA store
 constexpr int kOutBlockBytes32 = 32 * 32 * 4;  // one 32 x 32 fp32 block
 static_assert(kSlabWords * 4 <= kWarpScratch, "transpose slab larger than a warp's scratch");
-static_assert(kOutBlockBytes32 + 2 * kOutBlockBytes <= kWarpScratch, "gram staging larger than a warp's scratch");
+static_assert(kOutBlockBytes32 + 2 * kOutBlockBytes <= kWarpScratch, "W staging larger than a warp's scratch");
+static_assert(4 * kOutBlockBytes <= kWarpScratch, "two staging buffers of a block and its mirror");
 constexpr uint32_t kSmemBytes = kStages * kStageBytes + kSlabBytes + 1024 /*align*/ + 256 /*barriers*/;
 static_assert(kSmemBytes <= 232448, "dynamic shared memory above the 227 KB a CTA may use");
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
@@ -102,8 +105,7 @@ struct GemmParams {
   int tiles_m;          // bx: Ap / BM_PAIR
   int count;
   int64_t Ap, Bp;
-  float* Af;            // gram: out; poly: in (b A term)
-  uint16_t* Ah;         // gram: out (fp16 operand of A A)
+  const uint16_t* Ah;   // poly: fp16 A, for the b A term (the gram writes it through map_out)
   uint16_t* Ch;         // poly: out
   uint16_t* Xh;         // bx: fp16 iterate out (the other buffer of the pair)
   float a, b, c;
@@ -136,9 +138,9 @@ struct FinalArgs<true> {
   MuonGroup grp;
   WMaps wm;
 };
-static_assert(4 * sizeof(CUtensorMap) + sizeof(GemmParams) + sizeof(FinalArgs<true>) + 256 <= 32764,
+static_assert(3 * sizeof(CUtensorMap) + sizeof(GemmParams) + sizeof(FinalArgs<true>) + 256 <= 32764,
               "kernel parameters above the 32 KB parameter space");
-static_assert(4 * sizeof(CUtensorMap) + sizeof(GemmParams) + sizeof(FinalArgs<false>) <= 1024,
+static_assert(3 * sizeof(CUtensorMap) + sizeof(GemmParams) + sizeof(FinalArgs<false>) <= 1024,
               "parameters of the non-final GEMM launches above 1 KB");
 
 // ------------------------------------------------------------ PTX helpers --
@@ -446,10 +448,10 @@ __device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
   return static_cast<uint32_t>(f16_bits(lo)) | (static_cast<uint32_t>(f16_bits(hi)) << 16);
 }
 
-// Staging of 32 x 32 blocks for TMA stores.  Lane t holds row t of the block
-// (columns 0..31) in v.  fp16 blocks use the 64-byte swizzle (16-byte chunk q
-// of row r at chunk q ^ ((r >> 1) & 3)), fp32 blocks the 128-byte swizzle
-// (chunk q of row r at chunk q ^ (r & 7)); the buffers are 1024-byte aligned.
+// Staging of 32 x 32 fp16 blocks for TMA stores.  Lane t holds row t of the
+// block (columns 0..31) in v.  The blocks use the 64-byte swizzle (16-byte
+// chunk q of row r at chunk q ^ ((r >> 1) & 3)); the buffers are 1024-byte
+// aligned.
 __device__ __forceinline__ void stage_f16_rows(uint8_t* buf, int lane, const float (&v)[32]) {
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
@@ -467,15 +469,6 @@ __device__ __forceinline__ void stage_f16_cols(uint8_t* buf, int lane, const flo
   for (int j = 0; j < 32; ++j) {
     const uint32_t phys = chunk ^ ((static_cast<uint32_t>(j) >> 1) & 3u);
     *reinterpret_cast<uint16_t*>(buf + j * 64 + phys * 16 + within) = f16_bits(v[j]);
-  }
-}
-
-__device__ __forceinline__ void stage_f32_rows(uint8_t* buf, int lane, const float (&v)[32]) {
-#pragma unroll
-  for (int q = 0; q < 8; ++q) {
-    const uint32_t phys = static_cast<uint32_t>(q) ^ (static_cast<uint32_t>(lane) & 7u);
-    *reinterpret_cast<float4*>(buf + lane * 128 + phys * 16) =
-        make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
   }
 }
 
@@ -555,13 +548,20 @@ __device__ __forceinline__ void epilogue_block(const GemmParams& P, const MuonGr
 
 // ------------------------------------------------------------------ kernel --
 
-// kFinal: the last C X of the iteration (mode kBxFinal), which reads the
-// group's matrices and W maps from `fa`; every other launch has kFinal false.
-template <bool kFinal>
+// Kernel variants: kNonFinal for X X^T, A A and every C X but the last;
+// kFinalTma for the last C X (mode kBxFinal) when W and its bf16 copy move
+// through TMA; kFinalPlain for the last C X otherwise (plain loads and stores
+// through a transpose slab; also the output of opt_newton_schulz).  Each
+// variant compiles only its own epilogue.  The last C X reads the group's
+// matrices and W maps from `fa`.
+enum : int { kNonFinal = 0, kFinalTma = 1, kFinalPlain = 2 };
+
+template <int kVariant>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 ns_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
-               const __grid_constant__ CUtensorMap map_out, const __grid_constant__ CUtensorMap map_out32,
-               const __grid_constant__ GemmParams P, const __grid_constant__ FinalArgs<kFinal> fa) {
+               const __grid_constant__ CUtensorMap map_out, const __grid_constant__ GemmParams P,
+               const __grid_constant__ FinalArgs<kVariant != kNonFinal> fa) {
+  constexpr bool kFinal = kVariant != kNonFinal;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* stage_a = smem;                                  // kStages x 16 KB
@@ -763,7 +763,7 @@ ns_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
     uint8_t* out_stage = scratch + (warp - 2) * kWarpScratch;
     float* slab = reinterpret_cast<float*>(out_stage);
     uint32_t out_blocks = 0;
-    const bool w_tma = kFinal && P.w_tma != 0;
+    constexpr bool w_tma = kVariant == kFinalTma;
     const uint32_t wbar = smem_u32(&wload[warp - 2]);
     uint32_t wphase = 0;
     bool wait_failed = false;
@@ -811,70 +811,73 @@ ns_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
         }
         __syncwarp();
         tmem_ld32(taddr + c0, v);
-        if (P.mode == kBx) {
-          // X' block: staged in shared memory, stored by one TMA store; two
-          // staging buffers alternate
-          uint8_t* buf = out_stage + (out_blocks & 1) * kOutBlockBytes;
-          if (out_blocks >= 2 && lane == 0) bulk_wait_read_1();   // this buffer's previous store has read it
-          __syncwarp();
-          stage_f16_rows(buf, lane, v);
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            tma_store_3d(&map_out, smem_u32(buf), t.tn * BN + c0, row0, t.mat);
-            bulk_commit();
+        if constexpr (!kFinal) {
+          if (P.mode == kBx) {
+            // X' block: staged in shared memory, stored by one TMA store; two
+            // staging buffers alternate
+            uint8_t* buf = out_stage + (out_blocks & 1) * kOutBlockBytes;
+            if (out_blocks >= 2 && lane == 0) bulk_wait_read_1();   // this buffer's previous store has read it
+            __syncwarp();
+            stage_f16_rows(buf, lane, v);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_3d(&map_out, smem_u32(buf), t.tn * BN + c0, row0, t.mat);
+              bulk_commit();
+            }
+            ++out_blocks;
+          } else if (P.mode == kGram) {
+            // A in fp16 (and the mirror block of an off-diagonal tile); two
+            // staging buffers alternate
+            const int col0 = t.tn * BN + c0;
+            uint8_t* buf = out_stage + (out_blocks & 1) * (2 * kOutBlockBytes);
+            if (out_blocks >= 2 && lane == 0) bulk_wait_read_1();   // this buffer's previous stores have read it
+            __syncwarp();
+            stage_f16_rows(buf, lane, v);
+            if (t.tm != t.tn) stage_f16_cols(buf + kOutBlockBytes, lane, v);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_3d(&map_out, smem_u32(buf), col0, row0, t.mat);
+              if (t.tm != t.tn) tma_store_3d(&map_out, smem_u32(buf + kOutBlockBytes), row0, col0, t.mat);
+              bulk_commit();
+            }
+            ++out_blocks;
+          } else if (P.mode == kPoly) {
+            // C = a I + b A + c (A A) in fp16 (and its mirror block); two
+            // staging buffers alternate
+            const int col0 = t.tn * BN + c0;
+            const int row = row0 + lane;
+            const uint16_t* Arow = P.Ah + static_cast<int64_t>(t.mat) * P.Ap * P.Ap + static_cast<int64_t>(row) * P.Ap + col0;
+  #pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const uint4 a8 = __ldcs(reinterpret_cast<const uint4*>(Arow) + q);   // 8 fp16 values
+              const uint32_t w[4] = {a8.x, a8.y, a8.z, a8.w};
+  #pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[k]));
+                v[8 * q + 2 * k + 0] = P.b * f.x + P.c * v[8 * q + 2 * k + 0];
+                v[8 * q + 2 * k + 1] = P.b * f.y + P.c * v[8 * q + 2 * k + 1];
+              }
+            }
+  #pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] += (row == col0 + j) ? P.a : 0.f;   // + a I
+            uint8_t* buf = out_stage + (out_blocks & 1) * (2 * kOutBlockBytes);
+            if (out_blocks >= 2 && lane == 0) bulk_wait_read_1();
+            __syncwarp();
+            stage_f16_rows(buf, lane, v);
+            if (t.tm != t.tn) stage_f16_cols(buf + kOutBlockBytes, lane, v);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_3d(&map_out, smem_u32(buf), col0, row0, t.mat);
+              if (t.tm != t.tn) tma_store_3d(&map_out, smem_u32(buf + kOutBlockBytes), row0, col0, t.mat);
+              bulk_commit();
+            }
+            ++out_blocks;
           }
-          ++out_blocks;
-        } else if (P.mode == kGram) {
-          // A in fp32 and fp16 (and the fp16 mirror block of an off-diagonal
-          // tile); one staging buffer: the previous block's stores have read it
-          const int col0 = t.tn * BN + c0;
-          if (out_blocks >= 1 && lane == 0) bulk_wait_read_0();
-          __syncwarp();
-          stage_f32_rows(out_stage, lane, v);
-          stage_f16_rows(out_stage + kOutBlockBytes32, lane, v);
-          if (t.tm != t.tn) stage_f16_cols(out_stage + kOutBlockBytes32 + kOutBlockBytes, lane, v);
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            tma_store_3d(&map_out32, smem_u32(out_stage), col0, row0, t.mat);
-            tma_store_3d(&map_out, smem_u32(out_stage + kOutBlockBytes32), col0, row0, t.mat);
-            if (t.tm != t.tn)
-              tma_store_3d(&map_out, smem_u32(out_stage + kOutBlockBytes32 + kOutBlockBytes), row0, col0, t.mat);
-            bulk_commit();
-          }
-          ++out_blocks;
-        } else if (P.mode == kPoly) {
-          // C = a I + b A + c (A A) in fp16 (and its mirror block); two
-          // staging buffers alternate
-          const int col0 = t.tn * BN + c0;
-          const int row = row0 + lane;
-          const float* Arow = P.Af + static_cast<int64_t>(t.mat) * P.Ap * P.Ap + static_cast<int64_t>(row) * P.Ap + col0;
-#pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            const float4 a4 = __ldcs(reinterpret_cast<const float4*>(Arow) + q);
-            v[4 * q + 0] = P.b * a4.x + P.c * v[4 * q + 0];
-            v[4 * q + 1] = P.b * a4.y + P.c * v[4 * q + 1];
-            v[4 * q + 2] = P.b * a4.z + P.c * v[4 * q + 2];
-            v[4 * q + 3] = P.b * a4.w + P.c * v[4 * q + 3];
-          }
-#pragma unroll
-          for (int j = 0; j < 32; ++j) v[j] += (row == col0 + j) ? P.a : 0.f;   // + a I
-          uint8_t* buf = out_stage + (out_blocks & 1) * (2 * kOutBlockBytes);
-          if (out_blocks >= 2 && lane == 0) bulk_wait_read_1();
-          __syncwarp();
-          stage_f16_rows(buf, lane, v);
-          if (t.tm != t.tn) stage_f16_cols(buf + kOutBlockBytes, lane, v);
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            tma_store_3d(&map_out, smem_u32(buf), col0, row0, t.mat);
-            if (t.tm != t.tn) tma_store_3d(&map_out, smem_u32(buf + kOutBlockBytes), row0, col0, t.mat);
-            bulk_commit();
-          }
-          ++out_blocks;
-        } else if constexpr (kFinal) {
-          if (w_tma) {
+        } else {
+          if constexpr (w_tma) {
             // W <- W (1 - lr wd) - lr scale X', updated in place in the staging
             // area (128-byte swizzle: 16-byte chunk q of row r at q ^ (r & 7)),
             // its bf16 copy staged 4 KB further (64-byte swizzle); both leave by
@@ -1065,22 +1068,6 @@ cudaError_t make_out_map(CUtensorMap* map, const void* base, int64_t inner, int6
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-// 3-D map over `count` row-major fp32 matrices [rows][inner] for the fp32 Gram
-// output: box 32 x 32 elements (128-byte rows), 128-byte swizzle.
-cudaError_t make_out_map32(CUtensorMap* map, const void* base, int64_t inner, int64_t rows, int64_t count) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return cudaErrorNotSupported;
-  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows),
-                              static_cast<cuuint64_t>(count)};
-  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(inner * 4), static_cast<cuuint64_t>(inner * rows * 4)};
-  const cuuint32_t box[3] = {32, 32, 1};
-  const cuuint32_t estr[3] = {1, 1, 1};
-  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides, box, estr,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
-                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
-}
-
 // 2-D map over one row-major matrix [rows][cols] of W (fp32, 128-byte swizzle)
 // or of its bf16 copy (64-byte swizzle), box 32 x 32.
 cudaError_t make_w_map(CUtensorMap* map, const void* base, int64_t cols, int64_t rows, bool bf16) {
@@ -1117,9 +1104,11 @@ cudaError_t configure_gemm() {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (configured_dev != dev) {
-    e = cudaFuncSetAttribute(ns_gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    e = cudaFuncSetAttribute(ns_gemm_kernel<kNonFinal>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(ns_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+      e = cudaFuncSetAttribute(ns_gemm_kernel<kFinalTma>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(ns_gemm_kernel<kFinalPlain>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
     configured_dev = dev;
   }
@@ -1132,12 +1121,12 @@ int gemm_grid(const GemmParams& P) {
 }
 
 // X X^T, A A and every C X but the last
-cudaError_t launch_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mo, const CUtensorMap& mo32,
-                        const GemmParams& P, cudaStream_t stream) {
+cudaError_t launch_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mo, const GemmParams& P,
+                        cudaStream_t stream) {
   cudaError_t e = configure_gemm();
   if (e != cudaSuccess) return e;
   const FinalArgs<false> none{};
-  ns_gemm_kernel<false><<<gemm_grid(P), kThreads, kSmemBytes, stream>>>(ma, mb, mo, mo32, P, none);
+  ns_gemm_kernel<kNonFinal><<<gemm_grid(P), kThreads, kSmemBytes, stream>>>(ma, mb, mo, P, none);
   return cudaGetLastError();
 }
 
@@ -1146,7 +1135,10 @@ cudaError_t launch_gemm_final(const CUtensorMap& ma, const CUtensorMap& mb, cons
                               const FinalArgs<true>& fa, cudaStream_t stream) {
   cudaError_t e = configure_gemm();
   if (e != cudaSuccess) return e;
-  ns_gemm_kernel<true><<<gemm_grid(P), kThreads, kSmemBytes, stream>>>(ma, mb, mb, mb, P, fa);
+  if (P.w_tma)
+    ns_gemm_kernel<kFinalTma><<<gemm_grid(P), kThreads, kSmemBytes, stream>>>(ma, mb, mb, P, fa);
+  else
+    ns_gemm_kernel<kFinalPlain><<<gemm_grid(P), kThreads, kSmemBytes, stream>>>(ma, mb, mb, P, fa);
   return cudaGetLastError();
 }
 
@@ -1177,19 +1169,16 @@ cudaError_t launch_ns_iteration(const MuonGroup& grp, const NsBuffers& buf, cons
     CUtensorMap ma, mb;
     if ((e = make_map(&ma, X, Bp, Ap, cnt, BM)) != cudaSuccess) return e;
     if ((e = make_map(&mb, X, Bp, Ap, cnt, BN_HALF)) != cudaSuccess) return e;
-    CUtensorMap mo, mo32;
+    CUtensorMap mo;
     if ((e = make_out_map(&mo, buf.Ah, Ap, Ap, cnt)) != cudaSuccess) return e;
-    if ((e = make_out_map32(&mo32, buf.Af, Ap, Ap, cnt)) != cudaSuccess) return e;
     GemmParams P = base;
     P.mode = kGram;
     P.k_blocks = static_cast<int>(Bp / 64);
     P.tiles_per_mat = T * (T + 1) / 2;
     P.total_tiles = P.tiles_per_mat * grp.count;
-    P.Af = buf.Af;
-    P.Ah = buf.Ah;
     P.stall = (s.stall_first_stage && it == 0) ? 1 : 0;
     prof_begin(OPT_KERNEL_NS_GRAM, grp.count, grp.A, grp.B, stream);
-    e = launch_gemm(ma, mb, mo, mo32, P, stream);
+    e = launch_gemm(ma, mb, mo, P, stream);
     prof_end(stream);
     if (e != cudaSuccess) return e;
   }
@@ -1205,10 +1194,10 @@ cudaError_t launch_ns_iteration(const MuonGroup& grp, const NsBuffers& buf, cons
     P.k_blocks = static_cast<int>(Ap / 64);
     P.tiles_per_mat = T * (T + 1) / 2;
     P.total_tiles = P.tiles_per_mat * grp.count;
-    P.Af = buf.Af;
+    P.Ah = buf.Ah;
     P.Ch = buf.Ch;
     prof_begin(OPT_KERNEL_NS_POLY, grp.count, grp.A, grp.B, stream);
-    e = launch_gemm(ma, mb, mo, mo, P, stream);   // no fp32 output
+    e = launch_gemm(ma, mb, mo, P, stream);
     prof_end(stream);
     if (e != cudaSuccess) return e;
   }
@@ -1237,7 +1226,7 @@ cudaError_t launch_ns_iteration(const MuonGroup& grp, const NsBuffers& buf, cons
     } else {
       CUtensorMap mo;
       if ((e = make_out_map(&mo, X_next, Bp, Ap, cnt)) != cudaSuccess) return e;
-      e = launch_gemm(ma, mb, mo, mo, P, stream);   // no fp32 output
+      e = launch_gemm(ma, mb, mo, P, stream);
     }
     prof_end(stream);
     if (e != cudaSuccess) return e;

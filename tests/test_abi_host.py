@@ -131,12 +131,12 @@ def test_muon_argument_errors(L):
 
 def test_workspace_size_formula(L):
     # one matrix 300 x 200: wide orientation A=200 -> 256, B=300 -> 512
-    # fp16 iterate twice (ping-pong); Gram fp32 + fp16; fp16 polynomial;
-    # norm partials of 8192 elements each; one inverse norm
+    # fp16 iterate twice (ping-pong); fp16 Gram; fp16 polynomial; norm
+    # partials of 8192 elements each; one inverse norm
     Ap, Bp = 256, 512
     al = lambda x: (x + 1023) // 1024 * 1024
     ab, aa, blocks = Ap * Bp, Ap * Ap, -(-(300 * 200) // 8192)
-    want = 256 + 2 * al(ab * 2) + al(aa * 4) + al(aa * 2) + al(aa * 2) + al(blocks * 4) + al(4)
+    want = 256 + 2 * al(ab * 2) + al(aa * 2) + al(aa * 2) + al(blocks * 4) + al(4)
     assert L.opt_workspace_size(arr(tensor(300, 200)), 1, mp.KIND_MUON) == want
     # AdamW needs none
     assert L.opt_workspace_size(arr(tensor(1, 1000, 1), tensor(30, 40)), 2, mp.KIND_ADAMW) == 0
