@@ -399,12 +399,15 @@ enum {
   OPT_KERNEL_NS_POLY = 1,      /* C = a I + b A + c A A, fp16 tensor cores       */
   OPT_KERNEL_NS_BX = 2,        /* X' = C X, fp16 tensor cores (last one updates W) */
   OPT_KERNEL_ADAMW = 3,
-  OPT_KERNEL_MUON_PREP = 4,    /* momentum, Nesterov, norm partials              */
+  OPT_KERNEL_MUON_PREP = 4,    /* momentum, Nesterov, norm partials (and, with
+                                  Newton-Schulz, the fp16 iterate)              */
   OPT_KERNEL_MUON_NORM = 5,
   OPT_KERNEL_MUON_APPLY = 6,   /* ns_steps == 0 only                             */
-  OPT_KERNEL_MUON_OPERANDS = 7, /* normalised fp16 operand copies of X0 and X0^T */
+  OPT_KERNEL_MUON_OPERANDS = 7, /* fix-up: normalised fp16 X0 rewritten for the
+                                  matrices whose iterate left fp16's range       */
   OPT_KERNEL_GRAD_NORM = 8,     /* clipping: sums of squares of the gradients      */
-  OPT_KERNEL_CLIP_FINALIZE = 9  /* clipping: total norm and factor                 */
+  OPT_KERNEL_CLIP_FINALIZE = 9, /* clipping: total norm and factor                 */
+  OPT_KERNEL_MUON_SAMPLE = 10   /* per-matrix power-of-two scale of the iterate    */
 };
 
 MPOPT_API opt_status opt_profile_launches(void* const* events, opt_launch_info* info, int32_t capacity,

@@ -82,7 +82,7 @@ EXPORTED = ("opt_workspace_size", "opt_adamw_step", "opt_muon_step", "opt_mixed_
             "opt_last_cuda_error", "opt_abi_version")
 
 KERNEL_NAMES = {0: "ns_gram", 1: "ns_poly", 2: "ns_bx", 3: "adamw", 4: "muon_momentum", 5: "muon_norm",
-                6: "muon_apply", 7: "muon_operands", 8: "grad_norm", 9: "clip_finalize"}
+                6: "muon_apply", 7: "muon_fixup", 8: "grad_norm", 9: "clip_finalize", 10: "muon_sample"}
 WORKSPACE_CLIP = 0x10
 
 

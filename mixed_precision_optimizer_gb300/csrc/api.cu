@@ -254,7 +254,7 @@ GroupLayout group_layout(int64_t count, int64_t R, int64_t C) {
   shape_of(R, C, A, B, Ap, Bp);
   const size_t ab = static_cast<size_t>(Ap) * static_cast<size_t>(Bp);
   const size_t aa = static_cast<size_t>(Ap) * static_cast<size_t>(Ap);
-  const size_t blocks = static_cast<size_t>((A * B + kNormElemsPerBlock - 1) / kNormElemsPerBlock);
+  const size_t blocks = static_cast<size_t>(partials_per_matrix(A, B, Ap, Bp));
   GroupLayout L{};
   size_t off = 0;
   auto take = [&](size_t bytes) {
@@ -267,7 +267,7 @@ GroupLayout group_layout(int64_t count, int64_t R, int64_t C) {
   L.ah = take(count * aa * 2);
   L.ch = take(count * aa * 2);
   L.partial = take(count * blocks * 4);
-  L.inv = take(count * 4);
+  L.inv = take(count * kMatStats * 4);
   L.total = off;
   return L;
 }
@@ -283,6 +283,10 @@ NsBuffers carve(uint8_t* base, int64_t count, int64_t R, int64_t C, uint32_t* st
   b.Ch = reinterpret_cast<uint16_t*>(base + L.ch);
   b.partial = reinterpret_cast<float*>(base + L.partial);
   b.inv_norm = reinterpret_cast<float*>(base + L.inv);
+  b.x_scale = b.inv_norm + count;
+  b.amax = reinterpret_cast<uint32_t*>(b.inv_norm + 2 * count);
+  b.x0_scale = b.inv_norm + 3 * count;
+  b.fix = reinterpret_cast<uint32_t*>(b.inv_norm + 4 * count);
   b.status = status;
   return b;
 }
@@ -393,20 +397,37 @@ opt_status run_muon_class(const MuonPlanHp& hp, const ShapeClass& cls, uint8_t* 
       s.ns_only = hp.ns_only;
       s.grad_scale = hp.grad_scale;
       s.stall_first_stage = (hp.stall && g0 == 0) ? 1 : 0;
-      prof_begin(OPT_KERNEL_MUON_PREP, grp.count, grp.A, grp.B, stream);
-      cudaError_t e = launch_muon_momentum(grp, buf, s, stream);
-      prof_end(stream);
-      if (e != cudaSuccess) return cuda_fail(e, "muon momentum");
-      prof_begin(OPT_KERNEL_MUON_NORM, grp.count, grp.A, grp.B, stream);
-      e = launch_muon_norm(grp, buf, s, stream);
-      prof_end(stream);
-      if (e != cudaSuccess) return cuda_fail(e, "muon norm");
       const int ns_steps = hp.no_ortho ? 0 : hp.ns_steps;
+      cudaError_t e = cudaSuccess;
       if (ns_steps > 0) {
-        prof_begin(OPT_KERNEL_MUON_OPERANDS, grp.count, grp.A, grp.B, stream);
-        e = launch_muon_operands(grp, buf, s, stream);
+        // one pass over g and m: momentum, Nesterov and the fp16 iterate,
+        // scaled by a power of two from a sample; the normalisation is applied
+        // by the first X X^T and C X epilogues (x0_scale)
+        prof_begin(OPT_KERNEL_MUON_SAMPLE, grp.count, grp.A, grp.B, stream);
+        e = launch_muon_sample(grp, buf, s, stream);
         prof_end(stream);
-        if (e != cudaSuccess) return cuda_fail(e, "muon operands");
+        if (e != cudaSuccess) return cuda_fail(e, "muon sample");
+        prof_begin(OPT_KERNEL_MUON_PREP, grp.count, grp.A, grp.B, stream);
+        e = launch_muon_prologue(grp, buf, s, stream);
+        prof_end(stream);
+        if (e != cudaSuccess) return cuda_fail(e, "muon prologue");
+        prof_begin(OPT_KERNEL_MUON_NORM, grp.count, grp.A, grp.B, stream);
+        e = launch_muon_norm(grp, buf, s, true, stream);
+        prof_end(stream);
+        if (e != cudaSuccess) return cuda_fail(e, "muon norm");
+        prof_begin(OPT_KERNEL_MUON_OPERANDS, grp.count, grp.A, grp.B, stream);
+        e = launch_muon_fixup(grp, buf, s, stream);
+        prof_end(stream);
+        if (e != cudaSuccess) return cuda_fail(e, "muon fix-up");
+      } else {
+        prof_begin(OPT_KERNEL_MUON_PREP, grp.count, grp.A, grp.B, stream);
+        e = launch_muon_momentum(grp, buf, s, stream);
+        prof_end(stream);
+        if (e != cudaSuccess) return cuda_fail(e, "muon momentum");
+        prof_begin(OPT_KERNEL_MUON_NORM, grp.count, grp.A, grp.B, stream);
+        e = launch_muon_norm(grp, buf, s, false, stream);
+        prof_end(stream);
+        if (e != cudaSuccess) return cuda_fail(e, "muon norm");
       }
       if (ns_steps == 0) {
         prof_begin(OPT_KERNEL_MUON_APPLY, grp.count, grp.A, grp.B, stream);
@@ -819,8 +840,9 @@ constexpr size_t noalloc_align(size_t x) { return (x + kAlign - 1) / kAlign * kA
 constexpr size_t kNoallocScratchBytes =
     kHeaderBytes + 2 * noalloc_align(kNoallocMaxMin * kNoallocMaxMax * 2) +   // X x2 (ping-pong)
     2 * noalloc_align(kNoallocMaxMin * kNoallocMaxMin * 2) +                  // A fp16, C fp16
-    noalloc_align((kNoallocMaxMin * kNoallocMaxMax + kNormElemsPerBlock - 1) / kNormElemsPerBlock * 4) +
-    noalloc_align(4);
+    noalloc_align(static_cast<size_t>(partials_per_matrix(kNoallocMaxMin, kNoallocMaxMax, kNoallocMaxMin,
+                                                          kNoallocMaxMax)) * 4) +
+    noalloc_align(kMatStats * 4);
 
 }  // namespace
 

@@ -89,10 +89,16 @@ struct NsBuffers {
   uint16_t* Xh[2];   // fp16 iterate            [count][Ap][Bp], ping-pong
   uint16_t* Ah;      // fp16 Gram matrix        [count][Ap][Ap] (operand of A A and the b A term)
   uint16_t* Ch;      // fp16 a I + b A + c A A  [count][Ap][Ap]
-  float* partial;    // per-block sums of squares [count][norm_blocks]
-  float* inv_norm;   // 1 / (||G||_F + eps)     [count]
+  float* partial;    // per-block sums of squares [count][max(norm blocks, prologue tiles)]
+  // per matrix, [count] each:
+  float* inv_norm;   // 1 / (||G||_F + eps)
+  float* x_scale;    // power of two: the prologue writes fp16(gtilde * x_scale) as the iterate
+  uint32_t* amax;    // bits of max |gtilde * x_scale| (non-negative floats order as integers)
+  float* x0_scale;   // 1 / (x_scale (||G||_F + eps)), or 1 after a fix-up: X0 = x0_scale * iterate
+  uint32_t* fix;     // 1: the iterate left fp16's normal range, the fix-up rewrites X0 normalised
   uint32_t* status;  // workspace header word
 };
+constexpr int kMatStats = 5;   // per-matrix words above, after the partial sums
 
 struct MuonScalars {
   float mu, one_minus_mu;
@@ -114,18 +120,40 @@ constexpr int64_t kNormElemsPerBlock = 8192;
 inline int64_t norm_blocks_per_matrix(const MuonGroup& g) {
   return (g.A * g.B + kNormElemsPerBlock - 1) / kNormElemsPerBlock;
 }
-// Elementwise pass 2 (operands): 64 x 64 tiles of the padded W-layout space.
+// Prologue of the Newton-Schulz path: 64 x 64 tiles of the padded W-layout
+// space, one partial sum of squares per tile.
 constexpr int kPrepTile = 64;
 inline int64_t operand_blocks_per_matrix(const MuonGroup& g) {
   return (g.Ap / kPrepTile) * (g.Bp / kPrepTile);
 }
+constexpr int64_t partials_per_matrix(int64_t A, int64_t B, int64_t Ap, int64_t Bp) {
+  const int64_t blocks = (A * B + kNormElemsPerBlock - 1) / kNormElemsPerBlock;
+  const int64_t tiles = (Ap / kPrepTile) * (Bp / kPrepTile);
+  return blocks > tiles ? blocks : tiles;
+}
+// Samples per matrix that set x_scale: the largest sampled |gtilde| is mapped
+// just below 2^kXScaleExp, leaving 2^(16 - kXScaleExp) of headroom below
+// fp16's largest finite value for the elements the sample missed.
+constexpr int kScaleSamples = 4096;
+constexpr int kXScaleExp = 10;
 
+// Path without Newton-Schulz (ns_steps = 0, momentum SGD): momentum pass with
+// norm partials per 8192 elements, the norm, then the update.
 cudaError_t launch_muon_momentum(const MuonGroup& grp, const NsBuffers& buf, const MuonScalars& s,
                                  cudaStream_t stream);
-cudaError_t launch_muon_norm(const MuonGroup& grp, const NsBuffers& buf, const MuonScalars& s,
-                             cudaStream_t stream);
-cudaError_t launch_muon_operands(const MuonGroup& grp, const NsBuffers& buf, const MuonScalars& s,
+// Newton-Schulz path: the sample that sets x_scale, then the prologue (momentum,
+// Nesterov, the fp16 iterate in the wide orientation, tile partial sums and
+// the max), the norm (and x0_scale / fix), and the fix-up, which rewrites X0
+// only for matrices whose iterate left fp16's normal range.
+cudaError_t launch_muon_sample(const MuonGroup& grp, const NsBuffers& buf, const MuonScalars& s,
+                               cudaStream_t stream);
+cudaError_t launch_muon_prologue(const MuonGroup& grp, const NsBuffers& buf, const MuonScalars& s,
                                  cudaStream_t stream);
+// ns_path: partials are the prologue's tiles, and x0_scale / fix are set too
+cudaError_t launch_muon_norm(const MuonGroup& grp, const NsBuffers& buf, const MuonScalars& s, bool ns_path,
+                             cudaStream_t stream);
+cudaError_t launch_muon_fixup(const MuonGroup& grp, const NsBuffers& buf, const MuonScalars& s,
+                              cudaStream_t stream);
 // ns_steps == 0: O = X0 (no tensor-core work); writes the update / output.
 cudaError_t launch_muon_apply_direct(const MuonGroup& grp, const NsBuffers& buf,
                                      const MuonScalars& s, cudaStream_t stream);

@@ -115,6 +115,8 @@ struct GemmParams {
   uint32_t* sched;      // [0]: tiles claimed after the first, [1]: CTAs finished
   int stall;            // self-test: the even CTA of pair 0 never signals its first stage
   int w_tma;            // last C X: W and its bf16 copy move through TMA, with the maps in WMaps
+  const float* in_scale;  // first iteration: per-matrix x0_scale (X0 = x0_scale * iterate); X X^T's
+                          // output is multiplied by its square and C X's by it; nullptr later
 };
 
 // Tensor maps of the last C X's update, one pair per matrix of the group
@@ -793,6 +795,12 @@ ns_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
       const Tile t = decode_tile(P, tile);
       const int row0 = t.tm * BM_PAIR + static_cast<int>(rank) * BM + quarter * 32;
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * BN;
+      // first iteration: the iterate is x_scale * gtilde; normalise here
+      float in_f = 1.f;
+      if (P.in_scale != nullptr) {
+        in_f = P.in_scale[t.mat];
+        if (!kFinal && P.mode == kGram) in_f *= in_f;
+      }
       for (int c0 = half * (BN / 2); c0 < (half + 1) * (BN / 2); c0 += 32) {
         float v[32];
         // last C X through TMA: this block of W, in W's own layout (W rows are
@@ -811,6 +819,10 @@ ns_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
         }
         __syncwarp();
         tmem_ld32(taddr + c0, v);
+        if (P.in_scale != nullptr) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] *= in_f;
+        }
         if constexpr (!kFinal) {
           if (P.mode == kBx) {
             // X' block: staged in shared memory, stored by one TMA store; two
@@ -1158,6 +1170,7 @@ cudaError_t launch_ns_iteration(const MuonGroup& grp, const NsBuffers& buf, cons
   base.ns_only = s.ns_only;
   base.status = buf.status;
   base.sched = buf.status + kSchedWord;
+  base.in_scale = nullptr;
   const int T = static_cast<int>(Ap / 256);
   cudaError_t e;
 
@@ -1177,6 +1190,7 @@ cudaError_t launch_ns_iteration(const MuonGroup& grp, const NsBuffers& buf, cons
     P.tiles_per_mat = T * (T + 1) / 2;
     P.total_tiles = P.tiles_per_mat * grp.count;
     P.stall = (s.stall_first_stage && it == 0) ? 1 : 0;
+    P.in_scale = it == 0 ? buf.x0_scale : nullptr;
     prof_begin(OPT_KERNEL_NS_GRAM, grp.count, grp.A, grp.B, stream);
     e = launch_gemm(ma, mb, mo, P, stream);
     prof_end(stream);
@@ -1215,6 +1229,7 @@ cudaError_t launch_ns_iteration(const MuonGroup& grp, const NsBuffers& buf, cons
     P.tiles_per_mat = static_cast<int>((Ap / BM_PAIR) * (Bp / BN));
     P.total_tiles = P.tiles_per_mat * grp.count;
     P.Xh = X_next;
+    P.in_scale = it == 0 ? buf.x0_scale : nullptr;
     prof_begin(OPT_KERNEL_NS_BX, grp.count, grp.A, grp.B, stream);
     if (last) {
       // the last iteration's update of W moves through TMA when every matrix allows it

@@ -222,6 +222,53 @@ def test_newton_schulz_scale_invariance(scale):
     assert rel(ns_gpu(G), want) < NS_TOL
 
 
+@pytest.mark.parametrize("case", ["outlier", "sparse_tiny", "outlier_tall", "zeros"])
+def test_newton_schulz_iterate_outside_fp16_range(case):
+    """The one-pass prologue writes fp16(gtilde * x_scale) with x_scale a power
+    of two set from a strided sample of |gtilde|.  An element far beyond the
+    sampled maximum (here 2000 times it, at a position the sample skips)
+    would overflow fp16, and a gradient whose sampled elements are all zero
+    and whose others are tiny would lose fp16 precision: such matrices take
+    the fix-up, which rewrites X0 normalised from g and m.  Either way the
+    output is the oracle's; an all-zero gradient gives zeros."""
+    rng = np.random.default_rng(41)
+    shape = (1000, 384) if case == "outlier_tall" else (384, 1000)
+    if case in ("outlier", "outlier_tall"):
+        G = rng.standard_normal(shape).astype(np.float32)
+        G.reshape(-1)[1] = 1e4            # index 1: the sample's stride is n // 4096 = 93
+    elif case == "sparse_tiny":
+        G = np.zeros(shape, np.float32)
+        idx = rng.choice(G.size, 500, replace=False)
+        idx = idx[idx % 93 != 0]            # none at a sampled position
+        G.reshape(-1)[idx] = (rng.standard_normal(idx.size) * 1e-3).astype(np.float32)
+    else:
+        G = np.zeros(shape, np.float32)
+    got = ns_gpu(G)
+    if case == "zeros":
+        assert np.array_equal(got, np.zeros(shape))
+        return
+    want = OM.newton_schulz(G.astype(np.float64))
+    assert rel(got, want) < NS_TOL
+
+
+def test_muon_step_fixup_keeps_momentum_single_update():
+    """A Muon step whose gradient takes the fix-up: the momentum buffer is
+    updated exactly once (the fix-up reads the new m, it does not update it
+    again) and the update matches the oracle."""
+    rng = np.random.default_rng(43)
+    shape = (256, 640)
+    W = (rng.standard_normal(shape) * 0.02).astype(np.float32)
+    m = (rng.standard_normal(shape) * 1e-2).astype(np.float32)
+    g = (rng.standard_normal(shape) * 1e-2).astype(np.float32)
+    g.reshape(-1)[5] = 1e3                  # 1e5 times the gradient's scale, off the sample
+    Wd, md = dev(W), dev(m)
+    p = mp.Param(Wd, dev(g), md, None, None)
+    mp.muon_step(p, mp.muon_hp(), mp.alloc_workspace(mp.workspace_size([p], "muon")))
+    Wn, mn, _ = OM.muon_step(W, g, m, lr=0.02, momentum=0.95)
+    assert np.allclose(host(md), mn, rtol=1e-5, atol=1e-9)
+    assert rel(W.astype(np.float64) - host(Wd), W.astype(np.float64) - Wn) < NS_TOL
+
+
 def test_newton_schulz_many_steps():
     rng = np.random.default_rng(32)
     G = rng.standard_normal((256, 512)).astype(np.float32)
