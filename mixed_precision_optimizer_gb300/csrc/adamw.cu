@@ -12,11 +12,11 @@
 //   p = p*(1 - lr*lambda) - lr * (mhat / (sqrt(vhat) + eps))
 //   model = bf16_rne(p)
 //
-// Work decomposition: every tensor is cut into 16K-element chunks; a
-// persistent grid of (SMs x resident CTAs) strides over the chunk list of the
-// launch and finds each chunk's tensor by binary search in the descriptor
-// table, which is passed in the kernel's parameter space (up to 400 tensors
-// per launch; longer lists take several launches).  Inside
+// Work decomposition: every tensor is cut into 16K-element chunks; the grid
+// has one CTA per chunk of the launch, and each CTA finds its chunk's tensor
+// by binary search in the descriptor table, which is passed in the kernel's
+// parameter space (up to 400 tensors per launch; longer lists take several
+// launches).  Inside
 // a chunk each warp takes 256 consecutive elements at a time: lane l the
 // float4s l and 32 + l of every array, so that each of the warp's loads of
 // p, g, m, v and streaming stores of p, m, v covers 512 contiguous bytes (two
@@ -188,20 +188,11 @@ adamw_mta_kernel(const __grid_constant__ AdamwBatch batch) {
 
 cudaError_t launch_adamw(const AdamwBatch& batch, cudaStream_t stream) {
   if (batch.n <= 0 || batch.total_chunks <= 0) return cudaSuccess;
-  static thread_local int cached_dev = -1, cached_grid = 0;
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev != cached_dev) {
-    int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, adamw_mta_kernel, kAdamwThreads, 0);
-    if (e != cudaSuccess) return e;
-    // twice the resident CTAs: the chunk loop balances the tail (measured on
-    // GB300: 8 CTAs of 256 threads per SM beat 4 by ~3 %)
-    cached_grid = num_sms() * 2 * (per_sm > 0 ? per_sm : 1);
-    cached_dev = dev;
-  }
-  const int64_t grid = batch.total_chunks < cached_grid ? batch.total_chunks : cached_grid;
+  // one CTA per chunk, launched in chunk order: the chunks in flight at any
+  // moment are one contiguous sweep of the tensors (measured on GB300 over
+  // 1.05e9 parameters: 6.94 TB/s, against 6.37 TB/s for a persistent grid of
+  // twice the resident CTAs striding over the chunks)
+  const int64_t grid = batch.total_chunks < 0x7fffffff ? batch.total_chunks : 0x7fffffff;
   adamw_mta_kernel<<<static_cast<unsigned>(grid), kAdamwThreads, 0, stream>>>(batch);
   return cudaGetLastError();
 }

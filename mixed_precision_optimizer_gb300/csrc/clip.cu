@@ -94,8 +94,8 @@ clip_finalize_kernel(const float* partials, int64_t n, float max_norm, float* sc
 
 cudaError_t launch_grad_sumsq(const NormBatch& batch, float* partials, cudaStream_t stream) {
   if (batch.n <= 0 || batch.total_chunks <= 0) return cudaSuccess;
-  const int64_t cap = static_cast<int64_t>(num_sms()) * 8;
-  const int64_t grid = batch.total_chunks < cap ? batch.total_chunks : cap;
+  // one CTA per chunk, in chunk order: a contiguous sweep of the tensors
+  const int64_t grid = batch.total_chunks < 0x7fffffff ? batch.total_chunks : 0x7fffffff;
   grad_sumsq_kernel<<<static_cast<unsigned>(grid), kThreads, 0, stream>>>(batch, partials);
   return cudaGetLastError();
 }

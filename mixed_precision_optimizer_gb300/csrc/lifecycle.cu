@@ -36,8 +36,8 @@ __global__ void __launch_bounds__(kThreads) reload_kernel(const __grid_constant_
 
 cudaError_t launch_reload(const ReloadBatch& batch, cudaStream_t stream) {
   if (batch.n <= 0 || batch.total_chunks <= 0) return cudaSuccess;
-  const int64_t cap = static_cast<int64_t>(num_sms()) * 8;
-  const int64_t grid = batch.total_chunks < cap ? batch.total_chunks : cap;
+  // one CTA per chunk, in chunk order: a contiguous sweep of the tensors
+  const int64_t grid = batch.total_chunks < 0x7fffffff ? batch.total_chunks : 0x7fffffff;
   reload_kernel<<<static_cast<unsigned>(grid), kThreads, 0, stream>>>(batch);
   return cudaGetLastError();
 }
