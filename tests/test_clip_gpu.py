@@ -94,6 +94,30 @@ def test_clipped_step_against_oracle(max_norm):
         assert np.allclose(host(t["m"]), mn, rtol=1e-5, atol=1e-10)
 
 
+def test_clipped_step_with_iterate_fixup():
+    """Clipping active and a Muon gradient whose iterate takes the fix-up (one
+    element 1e4 times the rest, where the scale sample does not look): the
+    clipping factor enters the sample, the one-pass prologue and the fix-up
+    alike, so the update is the oracle's for g * factor."""
+    rng = np.random.default_rng(8)
+    vecs, mats = _problem(rng, n_vec=2, muon_shapes=((256, 640), (640, 256)))
+    for d in mats:
+        d["g"].reshape(-1)[7] = 1e2
+    params, dvec, dmat = _device(vecs, mats)
+    ws = mp.alloc_workspace(mp.workspace_size(params, clip=True))
+    scale = torch.zeros(1, device="cuda")
+    mp.mixed_step_clipped(params, mp.muon_hp(), mp.adamw_hp(step=1, **AH), 1.0, ws, None, scale)
+    assert mp.device_status(ws) == mp.OPT_OK
+    got_scale = float(host(scale)[0])
+    assert got_scale < 0.01
+    for d, t in zip(mats, dmat):
+        gc = d["g"].astype(np.float64) * got_scale
+        Wn, mn, _ = OM.muon_step(d["W"], gc, d["m"], lr=0.02, momentum=0.95)
+        upd = d["W"].astype(np.float64) - host(t["W"]).astype(np.float64)
+        assert np.linalg.norm(upd - (d["W"] - Wn)) / np.linalg.norm(d["W"] - Wn) < 2e-2
+        assert np.allclose(host(t["m"]), mn, rtol=1e-5, atol=1e-10)
+
+
 def test_disabled_clip_equals_unclipped_step():
     rng = np.random.default_rng(5)
     outs = []

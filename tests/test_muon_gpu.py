@@ -269,6 +269,31 @@ def test_muon_step_fixup_keeps_momentum_single_update():
     assert rel(W.astype(np.float64) - host(Wd), W.astype(np.float64) - Wn) < NS_TOL
 
 
+def test_non_finite_gradient_propagates():
+    """A NaN in the gradient is not skipped ("02 · Optimizer：算法与 infra"
+    §10: bf16 training has no loss scaler): its momentum element becomes NaN,
+    the Frobenius norm is NaN, and so is every element of the update, as in
+    the oracle; the other momentum elements are unaffected and the call ends
+    normally."""
+    rng = np.random.default_rng(47)
+    shape = (192, 320)
+    W = (rng.standard_normal(shape) * 0.02).astype(np.float32)
+    m = (rng.standard_normal(shape) * 1e-2).astype(np.float32)
+    g = (rng.standard_normal(shape) * 1e-2).astype(np.float32)
+    g[3, 5] = np.nan
+    Wd, md = dev(W), dev(m)
+    p = mp.Param(Wd, dev(g), md, None, None)
+    ws = mp.alloc_workspace(mp.workspace_size([p], "muon"))
+    mp.muon_step(p, mp.muon_hp(), ws)
+    assert mp.device_status(ws) == mp.OPT_OK
+    Wn, mn, _ = OM.muon_step(W, g, m, lr=0.02, momentum=0.95)
+    assert np.isnan(Wn).all() and np.isnan(host(Wd)).all()
+    m1 = host(md)
+    assert np.isnan(m1[3, 5]) and np.isnan(mn[3, 5])
+    ok = ~np.isnan(mn)
+    assert np.isnan(m1).sum() == 1 and np.allclose(m1[ok], mn[ok], rtol=1e-5, atol=1e-9)
+
+
 def test_newton_schulz_many_steps():
     rng = np.random.default_rng(32)
     G = rng.standard_normal((256, 512)).astype(np.float32)
