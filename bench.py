@@ -234,16 +234,44 @@ def flat_views(flat, offs, shapes):
     return [flat[o:o + int(math.prod(sh))].view(sh) for o, sh in zip(offs, shapes)]
 
 
+def step_groups(w: S.Workload):
+    """The tensors in the groups the library steps them in: one group per Muon
+    shape class (smallest first), then the AdamW tensors.  [(kind, indices)]."""
+    classes, adamw = {}, []
+    for i, sp in enumerate(w.tensors):
+        if is_muon(w, sp):
+            classes.setdefault(tuple(sorted(sp.shape)), []).append(i)
+        else:
+            adamw.append(i)
+    out = [("muon", ids) for ids in sorted(classes.values(), key=lambda ids: sum(w.tensors[i].numel for i in ids))]
+    if adamw:
+        out.append(("adamw", adamw))
+    return out
+
+
 def build_device_workload(w: S.Workload, device):
     """Parameters, optimizer state and gradients of the workload on the
     device.  As in a mixed-precision trainer, every main_grad is a view of one
     contiguous fp32 gradient buffer and every bf16 model copy a view of one
     contiguous bf16 buffer (same element offsets), so the e2e leg moves each
-    direction's data with one copy."""
+    direction's data with one copy per step group.  The buffers hold the
+    tensors group by group (step_groups), so each group is one contiguous
+    segment."""
     import torch
     import mixed_precision_optimizer_gb300 as mp
     shapes = [spec.shape for spec in w.tensors]
-    offs, n_flat = flat_layout(spec.numel for spec in w.tensors)
+    groups = step_groups(w)
+    order = [i for _, ids in groups for i in ids]
+    offs_in_order, n_flat = flat_layout(w.tensors[i].numel for i in order)
+    offs = [0] * len(w.tensors)
+    for i, o in zip(order, offs_in_order):
+        offs[i] = o
+    segments, pos = [], 0
+    for kind, ids in groups:
+        start = offs_in_order[pos]
+        pos += len(ids)
+        end = offs_in_order[pos] if pos < len(order) else n_flat
+        segments.append((kind, ids, start, end))
     grad_flat = torch.empty(n_flat, dtype=torch.float32, device=device)
     model_flat = torch.empty(n_flat, dtype=torch.bfloat16, device=device)
     grads, models = flat_views(grad_flat, offs, shapes), flat_views(model_flat, offs, shapes)
@@ -264,7 +292,7 @@ def build_device_workload(w: S.Workload, device):
             n_muon += spec.numel
         else:
             n_adamw += spec.numel
-    flat = {"offsets": offs, "shapes": shapes, "grad": grad_flat, "model": model_flat}
+    flat = {"offsets": offs, "shapes": shapes, "grad": grad_flat, "model": model_flat, "segments": segments}
     return params, n_muon, n_adamw, flat
 
 
@@ -565,6 +593,15 @@ def run_ours(args, dist: Dist):
             else:
                 mp.mixed_step(plist, hm, ha(t), ws)
 
+    def group_step(t, plist, kind):
+        """One step group through the public API (the e2e leg without clipping
+        or sharding): opt_adamw_step for the AdamW tensors, opt_mixed_step for
+        a Muon shape class."""
+        if kind == "adamw":
+            mp.adamw_step(plist, ha(t))
+        else:
+            mp.mixed_step(plist, hm, None, ws)
+
     stream = torch.cuda.current_stream()
     t = 1
     for _ in range(args.warmup):
@@ -606,7 +643,8 @@ def run_ours(args, dist: Dist):
                                "max": round(max(host_ms), 3), "launches_per_step": launches // args.steps}
 
     # ---- end to end through the public API with host buffers
-    line["e2e"] = run_e2e(args, step, prepare_set, params, flat, t, total, dist)
+    grouped = None if (args.shard or args.clip > 0) else group_step
+    line["e2e"] = run_e2e(args, step, prepare_set, params, flat, t, total, dist, grouped)
     t += args.e2e_steps
     line["clocks"] = clocks.summary()
     if args.compare_cublas and dist.rank == 0:
@@ -617,7 +655,7 @@ def run_ours(args, dist: Dist):
 
     # ---- AdamW GB/s by size decade: the 10,000-tensor sweep, on the device
     # once this workload's buffers are released
-    del step, params, flat, prepared, ws
+    del step, group_step, grouped, params, flat, prepared, ws
     import gc
     gc.collect()
     torch.cuda.empty_cache()
@@ -853,17 +891,22 @@ def adamw_buckets(params, hp, reps=5):
     return out
 
 
-def run_e2e(args, step_fn, prepare_set, params, flat, t, total, dist: Dist):
+def run_e2e(args, step_fn, prepare_set, params, flat, t, total, dist: Dist, group_step=None):
     """The same step through the public API, with main_grad arriving from
     pinned host memory and the bf16 model parameters read back to host
-    memory, every step, inside the timed region.  The gradients of all
-    tensors form one contiguous buffer, and so do the bf16 model copies
-    (build_device_workload), so each direction is one copy per step.  The
-    copies are pipelined with the compute: both buffers are double-buffered on
-    the device, step k uses buffer set k % 2, its gradients are copied in on a
-    host-to-device stream while step k-1 computes, and its model copy is read
-    back on a device-to-host stream while step k+1 computes; events order
-    every reuse of a buffer set."""
+    memory, every step, inside the timed region.
+
+    The gradients of all tensors form one contiguous buffer, and so do the
+    bf16 model copies, laid out group by group (build_device_workload).  With
+    `group_step` each step is one library call per step group (a Muon shape
+    class, or the AdamW tensors), and each group's gradients are one
+    host-to-device copy and its model copies one device-to-host copy: a
+    group's compute starts as soon as its own gradients have landed, and its
+    model copy leaves while the next group computes.  Without it (sharded or
+    clipped steps, whose calls span every tensor) a step is one call and each
+    direction one copy.  The copies are pipelined across steps too: both
+    buffers are double-buffered on the device, step k uses set k % 2, and
+    events order every reuse of a buffer set."""
     import torch
     import mixed_precision_optimizer_gb300 as mp
     if args.e2e_steps <= 0:
@@ -882,7 +925,16 @@ def run_e2e(args, step_fn, prepare_set, params, flat, t, total, dist: Dist):
     sets = [params, [mp.Param(p.main_param, g, p.exp_avg, p.exp_avg_sq, b, p.embedding_or_output, p.kind)
                      for p, g, b in zip(params, g2, b2)]]
     flats = [(flat["grad"], flat["model"]), (grad2, model2)]
-    prepared_sets = [prepare_set(x) for x in sets]
+    # step groups: (calls per set, flat segment); one group = the whole step
+    if group_step is not None:
+        groups = []
+        for kind, ids, a, b in flat["segments"]:
+            preps = [mp.prepare([st[i] for i in ids], "adamw" if kind == "adamw" else None) for st in sets]
+            groups.append((lambda tt, si, preps=preps, kind=kind: group_step(tt, preps[si], kind), a, b))
+    else:
+        preps = [prepare_set(x) for x in sets]
+        groups = [(lambda tt, si: step_fn(tt, preps[si]), 0, n_flat)]
+    G = len(groups)
     compute = torch.cuda.current_stream()
     s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
     # untimed: one pass of each copy direction over every host buffer; the
@@ -905,9 +957,9 @@ def run_e2e(args, step_fn, prepare_set, params, flat, t, total, dist: Dist):
             b_host.copy_(bd, non_blocking=True)
             if i == 0:
                 warm[3].record(s_out)
-    h2d_begin, h2d_done = [E() for _ in range(K)], [E() for _ in range(K)]
-    step_begin, step_done = [E() for _ in range(K)], [E() for _ in range(K)]
-    d2h_begin, d2h_done = [E() for _ in range(K)], [E() for _ in range(K)]
+    ev = lambda: [[E() for _ in range(G)] for _ in range(K)]
+    h2d_begin, h2d_done, step_done, d2h_begin, d2h_done = ev(), ev(), ev(), ev(), ev()
+    step_begin = [E() for _ in range(K)]
     start = E()
     torch.cuda.synchronize()
     idle_gbs = {"h2d": round(g_host.numel() * g_host.element_size() / (warm[0].elapsed_time(warm[1]) * 1e6), 1),
@@ -923,50 +975,59 @@ def run_e2e(args, step_fn, prepare_set, params, flat, t, total, dist: Dist):
     for k in range(K):
         h0 = time.perf_counter()
         gd, bd = flats[k % 2]
-        with torch.cuda.stream(s_in):                  # gradients of step k
-            if k >= 2:
-                s_in.wait_event(step_done[k - 2])     # step k-2 finished reading this set
-            h2d_begin[k].record(s_in)
-            gd.copy_(g_host, non_blocking=True)
-            h2d_done[k].record(s_in)
+        with torch.cuda.stream(s_in):                  # gradients of step k, group by group
+            for g, (_, a, b) in enumerate(groups):
+                if k >= 2:
+                    s_in.wait_event(step_done[k - 2][g])   # step k-2 finished reading this segment
+                h2d_begin[k][g].record(s_in)
+                gd[a:b].copy_(g_host[a:b], non_blocking=True)
+                h2d_done[k][g].record(s_in)
         h1 = time.perf_counter()
-        compute.wait_event(h2d_done[k])
-        if k >= 2:
-            compute.wait_event(d2h_done[k - 2])       # model copy of set k % 2 read back
-        step_begin[k].record(compute)
-        step_fn(t, prepared_sets[k % 2])
+        h_step = 0.0
+        for g, (call, a, b) in enumerate(groups):
+            compute.wait_event(h2d_done[k][g])
+            if k >= 2:
+                compute.wait_event(d2h_done[k - 2][g])   # model copy of this segment of set k % 2 read back
+            if g == 0:
+                step_begin[k].record(compute)
+            c0 = time.perf_counter()
+            call(t, k % 2)
+            h_step += time.perf_counter() - c0
+            step_done[k][g].record(compute)
+            with torch.cuda.stream(s_out):             # model parameters of this group
+                s_out.wait_event(step_done[k][g])
+                d2h_begin[k][g].record(s_out)
+                b_host[a:b].copy_(bd[a:b], non_blocking=True)
+                d2h_done[k][g].record(s_out)
         t += 1
-        step_done[k].record(compute)
-        h2 = time.perf_counter()
-        with torch.cuda.stream(s_out):                 # model parameters of step k
-            s_out.wait_event(step_done[k])
-            d2h_begin[k].record(s_out)
-            b_host.copy_(bd, non_blocking=True)
-            d2h_done[k].record(s_out)
         h3 = time.perf_counter()
         host_ms[0] += (h1 - h0) * 1e3
-        host_ms[1] += (h2 - h1) * 1e3
-        host_ms[2] += (h3 - h2) * 1e3
+        host_ms[1] += h_step * 1e3
+        host_ms[2] += ((h3 - h1) - h_step) * 1e3
     torch.cuda.synchronize()
     wall_ms = (time.perf_counter() - t_wall) * 1e3
     clocks.__exit__(None, None, None)
     dist.barrier()
-    ms = dist.max(start.elapsed_time(d2h_done[-1]))
-    # device time of each phase (begin event to done event on its own stream)
-    phase = {name: round(sum(b.elapsed_time(d) for b, d in zip(bs, ds)) / K, 3)
-             for name, bs, ds in (("h2d", h2d_begin, h2d_done), ("step", step_begin, step_done),
-                                  ("d2h", d2h_begin, d2h_done))}
-    h2d = g_host.numel() * g_host.element_size()
-    d2h = b_host.numel() * b_host.element_size()
+    ms = dist.max(start.elapsed_time(d2h_done[-1][-1]))
+    # device time of each phase per step: copies summed over the groups; the
+    # step from its first group's start to its last group's end
+    phase = {"h2d": round(sum(h2d_begin[k][g].elapsed_time(h2d_done[k][g]) for k in range(K) for g in range(G)) / K, 3),
+             "step": round(sum(step_begin[k].elapsed_time(step_done[k][-1]) for k in range(K)) / K, 3),
+             "d2h": round(sum(d2h_begin[k][g].elapsed_time(d2h_done[k][g]) for k in range(K) for g in range(G)) / K, 3)}
+    h2d = sum((b - a) for _, a, b in groups) * g_host.element_size()
+    d2h = sum((b - a) for _, a, b in groups) * b_host.element_size()
     del g_host, b_host
     arena.close()
     per_step = total * (1 if getattr(args, "shard", False) else dist.world)
     return {"value": round(per_step * K / (ms * 1e-3), 1), "unit": UNIT,
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
             "steps": K, "ms_per_step": round(ms / K, 3),
-            "pipelined": "main_grad and bf16 model buffers (each one contiguous buffer, one copy per direction) "
-                         "double-buffered; H2D, step and D2H on three streams; the first step's H2D and the "
-                         "last step's D2H are not overlapped and are included",
+            "calls_per_step": G,
+            "pipelined": ("one library call per step group (each Muon shape class, the AdamW tensors), each "
+                          "group's gradients one H2D copy and its bf16 model copies one D2H copy" if G > 1 else
+                          "one library call per step; main_grad and bf16 model buffers one copy per direction") +
+                         "; buffers double-buffered; H2D, compute and D2H on three streams; the first step's "
+                         "first H2D and the last step's last D2H are not overlapped and are included",
             "host_buffers": f"one cudaHostAlloc arena of {arena.nbytes} bytes (torch pinned memory); "
                             "copies warmed once before timing",
             "host_wall_ms_per_step": round(wall_ms / K, 3),

@@ -183,3 +183,27 @@ def test_measured_line_roofline_follows_from_the_kernels():
     assert r["executed_frac"] > r["frac"] and r["pages_count_frac"] > r["executed_frac"]
     a = line["roofline_adamw"]
     assert a["frac_of_nominal_8tbs"] == round(a["achieved"] / 8000.0, 4)
+
+
+def test_flat_buffers_hold_step_groups_contiguously():
+    """The e2e leg copies one segment of the flat gradient and model buffers
+    per step group: every tensor of a group lies inside its group's segment,
+    the segments tile the buffer in order, and the groups are each Muon shape
+    class (smallest first) and then the AdamW tensors."""
+    import torch
+    w = bench.S.scaled_copy(bench.S.tiny_mixed(), "groups",
+                            [(64, 96), (7,), (96, 64), (40, 40), (300,), (40, 40), (3, 5, 2)])
+    params, n_muon, n_adamw, flat = bench.build_device_workload(w, torch.device("cpu"))
+    segs = flat["segments"]
+    assert [k for k, *_ in segs] == ["muon", "muon", "adamw"]
+    assert sorted(map(tuple, (segs[0][1], segs[1][1]))) == [(0, 2), (3, 5)]
+    assert segs[0][1] == [3, 5]                           # 40 x 40 class (3200) before 64 x 96 (12288)
+    assert segs[0][2] == 0 and segs[-1][3] == flat["grad"].numel()
+    assert all(a[3] == b[2] for a, b in zip(segs, segs[1:]))
+    base = flat["grad"].data_ptr()
+    for kind, ids, a, b in segs:
+        for i in ids:
+            off = (params[i].main_grad.data_ptr() - base) // 4
+            assert a <= off and off + params[i].main_grad.numel() <= b
+            assert (params[i].model.data_ptr() - flat["model"].data_ptr()) // 2 == off
+    assert n_muon + n_adamw == w.numel
