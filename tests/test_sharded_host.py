@@ -177,7 +177,7 @@ def _rank_body(rank, world, port, q):
     dist.destroy_process_group()
 
 
-@pytest.mark.parametrize("world", [2])
+@pytest.mark.parametrize("world", [2, 3])
 def test_sharded_step_gloo_matches_unsharded_oracle(world):
     ctx = tmp.get_context("spawn")
     q = ctx.Queue()
@@ -211,6 +211,7 @@ def test_sharded_step_gloo_matches_unsharded_oracle(world):
                 off = plan.flat_begin[i] + rng[0] - bounds[r]
                 want = ref[i].main_param.numpy().reshape(-1)[rng[0]:rng[1]]
                 assert np.array_equal(master[off:off + rng[1] - rng[0]].view(np.uint32), want.view(np.uint32))
-    # both Muon and AdamW work was split across the two ranks
-    assert {plan.owner[i] for i in range(len(SPECS)) if plan.is_muon(i)} == {0, 1}
+    # both Muon and AdamW work was split across the ranks
+    n_muon = sum(plan.is_muon(i) for i in range(len(SPECS)))
+    assert len({plan.owner[i] for i in range(len(SPECS)) if plan.is_muon(i)}) == min(world, n_muon)
     assert all(plan.adamw_len(r) > 0 for r in range(world))
