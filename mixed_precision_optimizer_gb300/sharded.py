@@ -196,6 +196,8 @@ def exchange(params: Sequence[Param], plan: ShardPlan, group=None, src_ranks: Op
     for i, p in enumerate(params):
         if plan.numel[i] == 0:
             continue
+        if not p.model.is_contiguous():
+            raise ValueError("the bf16 model copies must be contiguous (a broadcast into a reshaped copy is lost)")
         raw = p.model.reshape(-1).view(torch.uint8)      # 2 bytes per element
         if plan.is_muon(i):
             works.append(dist.broadcast(raw, src=g(plan.owner[i]), group=group, async_op=True))
