@@ -311,56 +311,79 @@ def hyper(w: S.Workload):
     return hm, ha
 
 
-def gemm_flops(rec):
-    """Flops of one Newton-Schulz GEMM launch as the pages count them (dense
-    products): 2 A^2 B for X X^T and for C X, 2 A^3 for A A, so one iteration
-    is 2 (2 A^2 B + A^3), the pages' 4 m^2 n + 2 m^3."""
-    A, B, c = rec["a"], rec["b"], rec["count"]
-    return c * (2.0 * A * A * A if rec["kernel"] == "ns_poly" else 2.0 * A * A * B)
+NS_KERNELS = ("ns_gram", "ns_poly", "ns_sym", "ns_bx")
+
+
+def iteration_flops(A, B):
+    """Flops of one Newton-Schulz iteration on one matrix as the pages count
+    them (dense products): 2 (2 A^2 B + A^3), the pages' 4 m^2 n + 2 m^3."""
+    return 2.0 * (2.0 * A * A * B + A * A * A)
+
+
+def annotate_iterations(recs):
+    """Marks each C X launch with the iterations it completes: the polynomial
+    launches since the previous C X (one per iteration; grouped iterations
+    share one C X).  Records are in launch order."""
+    polys = 0
+    for r in recs:
+        if r["kernel"] == "ns_poly":
+            polys += 1
+        elif r["kernel"] == "ns_bx":
+            r["iters"] = polys
+            polys = 0
+    return recs
+
+
+def gemm_pages_flops(rec):
+    """The pages' dense count of the iterations a launch completes, all put
+    on the C X that ends them: 2 (2 A^2 B + A^3) per iteration and matrix."""
+    if rec["kernel"] != "ns_bx":
+        return 0.0
+    return rec["count"] * rec.get("iters", 1) * iteration_flops(rec["a"], rec["b"])
 
 
 def gemm_method_flops(rec):
-    """Flops of the method's own work in one launch: the symmetric products
-    X X^T and A A counted at their triangle (A^2 B and A^3), C X in full
-    (2 A^2 B), so one iteration is 3 A^2 B + A^3.  This is the roofline's
-    algorithmic count: a symmetric product needs only half its dense flops."""
+    """Flops of one launch's own products, the symmetric ones at their
+    triangle: X X^T A^2 B, A A and the products of grouped iterations A^3,
+    C X 2 A^2 B.  This is the roofline's algorithmic count.  Per-iteration
+    evaluation does 3 A^2 B + A^3 per iteration; a group of g iterations
+    does 3 A^2 B + (4 g - 3) A^3."""
     A, B, c = rec["a"], rec["b"], rec["count"]
     k = rec["kernel"]
     if k == "ns_gram":
         return c * 1.0 * A * A * B
-    if k == "ns_poly":
+    if k in ("ns_poly", "ns_sym"):
         return c * 1.0 * A * A * A
     return c * 2.0 * A * A * B
 
 
 def gemm_executed_flops(rec):
     """Flops the tensor cores actually execute: padded shapes, and only the
-    on-or-below-diagonal 256x256 blocks of the symmetric X X^T and A A."""
+    on-or-below-diagonal 256x256 blocks of the symmetric products."""
     Ap = -(-rec["a"] // 256) * 256
     Bp = -(-rec["b"] // 256) * 256
     T = Ap // 256
     c = rec["count"]
     if rec["kernel"] == "ns_gram":
         return c * T * (T + 1) * 2.0 * 128 * 256 * Bp
-    if rec["kernel"] == "ns_poly":
+    if rec["kernel"] in ("ns_poly", "ns_sym"):
         return c * T * (T + 1) * 2.0 * 128 * 256 * Ap
     return c * 2.0 * Ap * Ap * Bp
 
 
 def kernels_by_shape(recs, peak):
     """Per Newton-Schulz GEMM stage and Muon shape class (A x B, matrices per
-    launch): launches, ms per launch, TFLOP/s by the method's count (the
-    roofline's), as executed by the tensor cores, and by the pages' dense
-    count; the executed rate as a fraction of `peak`."""
+    launch): launches, ms per launch, TFLOP/s by the launch's own algorithmic
+    count (the roofline's) and as executed by the tensor cores; the executed
+    rate as a fraction of `peak`."""
     out = {}
     for r in recs:
-        if not r["kernel"].startswith("ns_"):
+        if r["kernel"] not in NS_KERNELS:
             continue
         k = out.setdefault(f"{r['kernel']} {r['a']}x{r['b']} x{r['count']}",
-                           dict(launches=0, ms=0.0, flops=0.0, method=0.0, ex=0.0))
+                           dict(launches=0, ms=0.0, method=0.0, ex=0.0))
         k["launches"] += 1
         k["ms"] += r["ms"]
-        k["flops"] += gemm_flops(r)
         k["method"] += gemm_method_flops(r)
         k["ex"] += gemm_executed_flops(r)
     res = {}
@@ -369,7 +392,6 @@ def kernels_by_shape(recs, peak):
         res[name] = {"launches": k["launches"], "ms_per_launch": round(k["ms"] / k["launches"], 4),
                      "tflops_method": round(k["method"] / sec / 1e12, 1),
                      "tflops_executed": round(k["ex"] / sec / 1e12, 1),
-                     "tflops_pages_count": round(k["flops"] / sec / 1e12, 1),
                      "executed_frac": round(k["ex"] / sec / 1e12 / peak, 3)}
     return res
 
@@ -671,12 +693,13 @@ def measured_line(args, w, recs, launches, elapsed_ms, total, dist, peaks, peak_
     """The JSON line's measured part: value, per-kernel times, the roofline of
     the dominant kernel and AdamW's bandwidth."""
     kernels = {}
+    annotate_iterations(recs)
     for r in recs:
         k = kernels.setdefault(r["kernel"], dict(launches=0, ms=0.0, flops=0.0, method=0.0, executed=0.0, elems=0))
         k["launches"] += 1
         k["ms"] += r["ms"]
-        if r["kernel"].startswith("ns_"):
-            k["flops"] += gemm_flops(r)
+        if r["kernel"] in NS_KERNELS:
+            k["flops"] += gemm_pages_flops(r)
             k["method"] += gemm_method_flops(r)
             k["executed"] += gemm_executed_flops(r)
         if r["kernel"] == "adamw":
@@ -685,16 +708,16 @@ def measured_line(args, w, recs, launches, elapsed_ms, total, dist, peaks, peak_
     kern_out = {}
     for name, k in kernels.items():
         e = dict(launches=k["launches"], ms_total=round(k["ms"], 3), share=round(k["ms"] / busy, 4))
-        if k["flops"]:
+        if k["method"]:
             sec = k["ms"] * 1e-3
             e["tflops_method"] = round(k["method"] / sec / 1e12, 1)
             e["tflops_executed"] = round(k["executed"] / sec / 1e12, 1)
-            e["tflops_pages_count"] = round(k["flops"] / sec / 1e12, 1)
         if k["elems"]:
             e["gbs"] = round(k["elems"] * ADAMW_BYTES_PER_PARAM / (k["ms"] * 1e-3) / 1e9, 1)
         kern_out[name] = e
-    # dominant kernel: the fp16 tensor-core GEMM (X X^T, A A and C X are one kernel)
-    ns = ("ns_gram", "ns_poly", "ns_bx")
+    # dominant kernel: the fp16 tensor-core GEMM (X X^T, A A, the grouped
+    # iterations' products and C X are one kernel)
+    ns = NS_KERNELS
     gemm_ms = sum(kernels.get(n, {}).get("ms", 0.0) for n in ns)
     adamw_ms = kernels.get("adamw", {}).get("ms", 0.0)
     sustained = peaks["bf16_tflops_sustained"]
@@ -709,19 +732,22 @@ def measured_line(args, w, recs, launches, elapsed_ms, total, dist, peaks, peak_
         # measured bf16 figure is the fp16 peak
         row = profile_row("ns_gemm_traffic") or {}
         pipe = profile_row("ns_gemm_tensor_pipe")
-        roofline = {"bound": "tensor", "kernel": "ns_gemm_kernel (fp16 x fp16 -> fp32: X X^T, A A, C X)",
+        roofline = {"bound": "tensor",
+                    "kernel": "ns_gemm_kernel (fp16 x fp16 -> fp32: X X^T, A A, grouped-iteration products, C X)",
                     "achieved": round(achieved, 1), "peak": sustained, "unit": "TFLOP/s",
                     "frac": round(achieved / sustained, 4), "traffic": row.get("bytes_per_launch"),
-                    "count": "method: X X^T and A A at their triangle (A^2 B, A^3), C X in full (2 A^2 B); "
-                             "3 A^2 B + A^3 per iteration and matrix",
+                    "count": "each launch's own products, symmetric ones at their triangle: X X^T A^2 B, A A and "
+                             "the grouped iterations' products A^3, C X 2 A^2 B (per iteration 3 A^2 B + A^3; "
+                             "a group of g iterations 3 A^2 B + (4 g - 3) A^3)",
                     "peak_source": f"{peak_src} bf16_tflops_sustained (of measured) x nominal fp16/bf16 ratio 1",
                     "per_launch_flops": round(me / nl), "avg_launch_ms": round(gemm_ms / nl, 4),
                     "executed_tflops": round(ex / sec / 1e12, 1),
                     "executed_frac": round(ex / sec / 1e12 / sustained, 4),
                     "executed_count": "padded to 256, every 256 x 256 block on or below the diagonal in full",
                     "pages_count_tflops": round(fl / sec / 1e12, 1),
-                    "pages_count_frac": round(fl / sec / 1e12 / sustained, 4),
-                    "pages_count": "2 (2 A^2 B + A^3) per iteration (dense products, the pages' 4 m^2 n + 2 m^3)",
+                    "pages_count": "iteration-equivalent rate: 2 (2 A^2 B + A^3) per iteration and matrix (the "
+                                   "pages' 4 m^2 n + 2 m^3, dense products) over the GEMM time; grouped iterations "
+                                   "do fewer flops, so this is not a tensor-pipe rate",
                     "burst_frac": round(achieved / peaks["bf16_tflops"], 4),
                     "traffic_source": row.get("how"),
                     "tensor_pipe_active_pct": pipe.get("pct") if pipe else None}

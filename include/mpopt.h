@@ -79,6 +79,10 @@ enum { OPT_FLAG_EMBEDDING_OR_OUTPUT = 1 };
 /* OR into opt_workspace_size's `routing` to size a workspace for
    opt_mixed_step_clipped (adds one float per 16K gradient elements). */
 enum { OPT_WORKSPACE_CLIP = 0x10 };
+/* OR into opt_workspace_size's `routing` to size the Newton-Schulz buffers of
+   every shape for grouped iterations (opt_muon_hp.flags OPT_MUON_NS_GROUPED);
+   without it only the shapes grouped by default get their two extra buffers. */
+enum { OPT_WORKSPACE_GROUPED = 0x20 };
 
 /*
  * AdamW hyper-parameters for one step ("02 · Optimizer：算法与 infra" §2, §3).
@@ -119,7 +123,20 @@ typedef struct {
  *                 OPT_SCALE_UNIT_RMS: k * sqrt(m / n) (§14.6), where
  *                 m = rows (fan_out) and n = cols (fan_in) of the parameter
  *   flags         OPT_MUON_NO_ORTHOGONALIZE: plain momentum SGD,
- *                 W <- W (1 - lr lambda) - lr * k * gtilde (§1), no Newton-Schulz
+ *                 W <- W (1 - lr lambda) - lr * k * gtilde (§1), no Newton-Schulz;
+ *                 evaluation order of the iterations (at most one of):
+ *                 OPT_MUON_NS_PER_ITERATION: every iteration as printed
+ *                 (A = X X^T, C = a I + b A + c A A, X <- C X);
+ *                 OPT_MUON_NS_GROUPED: up to three consecutive iterations
+ *                 share one X X^T and one C X.  Every C_k is a polynomial in
+ *                 the group's first Gram matrix, so A_{k+1} = C_k (A_k C_k)
+ *                 and X_{k+g} = (C_{k+g-1} ... C_k) X_k hold exactly; only
+ *                 the rounding differs.  Used for every shape whose workspace
+ *                 group has room for two more fp16 [A][A] buffers per matrix.
+ *                 Neither flag (the default): grouped for the shapes where it
+ *                 saves tensor-core work (padded max side >= 2 x padded min
+ *                 side, min side >= 1024, e.g. 4096 x 14336), per iteration
+ *                 otherwise
  *   ns_schedule   optional HOST array of ns_steps triples (a, b, c), one per
  *                 iteration in order (a coefficient schedule); NULL: ns_a..c
  */
@@ -140,7 +157,7 @@ typedef struct {
 } opt_muon_hp;
 
 enum { OPT_SCALE_SPECTRAL = 0, OPT_SCALE_SHAPE = 1, OPT_SCALE_UNIT_RMS = 2 };
-enum { OPT_MUON_NO_ORTHOGONALIZE = 1 };
+enum { OPT_MUON_NO_ORTHOGONALIZE = 1, OPT_MUON_NS_PER_ITERATION = 2, OPT_MUON_NS_GROUPED = 4 };
 
 /*
  * One parameter tensor.
@@ -183,14 +200,17 @@ typedef struct {
  * Bytes of device workspace that opt_mixed_step (and the other steps) need for
  * this tensor list: a 256-byte status header and the Newton-Schulz buffers of
  * the largest group of same-shape Muon matrices (the fp16 iterate twice, as a
- * ping-pong pair, the Gram matrix in fp32 and fp16, the fp16 polynomial
- * a I + b A + c A A, norm partials).  Shapes are padded to multiples of 256.
+ * ping-pong pair, the fp16 Gram matrix, the fp16 polynomial a I + b A + c A A,
+ * norm partials; for the shapes that take grouped iterations by default, two
+ * more fp16 [A][A] buffers).  Shapes are padded to multiples of 256.
  * AdamW needs no workspace: 0 for a list without Muon tensors.
  * `routing` selects how kinds are interpreted: OPT_KIND_AUTO as in
  * opt_mixed_step, OPT_KIND_ADAMW treats every tensor as AdamW, OPT_KIND_MUON
  * every tensor as Muon.  Returns 0 if the list is invalid.
  * A smaller workspace is accepted by the Muon path as long as one matrix of
- * each shape fits; matrices are then processed in smaller groups.
+ * each shape fits without the grouped-iteration buffers; matrices are then
+ * processed in smaller groups, and without grouped iterations when not even
+ * one matrix fits with their buffers.
  */
 MPOPT_API size_t opt_workspace_size(const opt_tensor* tensors, int32_t n, int32_t routing);
 
@@ -407,7 +427,9 @@ enum {
                                   matrices whose iterate left fp16's range       */
   OPT_KERNEL_GRAD_NORM = 8,     /* clipping: sums of squares of the gradients      */
   OPT_KERNEL_CLIP_FINALIZE = 9, /* clipping: total norm and factor                 */
-  OPT_KERNEL_MUON_SAMPLE = 10   /* per-matrix power-of-two scale of the iterate    */
+  OPT_KERNEL_MUON_SAMPLE = 10,  /* per-matrix power-of-two scale of the iterate    */
+  OPT_KERNEL_NS_SYM = 11        /* grouped iterations: product of two commuting
+                                   symmetric [A][A] matrices, fp16 tensor cores  */
 };
 
 MPOPT_API opt_status opt_profile_launches(void* const* events, opt_launch_info* info, int32_t capacity,

@@ -35,6 +35,9 @@ STATUS_NAMES = {0: "OPT_OK", 1: "OPT_ERR_INVALID_ARG", 2: "OPT_ERR_UNSUPPORTED",
 KIND_AUTO, KIND_ADAMW, KIND_MUON = 0, 1, 2
 SCALE_MODES = {"spectral": 0, "shape_scaling": 1, "unit_rms_norm": 2}
 MUON_NO_ORTHOGONALIZE = 1
+MUON_NS_PER_ITERATION = 2
+MUON_NS_GROUPED = 4
+NS_ORDERS = {"auto": 0, "per_iteration": MUON_NS_PER_ITERATION, "grouped": MUON_NS_GROUPED}
 FLAG_EMBEDDING_OR_OUTPUT = 1
 NS_COEFFS = (3.4445, -4.7750, 2.0315)
 
@@ -82,8 +85,10 @@ EXPORTED = ("opt_workspace_size", "opt_adamw_step", "opt_muon_step", "opt_mixed_
             "opt_last_cuda_error", "opt_abi_version")
 
 KERNEL_NAMES = {0: "ns_gram", 1: "ns_poly", 2: "ns_bx", 3: "adamw", 4: "muon_momentum", 5: "muon_norm",
-                6: "muon_apply", 7: "muon_fixup", 8: "grad_norm", 9: "clip_finalize", 10: "muon_sample"}
+                6: "muon_apply", 7: "muon_fixup", 8: "grad_norm", 9: "clip_finalize", 10: "muon_sample",
+                11: "ns_sym"}
 WORKSPACE_CLIP = 0x10
+WORKSPACE_GROUPED = 0x20
 
 
 class OptShardEntry(ctypes.Structure):
@@ -271,11 +276,14 @@ def adamw_hp(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01, step=
 
 
 def muon_hp(lr=0.02, momentum=0.95, weight_decay=0.0, eps=1e-7, nesterov=True, ns_steps=5,
-            coeffs=NS_COEFFS, scale_coeff=0.2, scale_mode="spectral", orthogonalize=True, schedule=None):
-    """schedule: optional list of ns_steps (a, b, c) triples, one per iteration."""
+            coeffs=NS_COEFFS, scale_coeff=0.2, scale_mode="spectral", orthogonalize=True, schedule=None,
+            ns_order="auto"):
+    """schedule: optional list of ns_steps (a, b, c) triples, one per iteration.
+    ns_order: "auto", "per_iteration" or "grouped" (opt_muon_hp.flags)."""
     a, b, c = coeffs
+    flags = (0 if orthogonalize else MUON_NO_ORTHOGONALIZE) | NS_ORDERS[ns_order]
     hp = OptMuonHP(lr, momentum, weight_decay, eps, 1 if nesterov else 0, int(ns_steps), a, b, c, scale_coeff,
-                   SCALE_MODES[scale_mode], 0 if orthogonalize else MUON_NO_ORTHOGONALIZE, None)
+                   SCALE_MODES[scale_mode], flags, None)
     if schedule is not None:
         flat = [float(x) for trip in schedule for x in trip]
         hp._schedule_buf = (ctypes.c_float * len(flat))(*flat)   # kept alive with the struct
@@ -283,10 +291,12 @@ def muon_hp(lr=0.02, momentum=0.95, weight_decay=0.0, eps=1e-7, nesterov=True, n
     return hp
 
 
-def workspace_size(params: Sequence[Param], routing="auto", clip=False) -> int:
+def workspace_size(params: Sequence[Param], routing="auto", clip=False, ns_order="auto") -> int:
+    """ns_order="grouped" sizes every Muon shape for grouped iterations."""
     r = {"auto": KIND_AUTO, "adamw": KIND_ADAMW, "muon": KIND_MUON}[routing]
     arr = _array(params)
-    return int(lib().opt_workspace_size(arr, len(params), r | (WORKSPACE_CLIP if clip else 0)))
+    r |= (WORKSPACE_CLIP if clip else 0) | (WORKSPACE_GROUPED if ns_order == "grouped" else 0)
+    return int(lib().opt_workspace_size(arr, len(params), r))
 
 
 def alloc_workspace(nbytes, device=None):

@@ -130,7 +130,9 @@ opt_status check_muon_hp(const opt_muon_hp* hp) {
   if (hp->eps < 0.f) return OPT_ERR_INVALID_ARG;
   if (hp->ns_steps < 0 || hp->ns_steps > 16) return OPT_ERR_INVALID_ARG;
   if (hp->scale_mode < OPT_SCALE_SPECTRAL || hp->scale_mode > OPT_SCALE_UNIT_RMS) return OPT_ERR_INVALID_ARG;
-  if (hp->flags & ~OPT_MUON_NO_ORTHOGONALIZE) return OPT_ERR_INVALID_ARG;
+  if (hp->flags & ~(OPT_MUON_NO_ORTHOGONALIZE | OPT_MUON_NS_PER_ITERATION | OPT_MUON_NS_GROUPED))
+    return OPT_ERR_INVALID_ARG;
+  if ((hp->flags & OPT_MUON_NS_PER_ITERATION) && (hp->flags & OPT_MUON_NS_GROUPED)) return OPT_ERR_INVALID_ARG;
   if (hp->ns_schedule)
     for (int i = 0; i < 3 * hp->ns_steps; ++i)
       if (!finite(hp->ns_schedule[i])) return OPT_ERR_INVALID_ARG;
@@ -244,12 +246,12 @@ void shape_of(int64_t R, int64_t C, int64_t& A, int64_t& B, int64_t& Ap, int64_t
 
 // Workspace of one group of `count` matrices with (min, max) = (A, B):
 //   X x2 [Ap][Bp] fp16 (ping-pong), A [Ap][Ap] fp16, C [Ap][Ap] fp16,
-//   norm partials, inverse norms.
+//   (grouped iterations) two more [Ap][Ap] fp16, norm partials, inverse norms.
 struct GroupLayout {
-  size_t xh0, xh1, ah, ch, partial, inv, total;
+  size_t xh0, xh1, ah, ch, th0, th1, partial, inv, total;
 };
 
-GroupLayout group_layout(int64_t count, int64_t R, int64_t C) {
+GroupLayout group_layout(int64_t count, int64_t R, int64_t C, bool grouped) {
   int64_t A, B, Ap, Bp;
   shape_of(R, C, A, B, Ap, Bp);
   const size_t ab = static_cast<size_t>(Ap) * static_cast<size_t>(Bp);
@@ -266,21 +268,34 @@ GroupLayout group_layout(int64_t count, int64_t R, int64_t C) {
   L.xh1 = take(count * ab * 2);
   L.ah = take(count * aa * 2);
   L.ch = take(count * aa * 2);
+  L.th0 = grouped ? take(count * aa * 2) : 0;
+  L.th1 = grouped ? take(count * aa * 2) : 0;
   L.partial = take(count * blocks * 4);
   L.inv = take(count * kMatStats * 4);
   L.total = off;
   return L;
 }
 
-size_t group_bytes(int64_t count, int64_t R, int64_t C) { return group_layout(count, R, C).total; }
+size_t group_bytes(int64_t count, int64_t R, int64_t C, bool grouped) {
+  return group_layout(count, R, C, grouped).total;
+}
 
-NsBuffers carve(uint8_t* base, int64_t count, int64_t R, int64_t C, uint32_t* status) {
-  const GroupLayout L = group_layout(count, R, C);
+// Whether a shape class takes grouped iterations by default (ns_grouping_pays).
+bool class_grouped_by_default(int64_t A, int64_t B) {
+  int64_t a, b, Ap, Bp;
+  shape_of(A, B, a, b, Ap, Bp);
+  return ns_grouping_pays(Ap, Bp);
+}
+
+NsBuffers carve(uint8_t* base, int64_t count, int64_t R, int64_t C, bool grouped, uint32_t* status) {
+  const GroupLayout L = group_layout(count, R, C, grouped);
   NsBuffers b{};
   b.Xh[0] = reinterpret_cast<uint16_t*>(base + L.xh0);
   b.Xh[1] = reinterpret_cast<uint16_t*>(base + L.xh1);
   b.Ah = reinterpret_cast<uint16_t*>(base + L.ah);
   b.Ch = reinterpret_cast<uint16_t*>(base + L.ch);
+  b.Th[0] = grouped ? reinterpret_cast<uint16_t*>(base + L.th0) : nullptr;
+  b.Th[1] = grouped ? reinterpret_cast<uint16_t*>(base + L.th1) : nullptr;
   b.partial = reinterpret_cast<float*>(base + L.partial);
   b.inv_norm = reinterpret_cast<float*>(base + L.inv);
   b.x_scale = b.inv_norm + count;
@@ -311,12 +326,14 @@ std::vector<ShapeClass> shape_classes(const std::vector<const opt_tensor*>& mats
   return out;
 }
 
-// Workspace for the Muon part with full groups (up to kMaxGroup matrices).
-size_t muon_bytes(const std::vector<ShapeClass>& classes) {
+// Workspace for the Muon part with full groups (up to kMaxGroup matrices),
+// with the buffers of grouped iterations for the classes that take them by
+// default (for every class with `all_grouped`).
+size_t muon_bytes(const std::vector<ShapeClass>& classes, bool all_grouped) {
   size_t need = 0;
   for (const ShapeClass& c : classes) {
     const int64_t cnt = static_cast<int64_t>(c.mats.size()) < kMaxGroup ? c.mats.size() : kMaxGroup;
-    const size_t b = group_bytes(cnt, c.A, c.B);
+    const size_t b = group_bytes(cnt, c.A, c.B, all_grouped || class_grouped_by_default(c.A, c.B));
     if (b > need) need = b;
   }
   return need;
@@ -330,6 +347,8 @@ struct MuonPlanHp {
   int no_ortho;              // plain momentum SGD
   const float* schedule;     // host (a, b, c) per iteration, or nullptr: (a, b, c) every time
   int stall;                 // self-test of the bounded waits (opt_selftest_wait_timeout)
+  int ns_order;              // 0: grouped iterations where they pay; OPT_MUON_NS_PER_ITERATION or
+                             // OPT_MUON_NS_GROUPED (every shape, when the workspace has room)
 };
 
 // lr * update scale for a parameter of shape R x C ("02 · Optimizer：算法与
@@ -350,9 +369,16 @@ float step_scale_of(const MuonPlanHp& hp, int64_t R, int64_t C) {
 // cols equal to (R, C) or (C, R) -- both orientations share a class.
 opt_status run_muon_class(const MuonPlanHp& hp, const ShapeClass& cls, uint8_t* region, size_t region_bytes,
                           uint32_t* status, cudaStream_t stream, float* const* outputs /*ns_only*/) {
-  // largest group that fits the region
-  int64_t cap = static_cast<int64_t>(cls.mats.size()) < kMaxGroup ? cls.mats.size() : kMaxGroup;
-  while (cap > 0 && group_bytes(cap, cls.A, cls.B) > region_bytes) --cap;
+  // grouped iterations (launch_ns_group) when asked for or when they pay and
+  // the region holds their two extra buffers for at least one matrix; then
+  // the largest group of matrices that fits the region
+  const int ns_steps = hp.no_ortho ? 0 : hp.ns_steps;
+  const int64_t want = static_cast<int64_t>(cls.mats.size()) < kMaxGroup ? cls.mats.size() : kMaxGroup;
+  bool grouped = ns_steps >= 2 && hp.ns_order != OPT_MUON_NS_PER_ITERATION &&
+                 (hp.ns_order == OPT_MUON_NS_GROUPED || class_grouped_by_default(cls.A, cls.B)) &&
+                 group_bytes(1, cls.A, cls.B, true) <= region_bytes;
+  int64_t cap = want;
+  while (cap > 0 && group_bytes(cap, cls.A, cls.B, grouped) > region_bytes) --cap;
   if (cap == 0) return OPT_ERR_WORKSPACE;
   // matrices of both orientations share a group (the orientation is per matrix)
   for (size_t g0 = 0; g0 < cls.mats.size(); g0 += static_cast<size_t>(cap)) {
@@ -380,7 +406,7 @@ opt_status run_muon_class(const MuonPlanHp& hp, const ShapeClass& cls, uint8_t* 
         const int64_t sc = t->scale_cols > 0 ? t->scale_cols : t->cols;
         M.step_scale = step_scale_of(hp, sr, sc);
       }
-      const NsBuffers buf = carve(region, static_cast<int64_t>(gn), cls.A, cls.B, status);
+      const NsBuffers buf = carve(region, static_cast<int64_t>(gn), cls.A, cls.B, grouped, status);
       MuonScalars s{};
       s.mu = hp.mu;
       s.one_minus_mu = static_cast<float>(1.0 - static_cast<double>(hp.mu));
@@ -397,7 +423,6 @@ opt_status run_muon_class(const MuonPlanHp& hp, const ShapeClass& cls, uint8_t* 
       s.ns_only = hp.ns_only;
       s.grad_scale = hp.grad_scale;
       s.stall_first_stage = (hp.stall && g0 == 0) ? 1 : 0;
-      const int ns_steps = hp.no_ortho ? 0 : hp.ns_steps;
       cudaError_t e = cudaSuccess;
       if (ns_steps > 0) {
         // one pass over g and m: momentum, Nesterov and the fp16 iterate,
@@ -435,9 +460,11 @@ opt_status run_muon_class(const MuonPlanHp& hp, const ShapeClass& cls, uint8_t* 
         prof_end(stream);
         if (e != cudaSuccess) return cuda_fail(e, "muon apply");
       }
-      for (int it = 0; it < ns_steps; ++it) {
-        e = launch_ns_iteration(grp, buf, s, it, stream);
+      int it = 0, gi = 0;
+      for (const int g : ns_group_sizes(ns_steps, grouped)) {
+        e = launch_ns_group(grp, buf, s, it, g, gi++, stream);
         if (e != cudaSuccess) return cuda_fail(e, "newton-schulz gemm");
+        it += g;
       }
     }
   }
@@ -471,14 +498,14 @@ opt_status split_tensors(const opt_tensor* tensors, int32_t n, int32_t routing, 
 }
 
 // AdamW needs no workspace; Muon needs the status header and the group buffers.
-size_t total_bytes(const std::vector<ShapeClass>& classes) {
-  return classes.empty() ? 0 : kHeaderBytes + muon_bytes(classes);
+size_t total_bytes(const std::vector<ShapeClass>& classes, bool all_grouped) {
+  return classes.empty() ? 0 : kHeaderBytes + muon_bytes(classes, all_grouped);
 }
 
 // Minimum workspace: one matrix per Muon group.
 size_t min_bytes(const std::vector<ShapeClass>& classes) {
   size_t m = 0;
-  for (const ShapeClass& c : classes) m = std::max(m, group_bytes(1, c.A, c.B));
+  for (const ShapeClass& c : classes) m = std::max(m, group_bytes(1, c.A, c.B, false));
   return classes.empty() ? 0 : kHeaderBytes + m;
 }
 
@@ -580,6 +607,7 @@ opt_status mixed_impl(const opt_muon_hp* hpm, const opt_adamw_hp* hpa, const opt
                   hpm->ns_a,       hpm->ns_b,               hpm->ns_c,         hpm->scale_coeff,
                   hpm->nesterov ? 1 : 0, hpm->ns_steps, 0,  grad_scale,        hpm->scale_mode,
                   (hpm->flags & OPT_MUON_NO_ORTHOGONALIZE) ? 1 : 0,          hpm->ns_schedule};
+    hp.ns_order = hpm->flags & (OPT_MUON_NS_PER_ITERATION | OPT_MUON_NS_GROUPED);
     for (const ShapeClass& c : classes) {
       if ((st = run_muon_class(hp, c, ws + off, ws_bytes - off, status, stream, nullptr)) != OPT_OK) return st;
     }
@@ -596,11 +624,12 @@ extern "C" {
 
 size_t opt_workspace_size(const opt_tensor* tensors, int32_t n, int32_t routing) {
   const bool with_clip = (routing & OPT_WORKSPACE_CLIP) != 0;
-  routing &= ~OPT_WORKSPACE_CLIP;
+  const bool all_grouped = (routing & OPT_WORKSPACE_GROUPED) != 0;
+  routing &= ~(OPT_WORKSPACE_CLIP | OPT_WORKSPACE_GROUPED);
   if (routing != OPT_KIND_AUTO && routing != OPT_KIND_ADAMW && routing != OPT_KIND_MUON) return 0;
   Split sp;
   if (split_tensors(tensors, n, routing, sp) != OPT_OK) return 0;
-  const size_t base = total_bytes(shape_classes(sp.muon));
+  const size_t base = total_bytes(shape_classes(sp.muon), all_grouped);
   if (!with_clip) return base;
   return (base ? base : kHeaderBytes) + clip_bytes(sp);
 }
@@ -946,7 +975,7 @@ extern "C" opt_status opt_newton_schulz_noalloc(const float* G, float* O, int64_
   t.kind = OPT_KIND_MUON;
   std::vector<const opt_tensor*> one{&t};
   const std::vector<ShapeClass> classes = shape_classes(one);
-  if (kHeaderBytes + group_bytes(1, rows, cols) > kNoallocScratchBytes) return OPT_ERR_WORKSPACE;
+  if (kHeaderBytes + group_bytes(1, rows, cols, false) > kNoallocScratchBytes) return OPT_ERR_WORKSPACE;
   uint8_t* base = nullptr;
   opt_status st = noalloc_scratch(&base);
   if (st != OPT_OK) return st;
@@ -954,6 +983,7 @@ extern "C" opt_status opt_newton_schulz_noalloc(const float* G, float* O, int64_
   const cudaError_t e = cudaMemsetAsync(base, 0, kHeaderBytes, s);   // status word starts at zero
   if (e != cudaSuccess) return cuda_fail(e, "noalloc: status header");
   MuonPlanHp hp{0.f, 0.f, 0.f, eps, a, b, c, 0.f, 0, ns_steps, 1};
+  hp.ns_order = OPT_MUON_NS_PER_ITERATION;   // the built-in scratch holds one iteration's buffers
   float* outs[1] = {O};
   return run_muon_class(hp, classes[0], base + kHeaderBytes, kNoallocScratchBytes - kHeaderBytes,
                         reinterpret_cast<uint32_t*>(base), s, outs);

@@ -4,6 +4,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <vector>
 #include <cuda_runtime.h>
 
 namespace mpopt {
@@ -89,6 +90,7 @@ struct NsBuffers {
   uint16_t* Xh[2];   // fp16 iterate            [count][Ap][Bp], ping-pong
   uint16_t* Ah;      // fp16 Gram matrix        [count][Ap][Ap] (operand of A A and the b A term)
   uint16_t* Ch;      // fp16 a I + b A + c A A  [count][Ap][Ap]
+  uint16_t* Th[2];   // two more fp16 [count][Ap][Ap] for grouped iterations, or nullptr
   float* partial;    // per-block sums of squares [count][max(norm blocks, prologue tiles)]
   // per matrix, [count] each:
   float* inv_norm;   // 1 / (||G||_F + eps)
@@ -161,8 +163,29 @@ cudaError_t launch_muon_apply_direct(const MuonGroup& grp, const NsBuffers& buf,
 // Tensor-core GEMM stages of one Newton-Schulz iteration.
 enum NsGemmMode : int { kGram = 0, kPoly = 1, kBx = 2, kBxFinal = 3 };
 
-cudaError_t launch_ns_iteration(const MuonGroup& grp, const NsBuffers& buf, const MuonScalars& s,
-                                int iteration, cudaStream_t stream);
+// Grouped iterations.  Every C_k is a polynomial in the first Gram matrix of
+// its group, so g consecutive iterations k0 .. k0+g-1 need only one X X^T and
+// one C X: A_{k+1} = C_k (A_k C_k) and M = C_{k0+g-1} ... C_k0 are products of
+// [Ap][Ap] symmetric matrices, and X_{k0+g} = M X_k0.  Each extra iteration
+// trades one X X^T (A^2 B) and one C X (2 A^2 B) for four A^3 products, which
+// pays when B is well above A.  Groups hold at most kNsMaxGroupIters
+// iterations: the product M spans eigenvalues up to a^g, and its fp16
+// rounding grows with that range.
+constexpr int kNsMaxGroupIters = 3;
+// Sizes of the groups of ns_steps iterations, in order: all 1 when not
+// grouped, else ceil(ns_steps / 3) groups as equal as possible, the larger
+// first (5 -> 3, 2).
+std::vector<int> ns_group_sizes(int ns_steps, bool grouped);
+// By default a shape class is grouped when padded B >= 2 padded A (a merged
+// iteration then does at least a fifth less tensor-core work; 60 % less for
+// 4096 x 14336) and A >= 1024 (smaller launches are bound by latency, and a
+// group launches more of them).
+inline bool ns_grouping_pays(int64_t Ap, int64_t Bp) { return Bp >= 2 * Ap && Ap >= 1024; }
+
+// The GEMMs of iterations it0 .. it0+g-1 (g = 1: X X^T, the polynomial, C X);
+// group_index selects the iterate buffer (the groups alternate between the two).
+cudaError_t launch_ns_group(const MuonGroup& grp, const NsBuffers& buf, const MuonScalars& s, int it0, int g,
+                            int group_index, cudaStream_t stream);
 
 // Device-status codes written to the workspace header.
 enum : uint32_t {

@@ -1156,97 +1156,169 @@ cudaError_t launch_gemm_final(const CUtensorMap& ma, const CUtensorMap& mb, cons
 
 }  // namespace
 
-cudaError_t launch_ns_iteration(const MuonGroup& grp, const NsBuffers& buf, const MuonScalars& s, int it,
-                                cudaStream_t stream) {
-  const int64_t Ap = grp.Ap, Bp = grp.Bp, cnt = grp.count;
-  GemmParams base{};
-  base.count = grp.count;
-  base.Ap = Ap;
-  base.Bp = Bp;
-  base.a = s.sched[it][0];
-  base.b = s.sched[it][1];
-  base.c = s.sched[it][2];
-  base.decay = s.decay;
-  base.ns_only = s.ns_only;
-  base.status = buf.status;
-  base.sched = buf.status + kSchedWord;
-  base.in_scale = nullptr;
+namespace {
+
+// Launch parameters shared by every GEMM of a group of iterations.
+GemmParams base_params(const MuonGroup& grp, const NsBuffers& buf, const MuonScalars& s) {
+  GemmParams P{};
+  P.count = grp.count;
+  P.Ap = grp.Ap;
+  P.Bp = grp.Bp;
+  P.decay = s.decay;
+  P.ns_only = s.ns_only;
+  P.status = buf.status;
+  P.sched = buf.status + kSchedWord;
+  P.in_scale = nullptr;
+  return P;
+}
+
+// Symmetric product out = L R^T over the blocks on or below the diagonal,
+// each off-diagonal block also stored as its mirror: the Gram matrix X X^T
+// (L = R = X, K = Bp), or the product of two symmetric matrices that commute
+// (K = Ap; R^T = R, and L R is symmetric), as in the grouped iterations.
+cudaError_t launch_sym(const MuonGroup& grp, const NsBuffers& buf, const MuonScalars& s, const uint16_t* L,
+                       const uint16_t* R, int64_t K, uint16_t* out, const float* in_scale, int stall, int kernel_id,
+                       cudaStream_t stream) {
+  const int64_t Ap = grp.Ap, cnt = grp.count;
   const int T = static_cast<int>(Ap / 256);
   cudaError_t e;
+  CUtensorMap ma, mb, mo;
+  if ((e = make_map(&ma, L, K, Ap, cnt, BM)) != cudaSuccess) return e;
+  if ((e = make_map(&mb, R, K, Ap, cnt, BN_HALF)) != cudaSuccess) return e;
+  if ((e = make_out_map(&mo, out, Ap, Ap, cnt)) != cudaSuccess) return e;
+  GemmParams P = base_params(grp, buf, s);
+  P.mode = kGram;
+  P.k_blocks = static_cast<int>(K / 64);
+  P.tiles_per_mat = T * (T + 1) / 2;
+  P.total_tiles = P.tiles_per_mat * grp.count;
+  P.stall = stall;
+  P.in_scale = in_scale;
+  prof_begin(kernel_id, grp.count, grp.A, grp.B, stream);
+  e = launch_gemm(ma, mb, mo, P, stream);
+  prof_end(stream);
+  return e;
+}
 
-  uint16_t* X = buf.Xh[it & 1];           // this iteration's iterate
-  uint16_t* X_next = buf.Xh[(it + 1) & 1];
+// The quintic's polynomial C = a I + b A + c (A A), fp16 in full.
+cudaError_t launch_poly(const MuonGroup& grp, const NsBuffers& buf, const MuonScalars& s, const uint16_t* A,
+                        uint16_t* out, int it, cudaStream_t stream) {
+  const int64_t Ap = grp.Ap, cnt = grp.count;
+  const int T = static_cast<int>(Ap / 256);
+  cudaError_t e;
+  CUtensorMap ma, mb, mo;
+  if ((e = make_map(&ma, A, Ap, Ap, cnt, BM)) != cudaSuccess) return e;
+  if ((e = make_map(&mb, A, Ap, Ap, cnt, BN_HALF)) != cudaSuccess) return e;
+  if ((e = make_out_map(&mo, out, Ap, Ap, cnt)) != cudaSuccess) return e;
+  GemmParams P = base_params(grp, buf, s);
+  P.mode = kPoly;
+  P.a = s.sched[it][0];
+  P.b = s.sched[it][1];
+  P.c = s.sched[it][2];
+  P.k_blocks = static_cast<int>(Ap / 64);
+  P.tiles_per_mat = T * (T + 1) / 2;
+  P.total_tiles = P.tiles_per_mat * grp.count;
+  P.Ah = A;
+  P.Ch = out;
+  prof_begin(OPT_KERNEL_NS_POLY, grp.count, grp.A, grp.B, stream);
+  e = launch_gemm(ma, mb, mo, P, stream);
+  prof_end(stream);
+  return e;
+}
 
-  // gram: A = X X^T  (operands: fp16 X [Ap][Bp], K = Bp, both K-major)
-  {
-    CUtensorMap ma, mb;
-    if ((e = make_map(&ma, X, Bp, Ap, cnt, BM)) != cudaSuccess) return e;
-    if ((e = make_map(&mb, X, Bp, Ap, cnt, BN_HALF)) != cudaSuccess) return e;
+// X' = M X (M K-major [Ap][Ap]; X [Ap][Bp] read as an MN-major B operand, one
+// box of 64 K rows x two 64-column blocks per stage).  The last one updates W
+// (or writes the Newton-Schulz output) instead of storing X'.
+cudaError_t launch_bx(const MuonGroup& grp, const NsBuffers& buf, const MuonScalars& s, const uint16_t* M,
+                      const uint16_t* X, uint16_t* X_next, bool last, const float* in_scale, cudaStream_t stream) {
+  const int64_t Ap = grp.Ap, Bp = grp.Bp, cnt = grp.count;
+  cudaError_t e;
+  CUtensorMap ma, mb;
+  if ((e = make_map(&ma, M, Ap, Ap, cnt, BM)) != cudaSuccess) return e;
+  if ((e = make_map_mn(&mb, X, Bp, Ap, cnt)) != cudaSuccess) return e;
+  GemmParams P = base_params(grp, buf, s);
+  P.mode = last ? kBxFinal : kBx;
+  P.k_blocks = static_cast<int>(Ap / 64);
+  P.tiles_m = static_cast<int>(Ap / BM_PAIR);
+  P.tiles_per_mat = static_cast<int>((Ap / BM_PAIR) * (Bp / BN));
+  P.total_tiles = P.tiles_per_mat * grp.count;
+  P.Xh = X_next;
+  P.in_scale = in_scale;
+  prof_begin(OPT_KERNEL_NS_BX, grp.count, grp.A, grp.B, stream);
+  if (last) {
+    // the last iteration's update of W moves through TMA when every matrix allows it
+    static thread_local FinalArgs<true> fa;
+    fa.grp = grp;
+    P.w_tma = (!s.ns_only && make_w_maps(grp, &fa.wm)) ? 1 : 0;
+    if (!P.w_tma) fa.wm = WMaps{};
+    e = launch_gemm_final(ma, mb, P, fa, stream);
+  } else {
     CUtensorMap mo;
-    if ((e = make_out_map(&mo, buf.Ah, Ap, Ap, cnt)) != cudaSuccess) return e;
-    GemmParams P = base;
-    P.mode = kGram;
-    P.k_blocks = static_cast<int>(Bp / 64);
-    P.tiles_per_mat = T * (T + 1) / 2;
-    P.total_tiles = P.tiles_per_mat * grp.count;
-    P.stall = (s.stall_first_stage && it == 0) ? 1 : 0;
-    P.in_scale = it == 0 ? buf.x0_scale : nullptr;
-    prof_begin(OPT_KERNEL_NS_GRAM, grp.count, grp.A, grp.B, stream);
-    e = launch_gemm(ma, mb, mo, P, stream);
-    prof_end(stream);
-    if (e != cudaSuccess) return e;
+    if ((e = make_out_map(&mo, X_next, Bp, Ap, cnt)) == cudaSuccess) e = launch_gemm(ma, mb, mo, P, stream);
   }
-  // poly: C = a I + b A + c A A  (operands: fp16 A [Ap][Ap], K = Ap)
-  {
-    CUtensorMap ma, mb;
-    if ((e = make_map(&ma, buf.Ah, Ap, Ap, cnt, BM)) != cudaSuccess) return e;
-    if ((e = make_map(&mb, buf.Ah, Ap, Ap, cnt, BN_HALF)) != cudaSuccess) return e;
-    CUtensorMap mo;
-    if ((e = make_out_map(&mo, buf.Ch, Ap, Ap, cnt)) != cudaSuccess) return e;
-    GemmParams P = base;
-    P.mode = kPoly;
-    P.k_blocks = static_cast<int>(Ap / 64);
-    P.tiles_per_mat = T * (T + 1) / 2;
-    P.total_tiles = P.tiles_per_mat * grp.count;
-    P.Ah = buf.Ah;
-    P.Ch = buf.Ch;
-    prof_begin(OPT_KERNEL_NS_POLY, grp.count, grp.A, grp.B, stream);
-    e = launch_gemm(ma, mb, mo, P, stream);
-    prof_end(stream);
-    if (e != cudaSuccess) return e;
+  prof_end(stream);
+  return e;
+}
+
+}  // namespace
+
+std::vector<int> ns_group_sizes(int ns_steps, bool grouped) {
+  std::vector<int> sizes;
+  if (!grouped) {
+    sizes.assign(static_cast<size_t>(ns_steps), 1);
+    return sizes;
   }
-  // bx: X' = C X  (operands: fp16 C [Ap][Ap] K-major, fp16 X [Ap][Bp] MN-major,
-  // one box of 64 K rows x two 64-column blocks per stage, K = Ap)
-  {
-    CUtensorMap ma, mb;
-    if ((e = make_map(&ma, buf.Ch, Ap, Ap, cnt, BM)) != cudaSuccess) return e;
-    if ((e = make_map_mn(&mb, X, Bp, Ap, cnt)) != cudaSuccess) return e;
-    const bool last = it == s.ns_steps - 1;
-    GemmParams P = base;
-    P.mode = last ? kBxFinal : kBx;
-    P.k_blocks = static_cast<int>(Ap / 64);
-    P.tiles_m = static_cast<int>(Ap / BM_PAIR);
-    P.tiles_per_mat = static_cast<int>((Ap / BM_PAIR) * (Bp / BN));
-    P.total_tiles = P.tiles_per_mat * grp.count;
-    P.Xh = X_next;
-    P.in_scale = it == 0 ? buf.x0_scale : nullptr;
-    prof_begin(OPT_KERNEL_NS_BX, grp.count, grp.A, grp.B, stream);
-    if (last) {
-      // the last iteration's update of W moves through TMA when every matrix allows it
-      static thread_local FinalArgs<true> fa;
-      fa.grp = grp;
-      P.w_tma = (!s.ns_only && make_w_maps(grp, &fa.wm)) ? 1 : 0;
-      if (!P.w_tma) fa.wm = WMaps{};
-      e = launch_gemm_final(ma, mb, P, fa, stream);
-    } else {
-      CUtensorMap mo;
-      if ((e = make_out_map(&mo, X_next, Bp, Ap, cnt)) != cudaSuccess) return e;
-      e = launch_gemm(ma, mb, mo, P, stream);
-    }
-    prof_end(stream);
-    if (e != cudaSuccess) return e;
+  const int groups = (ns_steps + kNsMaxGroupIters - 1) / kNsMaxGroupIters;
+  for (int k = 0; k < groups; ++k) sizes.push_back(ns_steps / groups + (k < ns_steps % groups ? 1 : 0));
+  return sizes;
+}
+
+cudaError_t launch_ns_group(const MuonGroup& grp, const NsBuffers& buf, const MuonScalars& s, int it0, int g,
+                            int group_index, cudaStream_t stream) {
+  const int64_t Ap = grp.Ap, Bp = grp.Bp;
+  const bool first = it0 == 0;
+  const float* in_scale = first ? buf.x0_scale : nullptr;   // X0 = x0_scale * iterate (first group only)
+  const uint16_t* X = buf.Xh[group_index & 1];
+  uint16_t* X_next = buf.Xh[(group_index + 1) & 1];
+  // [Ap][Ap] fp16 buffers: the Gram matrix, the polynomial, and (grouped
+  // iterations) two more; roles rotate so that no launch writes a buffer it reads
+  uint16_t* sq[4] = {buf.Ah, buf.Ch, buf.Th[0], buf.Th[1]};
+  auto free_slot = [](int x, int y, int z) {
+    for (int k = 0; k < 4; ++k)
+      if (k != x && k != y && k != z) return k;
+    return -1;
+  };
+  cudaError_t e;
+  int iA = 0, iC = 1, iM = 1;   // A_k, C_k and the running product M = C_k ... C_it0 (M = C_it0 at first)
+  // A_it0 = X X^T; C_it0 = a I + b A + c A A
+  if ((e = launch_sym(grp, buf, s, X, X, Bp, sq[iA], in_scale, first ? s.stall_first_stage : 0, OPT_KERNEL_NS_GRAM,
+                      stream)) != cudaSuccess)
+    return e;
+  if ((e = launch_poly(grp, buf, s, sq[iA], sq[iC], it0, stream)) != cudaSuccess) return e;
+  for (int j = 1; j < g; ++j) {
+    if (!buf.Th[0] || !buf.Th[1]) return cudaErrorInvalidValue;
+    // the next Gram matrix without the next iterate: X_{k+1} = C_k X_k, and
+    // C_k commutes with A_k, so A_{k+1} = C_k A_k C_k = C_k (A_k C_k)
+    const int iP = free_slot(iA, iC, iM);
+    if ((e = launch_sym(grp, buf, s, sq[iA], sq[iC], Ap, sq[iP], nullptr, 0, OPT_KERNEL_NS_SYM, stream)) !=
+        cudaSuccess)
+      return e;
+    if ((e = launch_sym(grp, buf, s, sq[iC], sq[iP], Ap, sq[iA], nullptr, 0, OPT_KERNEL_NS_SYM, stream)) !=
+        cudaSuccess)
+      return e;
+    // C_{k+1} from A_{k+1}, into the product's buffer (no longer read)
+    if ((e = launch_poly(grp, buf, s, sq[iA], sq[iP], it0 + j, stream)) != cudaSuccess) return e;
+    const int iC_next = iP;
+    const int iM_next = free_slot(iA, iC_next, iM);
+    // M <- C_{k+1} M (every factor a polynomial in A_it0: they commute)
+    if ((e = launch_sym(grp, buf, s, sq[iC_next], sq[iM], Ap, sq[iM_next], nullptr, 0, OPT_KERNEL_NS_SYM,
+                        stream)) != cudaSuccess)
+      return e;
+    iC = iC_next;
+    iM = iM_next;
   }
-  return cudaSuccess;
+  // X_{it0+g} = M X_it0
+  const bool last = it0 + g == s.ns_steps;
+  return launch_bx(grp, buf, s, sq[iM], X, X_next, last, in_scale, stream);
 }
 
 }  // namespace mpopt

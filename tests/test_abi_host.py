@@ -114,7 +114,7 @@ def test_muon_argument_errors(L):
     bad.scale_mode = 3
     assert L.opt_muon_step(ctypes.byref(bad), arr(tensor(8, 16)), ws, big, None) == inv
     bad = mp.muon_hp()
-    bad.flags = 4
+    bad.flags = 8                                           # not a defined flag
     assert L.opt_muon_step(ctypes.byref(bad), arr(tensor(8, 16)), ws, big, None) == inv
     sched = mp.muon_hp(ns_steps=2, schedule=[(1.0, 2.0, 3.0), (1.0, float("inf"), 3.0)])
     assert L.opt_muon_step(ctypes.byref(sched), arr(tensor(8, 16)), ws, big, None) == inv
@@ -150,9 +150,48 @@ def test_workspace_size_formula(L):
     # clipping adds the header (if absent) and one float per 16K gradient elements
     assert L.opt_workspace_size(arr(tensor(1, 1000, 1)), 1, mp.KIND_AUTO | mp.WORKSPACE_CLIP) == 256 + 1024
     assert L.opt_workspace_size(arr(tensor(300, 200)), 1, mp.KIND_AUTO | mp.WORKSPACE_CLIP) == want + 1024
+    # grouped iterations: two more fp16 [Ap][Ap] buffers, on request for any shape
+    assert L.opt_workspace_size(arr(tensor(300, 200)), 1, mp.KIND_MUON | mp.WORKSPACE_GROUPED) == want + 2 * al(aa * 2)
     # invalid list -> 0
     assert L.opt_workspace_size(arr(tensor(300, 200, ndim=3)), 1, mp.KIND_MUON) == 0
     assert L.opt_workspace_size(arr(tensor(300, 200)), 1, 9) == 0
+
+
+def test_grouped_iterations_by_default_where_they_pay(L):
+    """Shapes whose padded max side is at least twice the padded min side, with
+    a min side of 1024 or more, take grouped Newton-Schulz iterations by
+    default, and their workspace holds the two extra fp16 [Ap][Ap] buffers;
+    other shapes get them only when sized for grouping."""
+    al = lambda x: (x + 1023) // 1024 * 1024
+
+    def plain(R, C):
+        A, B = min(R, C), max(R, C)
+        Ap, Bp = -(-A // 256) * 256, -(-B // 256) * 256
+        blocks = max(-(-(A * B) // 8192), (Ap // 64) * (Bp // 64))
+        return 256 + 2 * al(Ap * Bp * 2) + 2 * al(Ap * Ap * 2) + al(blocks * 4) + al(20), al(Ap * Ap * 2)
+
+    for (R, C), grouped in (((1024, 4096), True), ((4096, 1024), True), ((1024, 2048), True),
+                            ((4096, 14336), True), ((1000, 2000), True), ((768, 2048), False),
+                            ((1024, 1024), False), ((4096, 4096), False), ((1024, 1700), False)):
+        base, aa = plain(R, C)
+        got = L.opt_workspace_size(arr(tensor(R, C)), 1, mp.KIND_MUON)
+        assert got == base + (2 * aa if grouped else 0), (R, C)
+        assert L.opt_workspace_size(arr(tensor(R, C)), 1, mp.KIND_MUON | mp.WORKSPACE_GROUPED) == base + 2 * aa
+
+
+def test_ns_order_flags(L):
+    """At most one evaluation-order flag; unknown flag bits are refused.  The
+    hyper-parameters are checked before the workspace, so an accepted flag
+    set reaches the missing-workspace error (4) and a refused one stops at 1."""
+    for flags, want in ((0, 4), (mp.MUON_NS_GROUPED, 4), (mp.MUON_NS_PER_ITERATION, 4),
+                        (mp.MUON_NS_GROUPED | mp.MUON_NS_PER_ITERATION, 1), (8, 1),
+                        (mp.MUON_NO_ORTHOGONALIZE | mp.MUON_NS_GROUPED, 4)):
+        hp = mp.muon_hp()
+        hp.flags = flags
+        assert L.opt_muon_step(ctypes.byref(hp), arr(tensor(8, 16)), None, 0, None) == want, flags
+    assert mp.muon_hp(ns_order="grouped").flags == mp.MUON_NS_GROUPED
+    assert mp.muon_hp(ns_order="per_iteration", orthogonalize=False).flags == (
+        mp.MUON_NS_PER_ITERATION | mp.MUON_NO_ORTHOGONALIZE)
 
 
 def test_clipped_step_argument_errors(L):

@@ -78,17 +78,42 @@ def test_smi_index(monkeypatch):
 
 def test_gemm_flop_accounting_matches_pages_formula():
     """One Newton-Schulz iteration's three launches add up to the pages'
-    4 m^2 n + 2 m^3 per matrix (dense count); the method's count (the
-    roofline's) takes the symmetric products at their triangle, 3 m^2 n + m^3;
-    the executed count lies between the two for large shapes."""
+    4 m^2 n + 2 m^3 per matrix (dense count, put on the C X that completes the
+    iteration); the launches' own count (the roofline's) takes the symmetric
+    products at their triangle, 3 m^2 n + m^3; the executed count lies between
+    the two for large shapes."""
     for A, B in ((1024, 4096), (4096, 14336), (256, 512)):
-        recs = [dict(kernel=k, count=3, a=A, b=B) for k in ("ns_gram", "ns_poly", "ns_bx")]
-        assert sum(bench.gemm_flops(r) for r in recs) == 3 * OM.ns_flops(A, B, 1)
+        recs = bench.annotate_iterations([dict(kernel=k, count=3, a=A, b=B) for k in ("ns_gram", "ns_poly", "ns_bx")])
+        pages = sum(bench.gemm_pages_flops(r) for r in recs)
+        assert pages == 3 * OM.ns_flops(A, B, 1)
         assert sum(bench.gemm_method_flops(r) for r in recs) == 3 * (3 * A * A * B + A ** 3)
         ex = sum(bench.gemm_executed_flops(r) for r in recs)
-        assert sum(bench.gemm_method_flops(r) for r in recs) <= ex <= sum(bench.gemm_flops(r) for r in recs)
-        # executed <= algorithmic for the symmetric stages
-        assert bench.gemm_executed_flops(recs[0]) < bench.gemm_flops(recs[0]) or A == 256
+        assert sum(bench.gemm_method_flops(r) for r in recs) <= ex <= pages
+        # executed below the dense count for the symmetric stage
+        assert bench.gemm_executed_flops(recs[0]) < 2.0 * 3 * A * A * B or A == 256
+
+
+def test_grouped_iteration_accounting():
+    """A group of g iterations is one X X^T, g polynomials, 3 (g - 1) more
+    symmetric [A][A] products and one C X: its own count is 3 A^2 B +
+    (4 g - 3) A^3 per matrix, and the pages' count of its g iterations lands on
+    the C X.  Five iterations as groups of 3 and 2 count the pages' five."""
+    A, B, n = 4096, 14336, 48
+    recs = []
+    for g in (3, 2):
+        recs.append(dict(kernel="ns_gram", count=n, a=A, b=B))
+        recs.append(dict(kernel="ns_poly", count=n, a=A, b=B))
+        for _ in range(g - 1):
+            recs += [dict(kernel="ns_sym", count=n, a=A, b=B), dict(kernel="ns_sym", count=n, a=A, b=B),
+                     dict(kernel="ns_poly", count=n, a=A, b=B), dict(kernel="ns_sym", count=n, a=A, b=B)]
+        recs.append(dict(kernel="ns_bx", count=n, a=A, b=B))
+    bench.annotate_iterations(recs)
+    assert [r["iters"] for r in recs if r["kernel"] == "ns_bx"] == [3, 2]
+    assert sum(bench.gemm_pages_flops(r) for r in recs) == n * OM.ns_flops(A, B, 5)
+    me = sum(bench.gemm_method_flops(r) for r in recs)
+    assert me == n * sum(3 * A * A * B + (4 * g - 3) * A ** 3 for g in (3, 2))
+    per_iteration = n * 5 * (3 * A * A * B + A ** 3)
+    assert 0.6 < me / per_iteration < 0.65          # 39 % fewer flops for this shape
 
 
 def _run_bench(*args):
@@ -153,16 +178,15 @@ def test_kernels_by_shape_groups_stages_and_classes():
     assert set(out) == {"ns_gram 4096x14336 x48", "ns_bx 1024x4096 x32"}
     g = out["ns_gram 4096x14336 x48"]
     assert g["launches"] == 2 and g["ms_per_launch"] == 7.4
-    # pages' count 2 A^2 B per matrix; the method's A^2 B; executed: 136 of the 256 blocks
-    assert g["tflops_pages_count"] == round(48 * 2.0 * 4096 ** 2 * 14336 / 7.4e-3 / 1e12, 1)
+    # the launch's own count A^2 B per matrix; executed: 136 of the 256 blocks
     assert g["tflops_method"] == round(48 * 1.0 * 4096 ** 2 * 14336 / 7.4e-3 / 1e12, 1)
     ex = 48 * 136 * 2.0 * 256 * 256 * 14336 / 7.4e-3 / 1e12
     assert g["tflops_executed"] == round(ex, 1) and g["executed_frac"] == round(ex / 1700.0, 3)
 
 
 def test_measured_line_roofline_follows_from_the_kernels():
-    """frac = the method's flops of the GEMM launches / their event time / the
-    sustained peak; the executed and the pages' counts beside it."""
+    """frac = the launches' own flops / their event time / the sustained peak;
+    the executed count and the pages' iteration-equivalent rate beside it."""
     class A:
         steps, clip, warmup = 2, 0.0, 1
     class D:
@@ -180,7 +204,8 @@ def test_measured_line_roofline_follows_from_the_kernels():
     ms = sum(x["ms"] for x in recs if x["kernel"] != "adamw")
     assert r["achieved"] == round(me / (ms * 1e-3) / 1e12, 1)
     assert r["frac"] == round(me / (ms * 1e-3) / 1e12 / 1708.2, 4)
-    assert r["executed_frac"] > r["frac"] and r["pages_count_frac"] > r["executed_frac"]
+    assert r["executed_frac"] > r["frac"] and r["pages_count_tflops"] > r["executed_tflops"]
+    assert r["pages_count_tflops"] == round(2 * 48 * OM.ns_flops(4096, 14336, 1) / (ms * 1e-3) / 1e12, 1)
     a = line["roofline_adamw"]
     assert a["frac_of_nominal_8tbs"] == round(a["achieved"] / 8000.0, 4)
 
