@@ -223,6 +223,21 @@ muon_prologue_kernel(const MuonGroup grp, NsBuffers buf, MuonScalars s) {
   uint16_t* Xh = buf.Xh[0] + static_cast<int64_t>(mat) * Ap * Bp;   // [Ap][Bp]
   float ss = 0.f;
   uint32_t mx = 0;
+  // every 16-byte load of the tile first: a load of g or m cannot be moved
+  // above a store to m, which the compiler must assume may alias it, so
+  // loads interleaved with the stores would wait for each other
+  float4 gq[kPrepTile / 16], mq[kPrepTile / 16];
+#pragma unroll
+  for (int k = 0; k < kPrepTile / 16; ++k) {
+    const int64_t r = r0 + lr0 + 16 * k, c = c0 + lc;
+    gq[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+    mq[k] = gq[k];
+    if (r < R && vec && c + 3 < C) {
+      const int64_t i = r * C + c;
+      gq[k] = __ldcs(reinterpret_cast<const float4*>(M.g + i));   // read once: evict first
+      if (!s.ns_only) mq[k] = *reinterpret_cast<const float4*>(M.m + i);
+    }
+  }
 #pragma unroll
   for (int k = 0; k < kPrepTile / 16; ++k) {
     const int lr = lr0 + 16 * k;
@@ -231,7 +246,7 @@ muon_prologue_kernel(const MuonGroup grp, NsBuffers buf, MuonScalars s) {
     if (r < R) {
       const int64_t i = r * C + c;
       if (vec && c + 3 < C) {
-        float4 g = *reinterpret_cast<const float4*>(M.g + i);
+        float4 g = gq[k];
         g.x *= gs;
         g.y *= gs;
         g.z *= gs;
@@ -242,12 +257,12 @@ muon_prologue_kernel(const MuonGroup grp, NsBuffers buf, MuonScalars s) {
           val[2] = g.z;
           val[3] = g.w;
         } else {
-          float4 m = *reinterpret_cast<const float4*>(M.m + i);
+          float4 m = mq[k];
           m.x = m.x + s.one_minus_mu * (g.x - m.x);
           m.y = m.y + s.one_minus_mu * (g.y - m.y);
           m.z = m.z + s.one_minus_mu * (g.z - m.z);
           m.w = m.w + s.one_minus_mu * (g.w - m.w);
-          *reinterpret_cast<float4*>(M.m + i) = m;
+          __stcs(reinterpret_cast<float4*>(M.m + i), m);   // not read again this step
           val[0] = gtilde(s, g.x, m.x);
           val[1] = gtilde(s, g.y, m.y);
           val[2] = gtilde(s, g.z, m.z);
