@@ -1035,6 +1035,19 @@ def run_e2e(args, step_fn, prepare_set, params, flat, t, total, dist: Dist, grou
     clocks.__exit__(None, None, None)
     dist.barrier()
     ms = dist.max(start.elapsed_time(d2h_done[-1][-1]))
+    # untimed: the idle copy bandwidth once more, after the loop (one H2D pass
+    # with no compute running), to tell a host whose copies are slow
+    # throughout from copies slowed while the loop runs
+    after = [E(), E()]
+    with torch.cuda.stream(s_in):
+        after[0].record(s_in)
+        flats[0][0].copy_(g_host, non_blocking=True)
+        after[1].record(s_in)
+    torch.cuda.synchronize()
+    idle_after = round(g_host.numel() * g_host.element_size() / (after[0].elapsed_time(after[1]) * 1e6), 1)
+    seg_bytes = [(b - a) * g_host.element_size() for _, a, b in groups]
+    step_gbs = sorted(sum(seg_bytes) / (sum(h2d_begin[k][g].elapsed_time(h2d_done[k][g]) for g in range(G)) * 1e6)
+                      for k in range(K))
     # device time of each phase per step: copies summed over the groups; the
     # step from its first group's start to its last group's end
     phase = {"h2d": round(sum(h2d_begin[k][g].elapsed_time(h2d_done[k][g]) for k in range(K) for g in range(G)) / K, 3),
@@ -1063,6 +1076,9 @@ def run_e2e(args, step_fn, prepare_set, params, flat, t, total, dist: Dist, grou
             "h2d_gbs": round(h2d / (phase["h2d"] * 1e6), 1) if phase["h2d"] > 0 else None,
             "d2h_gbs": round(d2h / (phase["d2h"] * 1e6), 1) if phase["d2h"] > 0 else None,
             "copy_gbs_before_timing": idle_gbs,
+            "h2d_gbs_after_timing": idle_after,
+            "h2d_gbs_per_step": {"min": round(step_gbs[0], 1), "median": round(statistics.median(step_gbs), 1),
+                                 "max": round(step_gbs[-1], 1)},
             "clocks": clocks.summary()}
 
 
