@@ -323,6 +323,29 @@ MPOPT_API opt_status opt_shard_plan(const opt_tensor* tensors, int32_t n, int32_
                                     double* rank_muon_work);
 
 /*
+ * How opt_muon_step / opt_mixed_step evaluate the Newton-Schulz iterations of
+ * one rows x cols matrix under `hp` (host only: nothing is launched, no GPU is
+ * needed).  Writes the size of each group of consecutive iterations that
+ * share one X X^T and one C X, in order (all 1: every iteration as written),
+ * into group_sizes[0 .. *n_groups) and their count into *n_groups; the sizes
+ * add up to hp->ns_steps.  The plan assumes a workspace from
+ * opt_workspace_size (with OPT_WORKSPACE_GROUPED when hp->flags has
+ * OPT_MUON_NS_GROUPED): a workspace without room for the grouped buffers
+ * evaluates every iteration as written.
+ * Grouping follows hp->flags (see opt_muon_hp), in groups of at most three,
+ * and splits a group into single iterations when the product of its
+ * polynomials could leave fp16's range: each iteration's largest |a + b l +
+ * c l^2| over the squared singular values it can reach (from [0, 1] after the
+ * normalisation, through the per-singular-value form of the iteration,
+ * "02 · Optimizer：算法与 infra" §5.2) is multiplied over the group, and
+ * groups above 4096 are split (the printed coefficients give about 42).
+ * Errors: OPT_ERR_INVALID_ARG for a null pointer, an invalid hp, rows or cols
+ * below 1, or capacity below hp->ns_steps.
+ */
+MPOPT_API opt_status opt_ns_plan(int64_t rows, int64_t cols, const opt_muon_hp* hp, int32_t* group_sizes,
+                                 int32_t capacity, int32_t* n_groups);
+
+/*
  * Newton-Schulz orthogonalisation alone ("02 · Optimizer：算法与 infra" §5.2):
  * O = NS_steps(G) for one fp32 rows x cols matrix G, same fp16 tensor-core
  * path as opt_muon_step.  G and O are device fp32 [rows*cols]; O may alias G.
@@ -337,7 +360,9 @@ MPOPT_API opt_status opt_newton_schulz(const float* G, float* O, int64_t rows, i
  * device memory: code hosted by a runtime that owns every device allocation
  * and gives extensions no allocator, or a path whose memory budget is fixed in
  * advance.  No counterpart on the pages: this is an interface convenience, the
- * arithmetic is exactly opt_newton_schulz's.
+ * arithmetic is opt_newton_schulz's with every iteration evaluated as written
+ * (as with OPT_MUON_NS_PER_ITERATION): the built-in scratch holds the buffers
+ * of one iteration, not those of grouped iterations.
  *   - Scratch is a 20 MiB array of device memory built into the library (a
  *     static __device__ array).  Every GPU that loads the library holds it until
  *     the process exits.  This entry point calls no cudaMalloc, cudaFree or

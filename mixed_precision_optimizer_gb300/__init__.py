@@ -13,6 +13,7 @@ Entry points (same names as the C ABI, without the ``opt_`` prefix):
 * ``mixed_step``      -- both, with the Muon/AdamW routing rule
 * ``newton_schulz``   -- Newton-Schulz orthogonalisation alone
 * ``workspace_size``  -- device scratch bytes a call needs
+* ``ns_plan``         -- how a matrix's Newton-Schulz iterations are grouped
 * ``device_status``   -- reads the device-side status word of a workspace
 * ``sharded.shard_plan`` -- opt_shard_plan: the data-parallel sharding plan
   (``sharded`` also holds the per-rank views and the bf16 exchange)
@@ -79,7 +80,7 @@ _lib = None
 
 EXPORTED = ("opt_workspace_size", "opt_adamw_step", "opt_muon_step", "opt_mixed_step", "opt_mixed_step_clipped",
             "opt_newton_schulz", "opt_newton_schulz_noalloc", "opt_noalloc_device_status",
-            "opt_reload_model_params", "opt_device_status", "opt_shard_plan",
+            "opt_reload_model_params", "opt_device_status", "opt_shard_plan", "opt_ns_plan",
             "opt_selftest_wait_timeout", "opt_profile_launches",
             "opt_strerror",
             "opt_last_cuda_error", "opt_abi_version")
@@ -131,6 +132,8 @@ def lib():
     L.opt_shard_plan.argtypes = [T, i32, i32, i32, i64, ctypes.POINTER(OptShardEntry), ctypes.POINTER(i64),
                                  ctypes.POINTER(ctypes.c_double)]
     L.opt_shard_plan.restype = ctypes.c_int
+    L.opt_ns_plan.argtypes = [i64, i64, ctypes.POINTER(OptMuonHP), ctypes.POINTER(i32), i32, ctypes.POINTER(i32)]
+    L.opt_ns_plan.restype = ctypes.c_int
     L.opt_noalloc_device_status.argtypes = [vp]
     L.opt_noalloc_device_status.restype = ctypes.c_int
     L.opt_reload_model_params.argtypes = [T, i32, vp]
@@ -297,6 +300,16 @@ def workspace_size(params: Sequence[Param], routing="auto", clip=False, ns_order
     arr = _array(params)
     r |= (WORKSPACE_CLIP if clip else 0) | (WORKSPACE_GROUPED if ns_order == "grouped" else 0)
     return int(lib().opt_workspace_size(arr, len(params), r))
+
+
+def ns_plan(rows, cols, hp: OptMuonHP):
+    """Sizes of the groups of Newton-Schulz iterations opt_muon_step uses for
+    a rows x cols matrix under hp (opt_ns_plan; host only)."""
+    cap = max(int(hp.ns_steps), 1)
+    out = (ctypes.c_int32 * cap)()
+    n = ctypes.c_int32(0)
+    _check(lib().opt_ns_plan(rows, cols, ctypes.byref(hp), out, cap, ctypes.byref(n)), "opt_ns_plan")
+    return list(out[:n.value])
 
 
 def alloc_workspace(nbytes, device=None):

@@ -365,6 +365,62 @@ float step_scale_of(const MuonPlanHp& hp, int64_t R, int64_t C) {
   return static_cast<float>(static_cast<double>(hp.lr) * static_cast<double>(hp.scale_coeff) * f);
 }
 
+// (a, b, c) of every iteration: the schedule when given, else the one triple.
+void fill_schedule(const MuonPlanHp& hp, MuonScalars& s) {
+  for (int it = 0; it < hp.ns_steps && it < 16; ++it) {
+    s.sched[it][0] = hp.schedule ? hp.schedule[3 * it + 0] : hp.a;
+    s.sched[it][1] = hp.schedule ? hp.schedule[3 * it + 1] : hp.b;
+    s.sched[it][2] = hp.schedule ? hp.schedule[3 * it + 2] : hp.c;
+  }
+}
+
+// Whether a class of (min, max) = (A, B) takes grouped iterations under hp
+// (before the check that the workspace has room for their buffers).
+bool wants_grouped(const MuonPlanHp& hp, int64_t A, int64_t B) {
+  const int ns_steps = hp.no_ortho ? 0 : hp.ns_steps;
+  return ns_steps >= 2 && hp.ns_order != OPT_MUON_NS_PER_ITERATION &&
+         (hp.ns_order == OPT_MUON_NS_GROUPED || class_grouped_by_default(A, B));
+}
+
+// Grouped iterations multiply the group's first iterate once by the product
+// M = C_{k0+g-1} ... C_k0, held in fp16.  C_k acts on each singular value s
+// of its input as p_k(s^2), p_k(l) = a_k + b_k l + c_k l^2, and iteration k
+// maps s to s |p_k(s^2)|.  The normalised input has every singular value in
+// [0, 1], so the values iteration k can see lie in [0, S_k] with S_0 = 1 and
+// S_{k+1} = max over [0, S_k] of s |p_k(s^2)|; the largest eigenvalue of M is
+// at most the product of max |p_k| over [0, S_k] (41 for the printed
+// coefficients).  A group whose bound exceeds kNsGroupBound (16x below
+// fp16's 65504) is split into single iterations.
+constexpr double kNsGroupBound = 4096.0;
+
+std::vector<int> fp16_safe_groups(const std::vector<int>& sizes, const MuonScalars& s, int ns_steps) {
+  constexpr int kGrid = 4096;
+  std::vector<double> bound(static_cast<size_t>(ns_steps));
+  double smax = 1.0;
+  for (int k = 0; k < ns_steps; ++k) {
+    const double a = s.sched[k][0], b = s.sched[k][1], c = s.sched[k][2];
+    double pmax = 0.0, next = 0.0;
+    for (int i = 0; i <= kGrid; ++i) {
+      const double x = smax * i / kGrid, l = x * x;
+      const double p = std::fabs(a + b * l + c * l * l);
+      pmax = std::max(pmax, p);
+      next = std::max(next, x * p);
+    }
+    bound[static_cast<size_t>(k)] = pmax * 1.01;   // margin for the grid
+    smax = std::min(next * 1.01, 1e30);
+  }
+  std::vector<int> out;
+  int it = 0;
+  for (const int g : sizes) {
+    double prod = 1.0;
+    for (int j = 0; j < g; ++j) prod *= bound[static_cast<size_t>(it + j)];
+    if (g > 1 && !(prod <= kNsGroupBound)) out.insert(out.end(), static_cast<size_t>(g), 1);
+    else out.push_back(g);
+    it += g;
+  }
+  return out;
+}
+
 // Runs Muon on the matrices of one shape class; all of them must have rows x
 // cols equal to (R, C) or (C, R) -- both orientations share a class.
 opt_status run_muon_class(const MuonPlanHp& hp, const ShapeClass& cls, uint8_t* region, size_t region_bytes,
@@ -374,9 +430,7 @@ opt_status run_muon_class(const MuonPlanHp& hp, const ShapeClass& cls, uint8_t* 
   // the largest group of matrices that fits the region
   const int ns_steps = hp.no_ortho ? 0 : hp.ns_steps;
   const int64_t want = static_cast<int64_t>(cls.mats.size()) < kMaxGroup ? cls.mats.size() : kMaxGroup;
-  bool grouped = ns_steps >= 2 && hp.ns_order != OPT_MUON_NS_PER_ITERATION &&
-                 (hp.ns_order == OPT_MUON_NS_GROUPED || class_grouped_by_default(cls.A, cls.B)) &&
-                 group_bytes(1, cls.A, cls.B, true) <= region_bytes;
+  const bool grouped = wants_grouped(hp, cls.A, cls.B) && group_bytes(1, cls.A, cls.B, true) <= region_bytes;
   int64_t cap = want;
   while (cap > 0 && group_bytes(cap, cls.A, cls.B, grouped) > region_bytes) --cap;
   if (cap == 0) return OPT_ERR_WORKSPACE;
@@ -412,11 +466,7 @@ opt_status run_muon_class(const MuonPlanHp& hp, const ShapeClass& cls, uint8_t* 
       s.one_minus_mu = static_cast<float>(1.0 - static_cast<double>(hp.mu));
       s.nesterov = hp.nesterov;
       s.eps = hp.eps;
-      for (int it = 0; it < hp.ns_steps && it < 16; ++it) {
-        s.sched[it][0] = hp.schedule ? hp.schedule[3 * it + 0] : hp.a;
-        s.sched[it][1] = hp.schedule ? hp.schedule[3 * it + 1] : hp.b;
-        s.sched[it][2] = hp.schedule ? hp.schedule[3 * it + 2] : hp.c;
-      }
+      fill_schedule(hp, s);
       s.decay = static_cast<float>(1.0 - static_cast<double>(hp.lr) * static_cast<double>(hp.wd));
       s.no_normalize = hp.no_ortho;
       s.ns_steps = hp.ns_steps;
@@ -461,7 +511,7 @@ opt_status run_muon_class(const MuonPlanHp& hp, const ShapeClass& cls, uint8_t* 
         if (e != cudaSuccess) return cuda_fail(e, "muon apply");
       }
       int it = 0, gi = 0;
-      for (const int g : ns_group_sizes(ns_steps, grouped)) {
+      for (const int g : fp16_safe_groups(ns_group_sizes(ns_steps, grouped), s, ns_steps)) {
         e = launch_ns_group(grp, buf, s, it, g, gi++, stream);
         if (e != cudaSuccess) return cuda_fail(e, "newton-schulz gemm");
         it += g;
@@ -495,6 +545,16 @@ opt_status split_tensors(const opt_tensor* tensors, int32_t n, int32_t routing, 
     (muon ? sp.muon : sp.adamw).push_back(&t);
   }
   return OPT_OK;
+}
+
+// The Muon plan's view of the caller's hyper-parameters.
+MuonPlanHp plan_hp(const opt_muon_hp& h, const float* grad_scale) {
+  MuonPlanHp hp{h.lr,          h.momentum,  h.weight_decay, h.eps,       h.ns_a,
+                h.ns_b,        h.ns_c,      h.scale_coeff,  h.nesterov ? 1 : 0,
+                h.ns_steps,    0,           grad_scale,     h.scale_mode,
+                (h.flags & OPT_MUON_NO_ORTHOGONALIZE) ? 1 : 0, h.ns_schedule};
+  hp.ns_order = h.flags & (OPT_MUON_NS_PER_ITERATION | OPT_MUON_NS_GROUPED);
+  return hp;
 }
 
 // AdamW needs no workspace; Muon needs the status header and the group buffers.
@@ -603,11 +663,7 @@ opt_status mixed_impl(const opt_muon_hp* hpm, const opt_adamw_hp* hpa, const opt
   if (any_muon) {
     uint32_t* status = reinterpret_cast<uint32_t*>(ws);
     const size_t off = kHeaderBytes + clip_region;
-    MuonPlanHp hp{hpm->lr,         hpm->momentum,           hpm->weight_decay, hpm->eps,
-                  hpm->ns_a,       hpm->ns_b,               hpm->ns_c,         hpm->scale_coeff,
-                  hpm->nesterov ? 1 : 0, hpm->ns_steps, 0,  grad_scale,        hpm->scale_mode,
-                  (hpm->flags & OPT_MUON_NO_ORTHOGONALIZE) ? 1 : 0,          hpm->ns_schedule};
-    hp.ns_order = hpm->flags & (OPT_MUON_NS_PER_ITERATION | OPT_MUON_NS_GROUPED);
+    const MuonPlanHp hp = plan_hp(*hpm, grad_scale);
     for (const ShapeClass& c : classes) {
       if ((st = run_muon_class(hp, c, ws + off, ws_bytes - off, status, stream, nullptr)) != OPT_OK) return st;
     }
@@ -716,6 +772,24 @@ opt_status opt_shard_plan(const opt_tensor* tensors, int32_t n, int32_t routing,
   }
   if (rank_muon_work)
     for (int32_t r = 0; r < world_size; ++r) rank_muon_work[r] = work[static_cast<size_t>(r)];
+  return OPT_OK;
+}
+
+opt_status opt_ns_plan(int64_t rows, int64_t cols, const opt_muon_hp* hp, int32_t* group_sizes, int32_t capacity,
+                       int32_t* n_groups) {
+  if (!group_sizes || !n_groups || rows < 1 || cols < 1) return OPT_ERR_INVALID_ARG;
+  opt_status st = check_muon_hp(hp);
+  if (st != OPT_OK) return st;
+  const MuonPlanHp ph = plan_hp(*hp, nullptr);
+  const int ns_steps = ph.no_ortho ? 0 : ph.ns_steps;
+  if (capacity < ns_steps) return OPT_ERR_INVALID_ARG;
+  int64_t A, B, Ap, Bp;
+  shape_of(rows, cols, A, B, Ap, Bp);
+  MuonScalars s{};
+  fill_schedule(ph, s);
+  const std::vector<int> sizes = fp16_safe_groups(ns_group_sizes(ns_steps, wants_grouped(ph, A, B)), s, ns_steps);
+  for (size_t k = 0; k < sizes.size(); ++k) group_sizes[k] = sizes[k];
+  *n_groups = static_cast<int32_t>(sizes.size());
   return OPT_OK;
 }
 

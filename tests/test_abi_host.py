@@ -179,6 +179,61 @@ def test_grouped_iterations_by_default_where_they_pay(L):
         assert L.opt_workspace_size(arr(tensor(R, C)), 1, mp.KIND_MUON | mp.WORKSPACE_GROUPED) == base + 2 * aa
 
 
+def test_ns_plan_grouping_rules(L):
+    """opt_ns_plan (host only) reports how a matrix's iterations are grouped:
+    groups of at most three, the larger first, for the shapes grouped by
+    default (padded max side >= 2 x padded min side, min side >= 1024) or
+    every shape with OPT_MUON_NS_GROUPED; one at a time otherwise."""
+    hp = mp.muon_hp()
+    assert mp.ns_plan(4096, 14336, hp) == [3, 2] and mp.ns_plan(14336, 4096, hp) == [3, 2]
+    assert mp.ns_plan(1024, 4096, hp) == [3, 2]
+    for shape in ((4096, 4096), (768, 2048), (1024, 1700), (300, 700), (1, 64)):
+        assert mp.ns_plan(*shape, hp) == [1] * 5, shape
+        assert mp.ns_plan(*shape, mp.muon_hp(ns_order="grouped")) == [3, 2], shape
+    assert mp.ns_plan(4096, 14336, mp.muon_hp(ns_order="per_iteration")) == [1] * 5
+    for steps, sizes in ((1, [1]), (2, [2]), (3, [3]), (4, [2, 2]), (6, [3, 3]), (7, [3, 2, 2]),
+                         (8, [3, 3, 2]), (16, [3, 3, 3, 3, 2, 2])):
+        assert mp.ns_plan(300, 700, mp.muon_hp(ns_steps=steps, ns_order="grouped")) == sizes, steps
+    assert mp.ns_plan(4096, 14336, mp.muon_hp(ns_steps=0)) == []
+    assert mp.ns_plan(4096, 14336, mp.muon_hp(orthogonalize=False)) == []
+
+
+def test_ns_plan_splits_groups_that_could_leave_fp16(L):
+    """A group is split into single iterations when the product of its
+    polynomials' largest values over the reachable singular values exceeds
+    4096.  With b = c = 0 an iteration multiplies every singular value by a:
+    a = 15 three times bounds the group by 15^3 = 3375 (grouped), a = 16 by
+    4096 plus the bound's margin (split).  The printed coefficients bound a
+    group of three by about 42."""
+    g = lambda a: mp.muon_hp(ns_order="grouped", schedule=[(a, 0.0, 0.0)] * 3 + [(1.0, 0.0, 0.0)] * 2)
+    assert mp.ns_plan(300, 700, g(15.0)) == [3, 2]
+    assert mp.ns_plan(300, 700, g(16.0)) == [1, 1, 1, 2]
+    assert mp.ns_plan(300, 700, g(-16.0)) == [1, 1, 1, 2]           # |p| counts
+    big_late = mp.muon_hp(ns_order="grouped", schedule=[(1.0, 0.0, 0.0)] * 3 + [(100.0, 0.0, 0.0)] * 2)
+    assert mp.ns_plan(300, 700, big_late) == [3, 1, 1]
+    # the printed coefficients, and a schedule whose quintics keep [0, 1]
+    # bounded, stay grouped; one whose singular values near 1 grow without
+    # bound (envelope 42 after four iterations) has its second group split
+    assert mp.ns_plan(300, 700, mp.muon_hp(ns_order="grouped")) == [3, 2]
+    bounded = [(3.4445, -4.7750, 2.0315), (3.2, -4.4, 1.9), (3.0, -4.0, 1.7), (2.8, -3.6, 1.55), (2.2, -2.1, 0.9)]
+    assert mp.ns_plan(300, 700, mp.muon_hp(ns_order="grouped", schedule=bounded)) == [3, 2]
+    growing = [(3.4445, -4.7750, 2.0315), (3.0, -3.8, 1.7), (2.8, -3.4, 1.5), (3.2, -4.3, 1.9), (2.5, -2.9, 1.3)]
+    assert mp.ns_plan(300, 700, mp.muon_hp(ns_order="grouped", schedule=growing)) == [3, 1, 1]
+
+
+def test_ns_plan_errors(L):
+    hp = mp.muon_hp()
+    out, n = (ctypes.c_int32 * 8)(), ctypes.c_int32(0)
+    assert L.opt_ns_plan(0, 10, ctypes.byref(hp), out, 8, ctypes.byref(n)) == 1
+    assert L.opt_ns_plan(10, 10, None, out, 8, ctypes.byref(n)) == 1
+    assert L.opt_ns_plan(10, 10, ctypes.byref(hp), None, 8, ctypes.byref(n)) == 1
+    assert L.opt_ns_plan(10, 10, ctypes.byref(hp), out, 4, ctypes.byref(n)) == 1     # capacity < ns_steps
+    bad = mp.muon_hp()
+    bad.flags = mp.MUON_NS_GROUPED | mp.MUON_NS_PER_ITERATION
+    assert L.opt_ns_plan(10, 10, ctypes.byref(bad), out, 8, ctypes.byref(n)) == 1
+    assert L.opt_ns_plan(10, 10, ctypes.byref(hp), out, 5, ctypes.byref(n)) == 0 and n.value == 5
+
+
 def test_ns_order_flags(L):
     """At most one evaluation-order flag; unknown flag bits are refused.  The
     hyper-parameters are checked before the workspace, so an accepted flag

@@ -126,9 +126,14 @@ def test_grouped_step_counts(steps):
 
 def test_grouped_coefficient_schedule():
     """A different (a, b, c) in every iteration: each polynomial of a group
-    takes its own iteration's coefficients."""
+    takes its own iteration's coefficients.  The schedule keeps the iteration
+    bounded on every singular value in [0, 1] (each quintic maps the range
+    the previous ones reach back into [0, 1.22]), so the plan keeps both
+    groups; a schedule that lets singular values near 1 grow without bound
+    is split into single iterations (test_abi_host.py)."""
     shape = (384, 1000)
-    sched = [(3.4445, -4.7750, 2.0315), (3.0, -3.8, 1.7), (2.8, -3.4, 1.5), (3.2, -4.3, 1.9), (2.5, -2.9, 1.3)]
+    sched = [(3.4445, -4.7750, 2.0315), (3.2, -4.4, 1.9), (3.0, -4.0, 1.7), (2.8, -3.6, 1.55), (2.2, -2.1, 0.9)]
+    assert mp.ns_plan(*shape, mp.muon_hp(schedule=sched, ns_order="grouped")) == [3, 2]
     rng = np.random.default_rng(7)
     W = (rng.standard_normal(shape) * 0.02).astype(np.float32)
     m = np.zeros(shape, np.float32)
@@ -209,3 +214,34 @@ def test_grouped_three_consecutive_steps_batched_both_orientations():
             assert rel(W0[i].astype(np.float64) - host(p.main_param), W0[i].astype(np.float64) - Wn) < NS_TOL
             assert np.allclose(hm[i], mn, rtol=1e-5, atol=1e-9)
             assert np.array_equal(bf16_host(p.model), OA.bf16_rne(host(p.main_param)))
+
+
+@pytest.mark.parametrize("case", ["default_wide", "default_square", "forced", "per_iteration", "split"])
+def test_launches_follow_the_plan(case):
+    """The GEMM launches of a step are the ones opt_ns_plan reports for the
+    matrix (host only), including a group split because its product could
+    leave fp16's range: two iterations that multiply every singular value by
+    70 bound the pair by about 4998 > 4096, so they run one at a time (the
+    result is 4900 X0, as in the oracle)."""
+    shape, hp, ws_order = {
+        "default_wide": ((1024, 2048), mp.muon_hp(), "auto"),
+        "default_square": ((512, 512), mp.muon_hp(), "auto"),
+        "forced": ((300, 700), mp.muon_hp(ns_order="grouped", ns_steps=7), "grouped"),
+        "per_iteration": ((1024, 4096), mp.muon_hp(ns_order="per_iteration"), "auto"),
+        "split": ((300, 700), mp.muon_hp(ns_order="grouped", ns_steps=2, schedule=[(70.0, 0.0, 0.0)] * 2),
+                  "grouped"),
+    }[case]
+    plan = mp.ns_plan(*shape, hp)
+    rng = np.random.default_rng(len(case))
+    W = (rng.standard_normal(shape) * 0.02).astype(np.float32)
+    m = np.zeros(shape, np.float32)
+    g = (rng.standard_normal(shape) * 1e-2).astype(np.float32)
+    W1, _, _, stages = muon_step_gpu(W, g, m, hp, ws_order)
+    assert stages == {"ns_gram": len(plan), "ns_poly": sum(plan), "ns_sym": sum(3 * (k - 1) for k in plan),
+                      "ns_bx": len(plan)}, (plan, stages)
+    if case == "split":
+        assert plan == [1, 1]
+    coeffs = [(hp.ns_schedule[3 * i], hp.ns_schedule[3 * i + 1], hp.ns_schedule[3 * i + 2])
+              for i in range(hp.ns_steps)] if hp.ns_schedule else OM.NS_COEFFS
+    Wn, _, _ = OM.muon_step(W, g, m, lr=0.02, momentum=0.95, ns_steps=hp.ns_steps, coeffs=coeffs)
+    assert rel(W.astype(np.float64) - W1, W.astype(np.float64) - Wn) < NS_TOL
