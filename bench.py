@@ -962,21 +962,30 @@ def run_e2e(args, step_fn, prepare_set, params, flat, t, total, dist: Dist, grou
         groups = [(lambda tt, si: step_fn(tt, preps[si]), 0, n_flat)]
     G = len(groups)
     compute = torch.cuda.current_stream()
+    # H2D: SM loads of the pinned buffers (opt_copy_from_host) on its own
+    # stream, beside the optimizer's kernels; the copy engines' host-to-device
+    # rate from page-locked memory varies with the pages and over time on these
+    # hosts.  D2H: the copy engines.
     s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    h2d_copy = lambda dst, src: mp.copy_from_host(dst, src, stream=s_in)
     # untimed: one pass of each copy direction over every host buffer; the
     # first pass is timed on its own to show the copy bandwidth of this host
-    # with no compute running (the two directions overlap each other)
+    # with no compute running (the two directions overlap each other), and a
+    # copy-engine H2D pass is timed for comparison
     E = lambda: torch.cuda.Event(enable_timing=True)
-    warm = [E() for _ in range(4)]
+    warm = [E() for _ in range(6)]
     s_in.wait_stream(compute)
     s_out.wait_stream(compute)
     for i, (gd, bd) in enumerate(flats):
         with torch.cuda.stream(s_in):
             if i == 0:
                 warm[0].record(s_in)
-            gd.copy_(g_host, non_blocking=True)
+            h2d_copy(gd, g_host)
             if i == 0:
                 warm[1].record(s_in)
+                warm[4].record(s_in)
+                gd.copy_(g_host, non_blocking=True)
+                warm[5].record(s_in)
         with torch.cuda.stream(s_out):
             if i == 0:
                 warm[2].record(s_out)
@@ -989,7 +998,9 @@ def run_e2e(args, step_fn, prepare_set, params, flat, t, total, dist: Dist, grou
     start = E()
     torch.cuda.synchronize()
     idle_gbs = {"h2d": round(g_host.numel() * g_host.element_size() / (warm[0].elapsed_time(warm[1]) * 1e6), 1),
-                "d2h": round(b_host.numel() * b_host.element_size() / (warm[2].elapsed_time(warm[3]) * 1e6), 1)}
+                "d2h": round(b_host.numel() * b_host.element_size() / (warm[2].elapsed_time(warm[3]) * 1e6), 1),
+                "h2d_copy_engine": round(g_host.numel() * g_host.element_size() /
+                                         (warm[4].elapsed_time(warm[5]) * 1e6), 1)}
     clocks = ClockSampler(smi_index(torch.cuda.current_device()), "_e2e").__enter__()
     dist.barrier()
     torch.cuda.synchronize()
@@ -1006,7 +1017,7 @@ def run_e2e(args, step_fn, prepare_set, params, flat, t, total, dist: Dist, grou
                 if k >= 2:
                     s_in.wait_event(step_done[k - 2][g])   # step k-2 finished reading this segment
                 h2d_begin[k][g].record(s_in)
-                gd[a:b].copy_(g_host[a:b], non_blocking=True)
+                h2d_copy(gd[a:b], g_host[a:b])
                 h2d_done[k][g].record(s_in)
         h1 = time.perf_counter()
         h_step = 0.0
@@ -1038,13 +1049,18 @@ def run_e2e(args, step_fn, prepare_set, params, flat, t, total, dist: Dist, grou
     # untimed: the idle copy bandwidth once more, after the loop (one H2D pass
     # with no compute running), to tell a host whose copies are slow
     # throughout from copies slowed while the loop runs
-    after = [E(), E()]
+    after = [E() for _ in range(4)]
     with torch.cuda.stream(s_in):
         after[0].record(s_in)
-        flats[0][0].copy_(g_host, non_blocking=True)
+        h2d_copy(flats[0][0], g_host)
         after[1].record(s_in)
+        after[2].record(s_in)
+        flats[0][0].copy_(g_host, non_blocking=True)
+        after[3].record(s_in)
     torch.cuda.synchronize()
-    idle_after = round(g_host.numel() * g_host.element_size() / (after[0].elapsed_time(after[1]) * 1e6), 1)
+    nb = g_host.numel() * g_host.element_size()
+    idle_after = {"h2d": round(nb / (after[0].elapsed_time(after[1]) * 1e6), 1),
+                  "h2d_copy_engine": round(nb / (after[2].elapsed_time(after[3]) * 1e6), 1)}
     seg_bytes = [(b - a) * g_host.element_size() for _, a, b in groups]
     step_gbs = sorted(sum(seg_bytes) / (sum(h2d_begin[k][g].elapsed_time(h2d_done[k][g]) for g in range(G)) * 1e6)
                       for k in range(K))
@@ -1067,6 +1083,8 @@ def run_e2e(args, step_fn, prepare_set, params, flat, t, total, dist: Dist, grou
                           "one library call per step; main_grad and bf16 model buffers one copy per direction") +
                          "; buffers double-buffered; H2D, compute and D2H on three streams; the first step's "
                          "first H2D and the last step's last D2H are not overlapped and are included",
+            "h2d_by": "SM loads of the pinned host buffers (opt_copy_from_host, 32 CTAs) on its own stream; "
+                      "D2H by the copy engines",
             "host_buffers": f"one cudaHostAlloc arena of {arena.nbytes} bytes (torch pinned memory); "
                             "copies warmed once before timing",
             "host_wall_ms_per_step": round(wall_ms / K, 3),

@@ -346,6 +346,26 @@ MPOPT_API opt_status opt_ns_plan(int64_t rows, int64_t cols, const opt_muon_hp* 
                                  int32_t capacity, int32_t* n_groups);
 
 /*
+ * Copies `bytes` from page-locked host memory `src` (cudaHostAlloc, or
+ * registered with cudaHostRegister) to device memory `dst` of the current
+ * device, enqueued on `stream`, with a kernel whose threads load the host
+ * buffer over the CPU-GPU link and store to device memory (32 CTAs, no
+ * shared memory: it runs beside the optimizer's kernels on another stream
+ * and leaves most SMs to them).  No counterpart on the pages: it serves callers whose gradients
+ * arrive in host memory.  On GB300 hosts the copy engines' host-to-device
+ * rate (cudaMemcpyAsync) from page-locked memory varies with the pages and
+ * over time, down to 13-40 GB/s on some buffers of some hosts, while loads by
+ * the SMs keep about 210 GB/s.
+ *   dst, src  4-byte aligned (16-byte aligned for the vector path), not
+ *             overlapping; bytes a multiple of 4.
+ * Errors: OPT_ERR_INVALID_ARG for null pointers, a src that is not
+ * page-locked host memory, or a dst that is not device memory of the current
+ * device; OPT_ERR_MISALIGNED for the alignment rules; OPT_ERR_CUDA if the
+ * launch fails.  bytes == 0 does nothing.
+ */
+MPOPT_API opt_status opt_copy_from_host(void* dst, const void* src, size_t bytes, void* stream);
+
+/*
  * Newton-Schulz orthogonalisation alone ("02 · Optimizer：算法与 infra" §5.2):
  * O = NS_steps(G) for one fp32 rows x cols matrix G, same fp16 tensor-core
  * path as opt_muon_step.  G and O are device fp32 [rows*cols]; O may alias G.

@@ -30,6 +30,8 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libmpopt.so")
 
 OPT_OK = 0
+OPT_ERR_INVALID_ARG = 1
+OPT_ERR_MISALIGNED = 3
 OPT_ERR_DEVICE_TIMEOUT = 6
 STATUS_NAMES = {0: "OPT_OK", 1: "OPT_ERR_INVALID_ARG", 2: "OPT_ERR_UNSUPPORTED", 3: "OPT_ERR_MISALIGNED",
                 4: "OPT_ERR_WORKSPACE", 5: "OPT_ERR_CUDA", 6: "OPT_ERR_DEVICE_TIMEOUT"}
@@ -81,6 +83,7 @@ _lib = None
 EXPORTED = ("opt_workspace_size", "opt_adamw_step", "opt_muon_step", "opt_mixed_step", "opt_mixed_step_clipped",
             "opt_newton_schulz", "opt_newton_schulz_noalloc", "opt_noalloc_device_status",
             "opt_reload_model_params", "opt_device_status", "opt_shard_plan", "opt_ns_plan",
+            "opt_copy_from_host",
             "opt_selftest_wait_timeout", "opt_profile_launches",
             "opt_strerror",
             "opt_last_cuda_error", "opt_abi_version")
@@ -134,6 +137,8 @@ def lib():
     L.opt_shard_plan.restype = ctypes.c_int
     L.opt_ns_plan.argtypes = [i64, i64, ctypes.POINTER(OptMuonHP), ctypes.POINTER(i32), i32, ctypes.POINTER(i32)]
     L.opt_ns_plan.restype = ctypes.c_int
+    L.opt_copy_from_host.argtypes = [vp, vp, sz, vp]
+    L.opt_copy_from_host.restype = ctypes.c_int
     L.opt_noalloc_device_status.argtypes = [vp]
     L.opt_noalloc_device_status.restype = ctypes.c_int
     L.opt_reload_model_params.argtypes = [T, i32, vp]
@@ -300,6 +305,20 @@ def workspace_size(params: Sequence[Param], routing="auto", clip=False, ns_order
     arr = _array(params)
     r |= (WORKSPACE_CLIP if clip else 0) | (WORKSPACE_GROUPED if ns_order == "grouped" else 0)
     return int(lib().opt_workspace_size(arr, len(params), r))
+
+
+def copy_from_host(dst, src, stream=None):
+    """dst (CUDA tensor) <- src (page-locked CPU tensor) by SM loads of the
+    host buffer (opt_copy_from_host), enqueued on `stream`; both contiguous,
+    with the same number of bytes."""
+    import torch
+    if not (dst.is_cuda and dst.is_contiguous() and not src.is_cuda and src.is_contiguous()):
+        raise ValueError("copy_from_host: dst must be a contiguous CUDA tensor and src a contiguous CPU tensor")
+    nbytes = src.numel() * src.element_size()
+    if dst.numel() * dst.element_size() != nbytes:
+        raise ValueError("copy_from_host: dst and src differ in size")
+    _check(lib().opt_copy_from_host(ctypes.c_void_p(dst.data_ptr()), ctypes.c_void_p(src.data_ptr()), nbytes,
+                                    _stream(stream)), "opt_copy_from_host")
 
 
 def ns_plan(rows, cols, hp: OptMuonHP):

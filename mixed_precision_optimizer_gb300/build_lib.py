@@ -20,7 +20,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 OBJ = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmpopt.so")
-SOURCES = ["api.cu", "adamw.cu", "clip.cu", "lifecycle.cu", "muon_elementwise.cu", "ns_gemm.cu"]
+SOURCES = ["api.cu", "adamw.cu", "clip.cu", "hostcopy.cu", "lifecycle.cu", "muon_elementwise.cu", "ns_gemm.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
          "--expt-relaxed-constexpr", "-I", os.path.join(ROOT, "include")]

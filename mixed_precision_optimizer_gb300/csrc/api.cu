@@ -793,6 +793,24 @@ opt_status opt_ns_plan(int64_t rows, int64_t cols, const opt_muon_hp* hp, int32_
   return OPT_OK;
 }
 
+opt_status opt_copy_from_host(void* dst, const void* src, size_t bytes, void* stream) {
+  if (bytes == 0) return OPT_OK;
+  if (!dst || !src) return OPT_ERR_INVALID_ARG;
+  if (((reinterpret_cast<uintptr_t>(dst) | reinterpret_cast<uintptr_t>(src)) & 3u) || (bytes & 3u))
+    return OPT_ERR_MISALIGNED;
+  cudaPointerAttributes sa{}, da{};
+  if (cudaPointerGetAttributes(&sa, src) != cudaSuccess || cudaPointerGetAttributes(&da, dst) != cudaSuccess) {
+    cudaGetLastError();
+    return OPT_ERR_INVALID_ARG;
+  }
+  if (sa.type != cudaMemoryTypeHost || sa.devicePointer == nullptr) return OPT_ERR_INVALID_ARG;
+  if (da.type != cudaMemoryTypeDevice && da.type != cudaMemoryTypeManaged) return OPT_ERR_INVALID_ARG;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || da.device != dev) return OPT_ERR_INVALID_ARG;
+  const cudaError_t e = launch_copy_from_host(dst, sa.devicePointer, bytes, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? OPT_OK : cuda_fail(e, "copy from host");
+}
+
 opt_status opt_reload_model_params(const opt_tensor* tensors, int32_t n, void* stream) {
   if (n < 0 || (n > 0 && !tensors)) return OPT_ERR_INVALID_ARG;
   for (int32_t i = 0; i < n; ++i) {

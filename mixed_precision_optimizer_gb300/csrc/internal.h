@@ -250,6 +250,10 @@ static_assert(sizeof(ReloadBatch) <= 32000, "kernel parameter space");
 
 cudaError_t launch_reload(const ReloadBatch& batch, cudaStream_t stream);
 
+// Host-to-device copy of page-locked host memory by SM loads
+// (opt_copy_from_host); src is the device-visible address of the host buffer.
+cudaError_t launch_copy_from_host(void* dst, const void* src, size_t bytes, cudaStream_t stream);
+
 int num_sms();   // SM count of the current device (cached per device)
 
 // Launch instrumentation (opt_profile_launches).  A launch site calls

@@ -288,3 +288,13 @@ def test_library_has_no_cpu_fallback():
             if f.endswith((".py", ".cu", ".h")):
                 src = open(os.path.join(dirpath, f), encoding="utf-8").read()
                 assert "oracle" not in src.replace("the oracle", ""), f
+
+
+def test_copy_from_host_argument_errors(L):
+    """Checked on the host before any CUDA call: null pointers, alignment,
+    and an empty copy that does nothing."""
+    assert L.opt_copy_from_host(None, ctypes.c_void_p(FAKE), 16, None) == 1
+    assert L.opt_copy_from_host(ctypes.c_void_p(FAKE), None, 16, None) == 1
+    assert L.opt_copy_from_host(ctypes.c_void_p(FAKE + 2), ctypes.c_void_p(FAKE), 16, None) == 3
+    assert L.opt_copy_from_host(ctypes.c_void_p(FAKE), ctypes.c_void_p(FAKE), 14, None) == 3
+    assert L.opt_copy_from_host(None, None, 0, None) == 0
