@@ -962,30 +962,41 @@ def run_e2e(args, step_fn, prepare_set, params, flat, t, total, dist: Dist, grou
         groups = [(lambda tt, si: step_fn(tt, preps[si]), 0, n_flat)]
     G = len(groups)
     compute = torch.cuda.current_stream()
-    # H2D: SM loads of the pinned buffers (opt_copy_from_host) on its own
-    # stream, beside the optimizer's kernels; the copy engines' host-to-device
-    # rate from page-locked memory varies with the pages and over time on these
-    # hosts.  D2H: the copy engines.
-    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
-    h2d_copy = lambda dst, src: mp.copy_from_host(dst, src, stream=s_in)
+    # H2D by two paths at once: the copy engines on one stream and SM loads of
+    # the pinned buffers (opt_copy_from_host) on another, each taking a share
+    # of every segment.  On these hosts either path's host-to-device rate can
+    # drop, with the pages, over time and from host to host, and the two share
+    # one limit of about 200 GB/s.  The copies need only keep up with the
+    # compute, and the SM loads slow the compute more than the copy engines
+    # do: each step gives the copy engines what they moved per ms on the step
+    # two back (finished by then) times 0.9 of that step's compute time, and
+    # the SM loads the rest (at least 5 % each, so both rates stay measured).
+    # D2H: the copy engines.
+    s_sm, s_ce, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    sm_copy = lambda dst, src, st: mp.copy_from_host(dst, src, stream=st)
+    ce_copy = lambda dst, src, st: dst.copy_(src, non_blocking=True)
     # untimed: one pass of each copy direction over every host buffer; the
-    # first pass is timed on its own to show the copy bandwidth of this host
-    # with no compute running (the two directions overlap each other), and a
-    # copy-engine H2D pass is timed for comparison
+    # first pass of each H2D path is timed on its own (the SM pass beside the
+    # first D2H, then the copy-engine pass) to show this host's copy rates
+    # with no compute running, and to set the first step's shares
     E = lambda: torch.cuda.Event(enable_timing=True)
     warm = [E() for _ in range(6)]
-    s_in.wait_stream(compute)
-    s_out.wait_stream(compute)
+    for st in (s_sm, s_ce, s_out):
+        st.wait_stream(compute)
     for i, (gd, bd) in enumerate(flats):
-        with torch.cuda.stream(s_in):
+        with torch.cuda.stream(s_sm):
             if i == 0:
-                warm[0].record(s_in)
-            h2d_copy(gd, g_host)
+                warm[0].record(s_sm)
+            sm_copy(gd, g_host, s_sm)
             if i == 0:
-                warm[1].record(s_in)
-                warm[4].record(s_in)
-                gd.copy_(g_host, non_blocking=True)
-                warm[5].record(s_in)
+                warm[1].record(s_sm)
+        with torch.cuda.stream(s_ce):
+            s_ce.wait_stream(s_sm)
+            if i == 0:
+                warm[4].record(s_ce)
+            ce_copy(gd, g_host, s_ce)
+            if i == 0:
+                warm[5].record(s_ce)
         with torch.cuda.stream(s_out):
             if i == 0:
                 warm[2].record(s_out)
@@ -993,36 +1004,66 @@ def run_e2e(args, step_fn, prepare_set, params, flat, t, total, dist: Dist, grou
             if i == 0:
                 warm[3].record(s_out)
     ev = lambda: [[E() for _ in range(G)] for _ in range(K)]
-    h2d_begin, h2d_done, step_done, d2h_begin, d2h_done = ev(), ev(), ev(), ev(), ev()
+    sm_b, sm_e, ce_b, ce_e, step_done, d2h_begin, d2h_done = (ev() for _ in range(7))
     step_begin = [E() for _ in range(K)]
     start = E()
     torch.cuda.synchronize()
-    idle_gbs = {"h2d": round(g_host.numel() * g_host.element_size() / (warm[0].elapsed_time(warm[1]) * 1e6), 1),
+    nb_g = g_host.numel() * g_host.element_size()
+    idle_gbs = {"h2d": round(nb_g / (warm[0].elapsed_time(warm[1]) * 1e6), 1),
                 "d2h": round(b_host.numel() * b_host.element_size() / (warm[2].elapsed_time(warm[3]) * 1e6), 1),
-                "h2d_copy_engine": round(g_host.numel() * g_host.element_size() /
-                                         (warm[4].elapsed_time(warm[5]) * 1e6), 1)}
+                "h2d_copy_engine": round(nb_g / (warm[4].elapsed_time(warm[5]) * 1e6), 1)}
+    clamp = lambda f: min(max(f, 0.05), 0.95)
+    f_sm = 0.5
+    need = sum(b - a for _, a, b in groups) * g_host.element_size()
+    shares, cuts = [], [[None] * G for _ in range(K)]
+
+    def rates(j):
+        """Bytes per ms of each H2D path on step j (finished)."""
+        out = []
+        for b_ev, e_ev, part in ((sm_b, sm_e, 0), (ce_b, ce_e, 1)):
+            t = sum(b_ev[j][g].elapsed_time(e_ev[j][g]) for g in range(G))
+            n = sum((cuts[j][g][1] - cuts[j][g][0]) if part == 0 else (cuts[j][g][2] - cuts[j][g][1])
+                    for g in range(G)) * g_host.element_size()
+            out.append(n / t if t > 0 and n > 0 else None)
+        return out
+
     clocks = ClockSampler(smi_index(torch.cuda.current_device()), "_e2e").__enter__()
     dist.barrier()
     torch.cuda.synchronize()
     t_wall = time.perf_counter()
-    host_ms = [0.0, 0.0, 0.0]
+    host_ms = [0.0, 0.0, 0.0, 0.0]
     start.record(compute)
-    s_in.wait_event(start)
-    s_out.wait_event(start)
+    for st in (s_sm, s_ce, s_out):
+        st.wait_event(start)
     for k in range(K):
+        hw = time.perf_counter()
+        if k >= 2:
+            # at most two steps in flight: step k-2's compute (and so its
+            # copies) has finished, and its copy rates set this step's shares
+            step_done[k - 2][G - 1].synchronize()
+            _, r_ce = rates(k - 2)
+            if r_ce:
+                f_sm = clamp(1.0 - 0.9 * r_ce * step_begin[k - 2].elapsed_time(step_done[k - 2][G - 1]) / need)
         h0 = time.perf_counter()
+        host_ms[3] += (h0 - hw) * 1e3
+        shares.append(f_sm)
         gd, bd = flats[k % 2]
-        with torch.cuda.stream(s_in):                  # gradients of step k, group by group
-            for g, (_, a, b) in enumerate(groups):
-                if k >= 2:
-                    s_in.wait_event(step_done[k - 2][g])   # step k-2 finished reading this segment
-                h2d_begin[k][g].record(s_in)
-                h2d_copy(gd[a:b], g_host[a:b])
-                h2d_done[k][g].record(s_in)
+        for g, (_, a, b) in enumerate(groups):     # gradients of step k, group by group
+            m = a + int((b - a) * f_sm) // 64 * 64
+            cuts[k][g] = (a, m, b)
+            for st, b_ev, e_ev, lo, hi, copy in ((s_sm, sm_b, sm_e, a, m, sm_copy), (s_ce, ce_b, ce_e, m, b, ce_copy)):
+                with torch.cuda.stream(st):
+                    if k >= 2:
+                        st.wait_event(step_done[k - 2][g])   # step k-2 finished reading this segment
+                    b_ev[k][g].record(st)
+                    if hi > lo:
+                        copy(gd[lo:hi], g_host[lo:hi], st)
+                    e_ev[k][g].record(st)
         h1 = time.perf_counter()
         h_step = 0.0
         for g, (call, a, b) in enumerate(groups):
-            compute.wait_event(h2d_done[k][g])
+            compute.wait_event(sm_e[k][g])
+            compute.wait_event(ce_e[k][g])
             if k >= 2:
                 compute.wait_event(d2h_done[k - 2][g])   # model copy of this segment of set k % 2 read back
             if g == 0:
@@ -1046,27 +1087,35 @@ def run_e2e(args, step_fn, prepare_set, params, flat, t, total, dist: Dist, grou
     clocks.__exit__(None, None, None)
     dist.barrier()
     ms = dist.max(start.elapsed_time(d2h_done[-1][-1]))
-    # untimed: the idle copy bandwidth once more, after the loop (one H2D pass
-    # with no compute running), to tell a host whose copies are slow
-    # throughout from copies slowed while the loop runs
+    # untimed: the idle copy rates once more, after the loop (one H2D pass
+    # of each path with no compute running), to tell a host whose copies are
+    # slow throughout from copies slowed while the loop runs
     after = [E() for _ in range(4)]
-    with torch.cuda.stream(s_in):
-        after[0].record(s_in)
-        h2d_copy(flats[0][0], g_host)
-        after[1].record(s_in)
-        after[2].record(s_in)
-        flats[0][0].copy_(g_host, non_blocking=True)
-        after[3].record(s_in)
+    with torch.cuda.stream(s_sm):
+        after[0].record(s_sm)
+        sm_copy(flats[0][0], g_host, s_sm)
+        after[1].record(s_sm)
+    with torch.cuda.stream(s_ce):
+        s_ce.wait_stream(s_sm)
+        after[2].record(s_ce)
+        ce_copy(flats[0][0], g_host, s_ce)
+        after[3].record(s_ce)
     torch.cuda.synchronize()
-    nb = g_host.numel() * g_host.element_size()
-    idle_after = {"h2d": round(nb / (after[0].elapsed_time(after[1]) * 1e6), 1),
-                  "h2d_copy_engine": round(nb / (after[2].elapsed_time(after[3]) * 1e6), 1)}
+    idle_after = {"h2d": round(nb_g / (after[0].elapsed_time(after[1]) * 1e6), 1),
+                  "h2d_copy_engine": round(nb_g / (after[2].elapsed_time(after[3]) * 1e6), 1)}
+    # a step's H2D spans from the first start to the last end of its parts
+    # (the two streams run staggered, so per-segment spans would overlap)
+    at = lambda e: start.elapsed_time(e)
+    span = [max(max(at(sm_e[k][g]), at(ce_e[k][g])) for g in range(G)) -
+            min(min(at(sm_b[k][g]), at(ce_b[k][g])) for g in range(G)) for k in range(K)]
     seg_bytes = [(b - a) * g_host.element_size() for _, a, b in groups]
-    step_gbs = sorted(sum(seg_bytes) / (sum(h2d_begin[k][g].elapsed_time(h2d_done[k][g]) for g in range(G)) * 1e6)
-                      for k in range(K))
-    # device time of each phase per step: copies summed over the groups; the
-    # step from its first group's start to its last group's end
-    phase = {"h2d": round(sum(h2d_begin[k][g].elapsed_time(h2d_done[k][g]) for k in range(K) for g in range(G)) / K, 3),
+    step_gbs = sorted(sum(seg_bytes) / (span[k] * 1e6) for k in range(K))
+    path_gbs = [[r / 1e6 if r else None for r in rates(k)] for k in range(K)]
+    med = lambda xs: round(statistics.median(xs), 1) if xs else None
+    # device time of each phase per step: the H2D span above, the D2H copies
+    # summed over the groups, the step from its first group's start to its
+    # last group's end
+    phase = {"h2d": round(sum(span) / K, 3),
              "step": round(sum(step_begin[k].elapsed_time(step_done[k][-1]) for k in range(K)) / K, 3),
              "d2h": round(sum(d2h_begin[k][g].elapsed_time(d2h_done[k][g]) for k in range(K) for g in range(G)) / K, 3)}
     h2d = sum((b - a) for _, a, b in groups) * g_host.element_size()
@@ -1083,13 +1132,20 @@ def run_e2e(args, step_fn, prepare_set, params, flat, t, total, dist: Dist, grou
                           "one library call per step; main_grad and bf16 model buffers one copy per direction") +
                          "; buffers double-buffered; H2D, compute and D2H on three streams; the first step's "
                          "first H2D and the last step's last D2H are not overlapped and are included",
-            "h2d_by": "SM loads of the pinned host buffers (opt_copy_from_host, 32 CTAs) on its own stream; "
-                      "D2H by the copy engines",
+            "h2d_by": "two paths at once, each a share of every segment: the copy engines and SM loads of the "
+                      "pinned host buffers (opt_copy_from_host), on two streams; each step the copy engines take "
+                      "what they moved per ms on the step two back times 0.9 of its compute time, the SM loads "
+                      "the rest (5-95 %, at most two steps in flight); D2H by the copy engines",
+            "h2d_paths": {"sm_share": {"first": round(shares[0], 3), "median": round(statistics.median(shares), 3),
+                                       "min": round(min(shares), 3), "max": round(max(shares), 3)},
+                          "sm_gbs_median": med([r[0] for r in path_gbs if r[0]]),
+                          "copy_engine_gbs_median": med([r[1] for r in path_gbs if r[1]])},
             "host_buffers": f"one cudaHostAlloc arena of {arena.nbytes} bytes (torch pinned memory); "
                             "copies warmed once before timing",
             "host_wall_ms_per_step": round(wall_ms / K, 3),
             "host_enqueue_ms_per_step": {"h2d": round(host_ms[0] / K, 3), "step": round(host_ms[1] / K, 3),
                                          "d2h": round(host_ms[2] / K, 3)},
+            "host_wait_ms_per_step": round(host_ms[3] / K, 3),
             "device_ms_per_step": phase,
             "h2d_gbs": round(h2d / (phase["h2d"] * 1e6), 1) if phase["h2d"] > 0 else None,
             "d2h_gbs": round(d2h / (phase["d2h"] * 1e6), 1) if phase["d2h"] > 0 else None,
