@@ -666,7 +666,8 @@ def run_ours(args, dist: Dist):
 
     # ---- end to end through the public API with host buffers
     grouped = None if (args.shard or args.clip > 0) else group_step
-    line["e2e"] = run_e2e(args, step, prepare_set, params, flat, t, total, dist, grouped)
+    line["e2e"] = run_e2e(args, step, prepare_set, params, flat, t, total, dist, grouped,
+                          step_ms=elapsed_ms / args.steps)
     t += args.e2e_steps
     line["clocks"] = clocks.summary()
     if args.compare_cublas and dist.rank == 0:
@@ -917,7 +918,18 @@ def adamw_buckets(params, hp, reps=5):
     return out
 
 
-def run_e2e(args, step_fn, prepare_set, params, flat, t, total, dist: Dist, group_step=None):
+def h2d_sm_share(r_sm, r_ce, t_budget_ms, need_bytes):
+    """Share of a step's H2D bytes for the SM loads, the rest going to the
+    copy engines, from each path's rate (bytes per ms) on an earlier step:
+    the copy engines take what they move in 0.9 of the time budget; when that
+    would leave the SM loads the longer of the two, the shares are set for
+    both to finish together.  Kept within [0.05, 0.95]."""
+    ce_first = 1.0 - 0.9 * r_ce * t_budget_ms / need_bytes
+    balanced = r_sm / (r_sm + r_ce)
+    return min(max(min(ce_first, balanced), 0.05), 0.95)
+
+
+def run_e2e(args, step_fn, prepare_set, params, flat, t, total, dist: Dist, group_step=None, step_ms=None):
     """The same step through the public API, with main_grad arriving from
     pinned host memory and the bf16 model parameters read back to host
     memory, every step, inside the timed region.
@@ -968,10 +980,12 @@ def run_e2e(args, step_fn, prepare_set, params, flat, t, total, dist: Dist, grou
     # drop, with the pages, over time and from host to host, and the two share
     # one limit of about 200 GB/s.  The copies need only keep up with the
     # compute, and the SM loads slow the compute more than the copy engines
-    # do: each step gives the copy engines what they moved per ms on the step
-    # two back (finished by then) times 0.9 of that step's compute time, and
-    # the SM loads the rest (at least 5 % each, so both rates stay measured).
-    # D2H: the copy engines.
+    # do.  Each step uses the rates the two paths reached on the step two back
+    # (finished by then): the copy engines get what they move in 0.9 of the
+    # device-resident step time and the SM loads the rest; when that would
+    # leave the SM loads the longer of the two, the shares are set for both
+    # paths to finish together instead.  At least 5 % each, so that both
+    # rates stay measured.  D2H: the copy engines.
     s_sm, s_ce, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
     sm_copy = lambda dst, src, st: mp.copy_from_host(dst, src, stream=st)
     ce_copy = lambda dst, src, st: dst.copy_(src, non_blocking=True)
@@ -1012,7 +1026,6 @@ def run_e2e(args, step_fn, prepare_set, params, flat, t, total, dist: Dist, grou
     idle_gbs = {"h2d": round(nb_g / (warm[0].elapsed_time(warm[1]) * 1e6), 1),
                 "d2h": round(b_host.numel() * b_host.element_size() / (warm[2].elapsed_time(warm[3]) * 1e6), 1),
                 "h2d_copy_engine": round(nb_g / (warm[4].elapsed_time(warm[5]) * 1e6), 1)}
-    clamp = lambda f: min(max(f, 0.05), 0.95)
     f_sm = 0.5
     need = sum(b - a for _, a, b in groups) * g_host.element_size()
     shares, cuts = [], [[None] * G for _ in range(K)]
@@ -1041,9 +1054,10 @@ def run_e2e(args, step_fn, prepare_set, params, flat, t, total, dist: Dist, grou
             # at most two steps in flight: step k-2's compute (and so its
             # copies) has finished, and its copy rates set this step's shares
             step_done[k - 2][G - 1].synchronize()
-            _, r_ce = rates(k - 2)
-            if r_ce:
-                f_sm = clamp(1.0 - 0.9 * r_ce * step_begin[k - 2].elapsed_time(step_done[k - 2][G - 1]) / need)
+            r_sm, r_ce = rates(k - 2)
+            if r_sm and r_ce:
+                t_budget = step_ms if step_ms else step_begin[k - 2].elapsed_time(step_done[k - 2][G - 1])
+                f_sm = h2d_sm_share(r_sm, r_ce, t_budget, need)
         h0 = time.perf_counter()
         host_ms[3] += (h0 - hw) * 1e3
         shares.append(f_sm)
@@ -1133,9 +1147,9 @@ def run_e2e(args, step_fn, prepare_set, params, flat, t, total, dist: Dist, grou
                          "; buffers double-buffered; H2D, compute and D2H on three streams; the first step's "
                          "first H2D and the last step's last D2H are not overlapped and are included",
             "h2d_by": "two paths at once, each a share of every segment: the copy engines and SM loads of the "
-                      "pinned host buffers (opt_copy_from_host), on two streams; each step the copy engines take "
-                      "what they moved per ms on the step two back times 0.9 of its compute time, the SM loads "
-                      "the rest (5-95 %, at most two steps in flight); D2H by the copy engines",
+                      "pinned host buffers (opt_copy_from_host), on two streams; from the rates of the step two "
+                      "back, the SM share is min(1 - 0.9 r_ce T / bytes, r_sm / (r_sm + r_ce)), T the "
+                      "device-resident step time (5-95 %, at most two steps in flight); D2H by the copy engines",
             "h2d_paths": {"sm_share": {"first": round(shares[0], 3), "median": round(statistics.median(shares), 3),
                                        "min": round(min(shares), 3), "max": round(max(shares), 3)},
                           "sm_gbs_median": med([r[0] for r in path_gbs if r[0]]),

@@ -232,3 +232,18 @@ def test_flat_buffers_hold_step_groups_contiguously():
             assert a <= off and off + params[i].main_grad.numel() <= b
             assert (params[i].model.data_ptr() - flat["model"].data_ptr()) // 2 == off
     assert n_muon + n_adamw == w.numel
+
+
+def test_h2d_share_rule():
+    """The e2e leg's split of each step's gradients between the copy engines
+    and SM loads: copy engines first while they keep up with the step,
+    balanced when neither path alone does, never below 5 % for either."""
+    need, T = 18.2e9, 118.0                              # bytes per step, ms
+    assert bench.h2d_sm_share(200e6, 200e6, T, need) == 0.05         # copy engines cover the step
+    f = bench.h2d_sm_share(200e6, 30e6, T, need)                      # slow copy engines
+    assert abs(f - (1 - 0.9 * 30e6 * T / need)) < 1e-12
+    assert (1 - f) * need / 30e6 <= 0.9 * T + 1e-9 and f * need / 200e6 < 0.9 * T
+    f = bench.h2d_sm_share(100e6, 50e6, T, need)                      # both slow: finish together
+    assert abs(f - 100 / 150) < 1e-12
+    assert abs(f * need / 100e6 - (1 - f) * need / 50e6) < 1e-6
+    assert bench.h2d_sm_share(200e6, 1e3, T, need) == 0.95            # copy engines all but stalled
