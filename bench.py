@@ -1026,8 +1026,12 @@ def run_e2e(args, step_fn, prepare_set, params, flat, t, total, dist: Dist, grou
     idle_gbs = {"h2d": round(nb_g / (warm[0].elapsed_time(warm[1]) * 1e6), 1),
                 "d2h": round(b_host.numel() * b_host.element_size() / (warm[2].elapsed_time(warm[3]) * 1e6), 1),
                 "h2d_copy_engine": round(nb_g / (warm[4].elapsed_time(warm[5]) * 1e6), 1)}
-    f_sm = 0.5
     need = sum(b - a for _, a, b in groups) * g_host.element_size()
+    # first shares from the idle rates; later ones from the rates of the step
+    # two back, each path's rate smoothed over the steps and each change of
+    # the share halved (a path's rate varies with the pages it reads)
+    r_avg = [idle_gbs["h2d"] * 1e6, idle_gbs["h2d_copy_engine"] * 1e6]     # bytes per ms
+    f_sm = h2d_sm_share(r_avg[0], r_avg[1], step_ms, need) if step_ms else 0.5
     shares, cuts = [], [[None] * G for _ in range(K)]
 
     def rates(j):
@@ -1054,10 +1058,11 @@ def run_e2e(args, step_fn, prepare_set, params, flat, t, total, dist: Dist, grou
             # at most two steps in flight: step k-2's compute (and so its
             # copies) has finished, and its copy rates set this step's shares
             step_done[k - 2][G - 1].synchronize()
-            r_sm, r_ce = rates(k - 2)
-            if r_sm and r_ce:
+            r_now = rates(k - 2)
+            if r_now[0] and r_now[1]:
+                r_avg = [0.5 * a + 0.5 * b for a, b in zip(r_avg, r_now)]
                 t_budget = step_ms if step_ms else step_begin[k - 2].elapsed_time(step_done[k - 2][G - 1])
-                f_sm = h2d_sm_share(r_sm, r_ce, t_budget, need)
+                f_sm = 0.5 * f_sm + 0.5 * h2d_sm_share(r_avg[0], r_avg[1], t_budget, need)
         h0 = time.perf_counter()
         host_ms[3] += (h0 - hw) * 1e3
         shares.append(f_sm)
@@ -1147,13 +1152,17 @@ def run_e2e(args, step_fn, prepare_set, params, flat, t, total, dist: Dist, grou
                          "; buffers double-buffered; H2D, compute and D2H on three streams; the first step's "
                          "first H2D and the last step's last D2H are not overlapped and are included",
             "h2d_by": "two paths at once, each a share of every segment: the copy engines and SM loads of the "
-                      "pinned host buffers (opt_copy_from_host), on two streams; from the rates of the step two "
-                      "back, the SM share is min(1 - 0.9 r_ce T / bytes, r_sm / (r_sm + r_ce)), T the "
-                      "device-resident step time (5-95 %, at most two steps in flight); D2H by the copy engines",
+                      "pinned host buffers (opt_copy_from_host), on two streams; the SM share moves halfway "
+                      "each step towards min(1 - 0.9 r_ce T / bytes, r_sm / (r_sm + r_ce)), T the device-resident "
+                      "step time, r each path's rate averaged over the steps up to two back (first step: idle "
+                      "rates; 5-95 %, at most two steps in flight); D2H by the copy engines",
             "h2d_paths": {"sm_share": {"first": round(shares[0], 3), "median": round(statistics.median(shares), 3),
                                        "min": round(min(shares), 3), "max": round(max(shares), 3)},
                           "sm_gbs_median": med([r[0] for r in path_gbs if r[0]]),
-                          "copy_engine_gbs_median": med([r[1] for r in path_gbs if r[1]])},
+                          "copy_engine_gbs_median": med([r[1] for r in path_gbs if r[1]]),
+                          "by_step": [[round(f, 3), round(r[0] or 0, 1), round(r[1] or 0, 1)]
+                                      for f, r in zip(shares, path_gbs)],
+                          "by_step_fields": ["sm_share", "sm_gbs", "copy_engine_gbs"]},
             "host_buffers": f"one cudaHostAlloc arena of {arena.nbytes} bytes (torch pinned memory); "
                             "copies warmed once before timing",
             "host_wall_ms_per_step": round(wall_ms / K, 3),

@@ -46,9 +46,12 @@ def snapshot(params):
     return out
 
 
-@pytest.mark.parametrize("clip", [0.0, 0.5])
-def test_captured_step_replays_bit_exact(clip):
-    hm = mp.muon_hp(lr=0.02, momentum=0.95)
+@pytest.mark.parametrize("clip,order", [(0.0, "auto"), (0.5, "auto"), (0.0, "grouped")])
+def test_captured_step_replays_bit_exact(clip, order):
+    """Eager steps and the replays of a captured step give the same bits, with
+    the iterations evaluated one by one and in groups (whose launches rotate
+    four square buffers)."""
+    hm = mp.muon_hp(lr=0.02, momentum=0.95, ns_order=order)
     ha = mp.adamw_hp(lr=1e-3, weight_decay=0.1, step=1)
 
     def step(params, ws):
@@ -58,7 +61,7 @@ def test_captured_step_replays_bit_exact(clip):
             mp.mixed_step(params, hm, ha, ws)
 
     eager, captured = make_params(), make_params()
-    nbytes = mp.workspace_size(eager, clip=clip > 0)
+    nbytes = mp.workspace_size(eager, clip=clip > 0, ns_order=order)
     ws_e = mp.alloc_workspace(nbytes)
     ws_c = mp.alloc_workspace(nbytes)
     reps = 3
