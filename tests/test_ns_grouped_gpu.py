@@ -245,3 +245,34 @@ def test_launches_follow_the_plan(case):
               for i in range(hp.ns_steps)] if hp.ns_schedule else OM.NS_COEFFS
     Wn, _, _ = OM.muon_step(W, g, m, lr=0.02, momentum=0.95, ns_steps=hp.ns_steps, coeffs=coeffs)
     assert rel(W.astype(np.float64) - W1, W.astype(np.float64) - Wn) < NS_TOL
+
+
+@pytest.mark.parametrize("case", ["more_than_64", "workspace_for_two"])
+def test_grouped_batches(case):
+    """A class of 70 matrices runs as batches of at most 64; a workspace with
+    room for the grouped buffers of two matrices runs five matrices two at a
+    time.  Every matrix matches the oracle, and the launches show the batches."""
+    shape = (96, 200)
+    n = 70 if case == "more_than_64" else 5
+    rng = np.random.default_rng(n)
+    Ws = [(rng.standard_normal(shape) * 0.02).astype(np.float32) for _ in range(n)]
+    gs = [(rng.standard_normal(shape) * 1e-2).astype(np.float32) for _ in range(n)]
+    params = [mp.Param(dev(W), dev(g), torch.zeros(shape, device="cuda"), None,
+                       torch.zeros(shape, dtype=torch.bfloat16, device="cuda")) for W, g in zip(Ws, gs)]
+    hp = mp.muon_hp(ns_order="grouped")
+    if case == "more_than_64":
+        nbytes = mp.workspace_size(params, "muon", ns_order="grouped")
+        batches = [64, 6]
+    else:
+        nbytes = mp.workspace_size(params[:2], "muon", ns_order="grouped")
+        batches = [2, 2, 1]
+    ws = mp.alloc_workspace(nbytes)
+    with mp.LaunchProfiler(1024) as prof:
+        mp.mixed_step(params, hp, None, ws)
+    torch.cuda.synchronize()
+    assert mp.device_status(ws) == mp.OPT_OK
+    bx = [r["count"] for r in prof.records() if r["kernel"] == "ns_bx"]
+    assert bx == [b for b in batches for _ in range(2)]          # two groups of iterations per batch
+    for W, g, p in zip(Ws, gs, params):
+        Wn, _, _ = OM.muon_step(W, g, np.zeros(shape, np.float32), lr=0.02, momentum=0.95)
+        check_update(shape, W, host(p.main_param), Wn, 0.02)
