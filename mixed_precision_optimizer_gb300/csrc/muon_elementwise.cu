@@ -234,7 +234,7 @@ muon_prologue_kernel(const MuonGroup grp, NsBuffers buf, MuonScalars s) {
     mq[k] = gq[k];
     if (r < R && vec && c + 3 < C) {
       const int64_t i = r * C + c;
-      gq[k] = __ldcs(reinterpret_cast<const float4*>(M.g + i));   // read once: evict first
+      gq[k] = *reinterpret_cast<const float4*>(M.g + i);
       if (!s.ns_only) mq[k] = *reinterpret_cast<const float4*>(M.m + i);
     }
   }
@@ -262,7 +262,7 @@ muon_prologue_kernel(const MuonGroup grp, NsBuffers buf, MuonScalars s) {
           m.y = m.y + s.one_minus_mu * (g.y - m.y);
           m.z = m.z + s.one_minus_mu * (g.z - m.z);
           m.w = m.w + s.one_minus_mu * (g.w - m.w);
-          __stcs(reinterpret_cast<float4*>(M.m + i), m);   // not read again this step
+          *reinterpret_cast<float4*>(M.m + i) = m;
           val[0] = gtilde(s, g.x, m.x);
           val[1] = gtilde(s, g.y, m.y);
           val[2] = gtilde(s, g.z, m.z);
