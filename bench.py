@@ -938,9 +938,10 @@ def run_e2e(args, step_fn, prepare_set, params, flat, t, total, dist: Dist, grou
     bf16 model copies, laid out group by group (build_device_workload).  With
     `group_step` each step is one library call per step group (a Muon shape
     class, or the AdamW tensors), and each group's gradients are one
-    host-to-device copy and its model copies one device-to-host copy: a
-    group's compute starts as soon as its own gradients have landed, and its
-    model copy leaves while the next group computes.  Without it (sharded or
+    host-to-device segment (shared between the copy engines and SM loads,
+    below) and its model copies one device-to-host copy: a group's compute
+    starts as soon as its own gradients have landed, and its model copy
+    leaves while the next group computes.  Without it (sharded or
     clipped steps, whose calls span every tensor) a step is one call and each
     direction one copy.  The copies are pipelined across steps too: both
     buffers are double-buffered on the device, step k uses set k % 2, and
