@@ -70,6 +70,8 @@ def parse():
                          "matrix, bf16 exchange by broadcasts); total work fixed as N grows (strong scaling)")
     ap.add_argument("--no-sweep", action="store_true",
                     help="skip the AdamW size sweep (10,000 tensors, GB/s per size decade) after the main workload")
+    ap.add_argument("--ns-order", choices=["auto", "per_iteration", "grouped"], default="auto",
+                    help="evaluation order of the Newton-Schulz iterations (opt_muon_hp.flags)")
     ap.add_argument("--clock-log", default=None, help="directory for the nvidia-smi clock samples (default: temp)")
     return ap.parse_args()
 
@@ -296,12 +298,12 @@ def build_device_workload(w: S.Workload, device):
     return params, n_muon, n_adamw, flat
 
 
-def hyper(w: S.Workload):
+def hyper(w: S.Workload, ns_order="auto"):
     import mixed_precision_optimizer_gb300 as mp
     hm = None
     if w.muon is not None:
         hm = mp.muon_hp(lr=w.muon.lr, momentum=w.muon.momentum, weight_decay=w.muon.weight_decay,
-                        nesterov=w.muon.nesterov, ns_steps=w.muon.ns_steps)
+                        nesterov=w.muon.nesterov, ns_steps=w.muon.ns_steps, ns_order=ns_order)
 
     def ha(t):
         if w.adamw is None:
@@ -581,7 +583,7 @@ def run_ours(args, dist: Dist):
     w = S.WORKLOADS[args.workload]()
     params, n_muon, n_adamw, flat = build_device_workload(w, device)
     total = n_muon + n_adamw
-    hm, ha = hyper(w)
+    hm, ha = hyper(w, args.ns_order)
     if args.shard:
         # this rank keeps the replicated main_grad and bf16 model of every
         # tensor, and master/state only for what the plan gives it
@@ -605,7 +607,7 @@ def run_ours(args, dist: Dist):
             sh.sharded_step(pset[0], plan, state, hm, ha(t), ws, prepared=pset[1])
     else:
         prepare_set = mp.prepare
-        ws = mp.alloc_workspace(mp.workspace_size(params, clip=args.clip > 0), device)
+        ws = mp.alloc_workspace(mp.workspace_size(params, clip=args.clip > 0, ns_order=args.ns_order), device)
         prepared = mp.prepare(params)
 
         def step(t, plist=None):
@@ -788,6 +790,7 @@ def measured_line(args, w, recs, launches, elapsed_ms, total, dist, peaks, peak_
         "config": cfg,
         "parallelism": (f"sharded x{dist.world} (ZeRO-1 AdamW, one owner per Muon matrix)" if shard
                         else f"replicas x{dist.world}" if dist.world > 1 else "1 GPU"),
+        "ns_order": getattr(args, "ns_order", "auto"),
         "adamw_gbs": kern_out.get("adamw", {}).get("gbs"),
         "ns_tflops_method": roofline.get("achieved") if roofline["bound"] == "tensor" else None,
         "roofline": roofline,
