@@ -418,3 +418,41 @@ def test_plain_momentum_sgd():
     Wn, mn, _ = OM.muon_step(W, g, m, lr=0.1, momentum=0.5, orthogonalize=False, scale_coeff=1.0)
     # m = 0.5 * 2 = 1; gtilde = lerp(2, 1, 0.5) = 1.5
     assert np.allclose(mn, 1.0) and np.allclose(Wn, 1 - 0.1 * 1.5)
+
+
+@pytest.mark.parametrize("sizes", [[3, 2], [2, 2, 1], [1, 2, 2], [5], [2, 3]])
+@pytest.mark.parametrize("shape", [(64, 200), (200, 64), (96, 96)])
+def test_grouped_iterations_are_exact_algebra(sizes, shape):
+    """The grouped evaluation of the Newton-Schulz iterations (reading R20 of
+    the design): within a group every C_k = a I + b A_k + c A_k^2 is a
+    polynomial in the group's first Gram matrix, so A_{k+1} = C_k (A_k C_k)
+    and X_{k0+g} = (C_{k0+g-1} ... C_k0) X_k0.  In fp64 that equals the
+    iteration as printed ("优化器：AdamW、Muon 与分布式优化器", newton_schulz)
+    to rounding, for every split of the five iterations and for a
+    coefficient schedule."""
+    rng = np.random.default_rng(sum(sizes) * 1000 + shape[0])
+    G = rng.standard_normal(shape)
+    for coeffs in (OM.NS_COEFFS, [(3.4445, -4.775, 2.0315), (3.2, -4.4, 1.9), (3.0, -4.0, 1.7),
+                                  (2.8, -3.6, 1.55), (2.2, -2.1, 0.9)]):
+        sched = [tuple(coeffs)] * 5 if np.isscalar(coeffs[0]) else list(coeffs)
+        X = G / (np.linalg.norm(G) + 1e-7)
+        tr = shape[0] > shape[1]
+        if tr:
+            X = X.T
+        I = np.eye(X.shape[0])
+        k = 0
+        for g in sizes:
+            A = X @ X.T
+            a, b, c = sched[k]
+            C = a * I + b * A + c * (A @ A)
+            M = C
+            for j in range(1, g):
+                A = C @ (A @ C)
+                a, b, c = sched[k + j]
+                C = a * I + b * A + c * (A @ A)
+                M = C @ M
+            X = M @ X
+            k += g
+        got = X.T if tr else X
+        want = OM.newton_schulz(G, 5, coeffs)
+        assert np.abs(got - want).max() <= 1e-10 * np.abs(want).max()
