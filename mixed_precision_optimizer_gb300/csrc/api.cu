@@ -388,9 +388,10 @@ bool wants_grouped(const MuonPlanHp& hp, int64_t A, int64_t B) {
 // maps s to s |p_k(s^2)|.  The normalised input has every singular value in
 // [0, 1], so the values iteration k can see lie in [0, S_k] with S_0 = 1 and
 // S_{k+1} = max over [0, S_k] of s |p_k(s^2)|; the largest eigenvalue of M is
-// at most the product of max |p_k| over [0, S_k] (41 for the printed
-// coefficients).  A group whose bound exceeds kNsGroupBound (16x below
-// fp16's 65504) is split into single iterations.
+// at most the product of max |p_k| over [0, S_k] (3.44^3 = 41 for three
+// iterations of the printed coefficients, about 42 with the grid's 1 %
+// margin).  A group whose bound exceeds kNsGroupBound (16x below fp16's
+// 65504) is split into single iterations.
 constexpr double kNsGroupBound = 4096.0;
 
 std::vector<int> fp16_safe_groups(const std::vector<int>& sizes, const MuonScalars& s, int ns_steps) {
