@@ -984,12 +984,12 @@ def run_e2e(args, step_fn, prepare_set, params, flat, t, total, dist: Dist, grou
     # drop, with the pages, over time and from host to host, and the two share
     # one limit of about 200 GB/s.  The copies need only keep up with the
     # compute, and the SM loads slow the compute more than the copy engines
-    # do.  Each step uses the rates the two paths reached on the step two back
-    # (finished by then): the copy engines get what they move in 0.9 of the
-    # device-resident step time and the SM loads the rest; when that would
-    # leave the SM loads the longer of the two, the shares are set for both
-    # paths to finish together instead.  At least 5 % each, so that both
-    # rates stay measured.  D2H: the copy engines.
+    # do.  Each step uses the rates the two paths reached on earlier steps
+    # (the step two back is finished by then): the copy engines get what they
+    # move in 0.9 of the device-resident step time and the SM loads the rest;
+    # when that would leave the SM loads the longer of the two, the shares are
+    # set for both paths to finish together instead.  At least 5 % each, so
+    # that both rates stay measured.  D2H: the copy engines.
     s_sm, s_ce, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
     sm_copy = lambda dst, src, st: mp.copy_from_host(dst, src, stream=st)
     ce_copy = lambda dst, src, st: dst.copy_(src, non_blocking=True)
@@ -1031,11 +1031,12 @@ def run_e2e(args, step_fn, prepare_set, params, flat, t, total, dist: Dist, grou
                 "d2h": round(b_host.numel() * b_host.element_size() / (warm[2].elapsed_time(warm[3]) * 1e6), 1),
                 "h2d_copy_engine": round(nb_g / (warm[4].elapsed_time(warm[5]) * 1e6), 1)}
     need = sum(b - a for _, a, b in groups) * g_host.element_size()
-    # first shares from the idle rates; later ones from the rates of the step
-    # two back, each path's rate smoothed over the steps and each change of
-    # the share halved (a path's rate varies with the pages it reads)
-    r_avg = [idle_gbs["h2d"] * 1e6, idle_gbs["h2d_copy_engine"] * 1e6]     # bytes per ms
-    f_sm = h2d_sm_share(r_avg[0], r_avg[1], step_ms, need) if step_ms else 0.5
+    # first shares from the idle rates; later ones from each path's slowest
+    # rate over its last three measured steps (a path's rate can swing several
+    # fold from step to step with the pages it reads, and a step lasts as long
+    # as its slower path)
+    hist = [[idle_gbs["h2d"] * 1e6], [idle_gbs["h2d_copy_engine"] * 1e6]]     # bytes per ms
+    f_sm = h2d_sm_share(hist[0][0], hist[1][0], step_ms, need) if step_ms else 0.5
     shares, cuts = [], [[None] * G for _ in range(K)]
 
     def rates(j):
@@ -1064,9 +1065,10 @@ def run_e2e(args, step_fn, prepare_set, params, flat, t, total, dist: Dist, grou
             step_done[k - 2][G - 1].synchronize()
             r_now = rates(k - 2)
             if r_now[0] and r_now[1]:
-                r_avg = [0.5 * a + 0.5 * b for a, b in zip(r_avg, r_now)]
+                for h, r in zip(hist, r_now):
+                    h.append(r)
                 t_budget = step_ms if step_ms else step_begin[k - 2].elapsed_time(step_done[k - 2][G - 1])
-                f_sm = 0.5 * f_sm + 0.5 * h2d_sm_share(r_avg[0], r_avg[1], t_budget, need)
+                f_sm = h2d_sm_share(min(hist[0][-3:]), min(hist[1][-3:]), t_budget, need)
         h0 = time.perf_counter()
         host_ms[3] += (h0 - hw) * 1e3
         shares.append(f_sm)
@@ -1156,10 +1158,10 @@ def run_e2e(args, step_fn, prepare_set, params, flat, t, total, dist: Dist, grou
                          "; buffers double-buffered; H2D, compute and D2H on three streams; the first step's "
                          "first H2D and the last step's last D2H are not overlapped and are included",
             "h2d_by": "two paths at once, each a share of every segment: the copy engines and SM loads of the "
-                      "pinned host buffers (opt_copy_from_host), on two streams; the SM share moves halfway "
-                      "each step towards min(1 - 0.9 r_ce T / bytes, r_sm / (r_sm + r_ce)), T the device-resident "
-                      "step time, r each path's rate averaged over the steps up to two back (first step: idle "
-                      "rates; 5-95 %, at most two steps in flight); D2H by the copy engines",
+                      "pinned host buffers (opt_copy_from_host), on two streams; the SM share is "
+                      "min(1 - 0.9 r_ce T / bytes, r_sm / (r_sm + r_ce)), T the device-resident step time, r each "
+                      "path's slowest rate over its last three measured steps (the newest two back; first steps: "
+                      "idle rates; 5-95 %, at most two steps in flight); D2H by the copy engines",
             "h2d_paths": {"sm_share": {"first": round(shares[0], 3), "median": round(statistics.median(shares), 3),
                                        "min": round(min(shares), 3), "max": round(max(shares), 3)},
                           "sm_gbs_median": med([r[0] for r in path_gbs if r[0]]),
