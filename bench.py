@@ -1021,9 +1021,6 @@ def run_e2e(args, step_fn, prepare_set, params, flat, t, total, dist: Dist, grou
             b_host.copy_(bd, non_blocking=True)
             if i == 0:
                 warm[3].record(s_out)
-    ev = lambda: [[E() for _ in range(G)] for _ in range(K)]
-    sm_b, sm_e, ce_b, ce_e, step_done, d2h_begin, d2h_done = (ev() for _ in range(7))
-    step_begin = [E() for _ in range(K)]
     start = E()
     torch.cuda.synchronize()
     nb_g = g_host.numel() * g_host.element_size()
@@ -1036,77 +1033,102 @@ def run_e2e(args, step_fn, prepare_set, params, flat, t, total, dist: Dist, grou
     # fold from step to step with the pages it reads, and a step lasts as long
     # as its slower path)
     hist = [[idle_gbs["h2d"] * 1e6], [idle_gbs["h2d_copy_engine"] * 1e6]]     # bytes per ms
-    f_sm = h2d_sm_share(hist[0][0], hist[1][0], step_ms, need) if step_ms else 0.5
-    shares, cuts = [], [[None] * G for _ in range(K)]
+    ctl = {"f_sm": h2d_sm_share(hist[0][0], hist[1][0], step_ms, need) if step_ms else 0.5, "t": t}
 
-    def rates(j):
-        """Bytes per ms of each H2D path on step j (finished)."""
+    def rates(run, j):
+        """Bytes per ms of each H2D path on step j of a run (finished)."""
         out = []
-        for b_ev, e_ev, part in ((sm_b, sm_e, 0), (ce_b, ce_e, 1)):
-            t = sum(b_ev[j][g].elapsed_time(e_ev[j][g]) for g in range(G))
-            n = sum((cuts[j][g][1] - cuts[j][g][0]) if part == 0 else (cuts[j][g][2] - cuts[j][g][1])
-                    for g in range(G)) * g_host.element_size()
-            out.append(n / t if t > 0 and n > 0 else None)
+        for b_ev, e_ev, part in ((run["sm_b"], run["sm_e"], 0), (run["ce_b"], run["ce_e"], 1)):
+            tt = sum(b_ev[j][g].elapsed_time(e_ev[j][g]) for g in range(G))
+            n = sum((run["cuts"][j][g][1] - run["cuts"][j][g][0]) if part == 0 else
+                    (run["cuts"][j][g][2] - run["cuts"][j][g][1]) for g in range(G)) * g_host.element_size()
+            out.append(n / tt if tt > 0 and n > 0 else None)
         return out
 
+    def run_steps(n):
+        """Enqueues n pipelined steps (H2D on two paths, compute, D2H); the
+        shares follow the rates of earlier steps, carried over between runs."""
+        ev = lambda: [[E() for _ in range(G)] for _ in range(n)]
+        run = {k: ev() for k in ("sm_b", "sm_e", "ce_b", "ce_e", "step_done", "d2h_begin", "d2h_done")}
+        run.update(step_begin=[E() for _ in range(n)], cuts=[[None] * G for _ in range(n)], shares=[],
+                   host_ms=[0.0, 0.0, 0.0, 0.0])
+        sm_b, sm_e, ce_b, ce_e = run["sm_b"], run["sm_e"], run["ce_b"], run["ce_e"]
+        step_done, d2h_begin, d2h_done, step_begin = run["step_done"], run["d2h_begin"], run["d2h_done"], \
+            run["step_begin"]
+        host_ms = run["host_ms"]
+        for k in range(n):
+            hw = time.perf_counter()
+            if k >= 2:
+                # at most two steps in flight: step k-2's compute (and so its
+                # copies) has finished, and its copy rates set this step's shares
+                step_done[k - 2][G - 1].synchronize()
+                r_now = rates(run, k - 2)
+                if r_now[0] and r_now[1]:
+                    for h, r in zip(hist, r_now):
+                        h.append(r)
+                    t_budget = step_ms if step_ms else step_begin[k - 2].elapsed_time(step_done[k - 2][G - 1])
+                    ctl["f_sm"] = h2d_sm_share(min(hist[0][-3:]), min(hist[1][-3:]), t_budget, need)
+            h0 = time.perf_counter()
+            host_ms[3] += (h0 - hw) * 1e3
+            f_sm = ctl["f_sm"]
+            run["shares"].append(f_sm)
+            gd, bd = flats[k % 2]
+            for g, (_, a, b) in enumerate(groups):     # gradients of step k, group by group
+                m = a + int((b - a) * f_sm) // 64 * 64
+                run["cuts"][k][g] = (a, m, b)
+                for st, b_ev, e_ev, lo, hi, copy in ((s_sm, sm_b, sm_e, a, m, sm_copy),
+                                                     (s_ce, ce_b, ce_e, m, b, ce_copy)):
+                    with torch.cuda.stream(st):
+                        if k >= 2:
+                            st.wait_event(step_done[k - 2][g])   # step k-2 finished reading this segment
+                        b_ev[k][g].record(st)
+                        if hi > lo:
+                            copy(gd[lo:hi], g_host[lo:hi], st)
+                        e_ev[k][g].record(st)
+            h1 = time.perf_counter()
+            h_step = 0.0
+            for g, (call, a, b) in enumerate(groups):
+                compute.wait_event(sm_e[k][g])
+                compute.wait_event(ce_e[k][g])
+                if k >= 2:
+                    compute.wait_event(d2h_done[k - 2][g])   # model copy of this segment of set k % 2 read back
+                if g == 0:
+                    step_begin[k].record(compute)
+                c0 = time.perf_counter()
+                call(ctl["t"], k % 2)
+                h_step += time.perf_counter() - c0
+                step_done[k][g].record(compute)
+                with torch.cuda.stream(s_out):             # model parameters of this group
+                    s_out.wait_event(step_done[k][g])
+                    d2h_begin[k][g].record(s_out)
+                    b_host[a:b].copy_(bd[a:b], non_blocking=True)
+                    d2h_done[k][g].record(s_out)
+            ctl["t"] += 1
+            h3 = time.perf_counter()
+            host_ms[0] += (h1 - h0) * 1e3
+            host_ms[1] += h_step * 1e3
+            host_ms[2] += ((h3 - h1) - h_step) * 1e3
+        return run
+
+    # untimed: as many e2e steps as the bench's warm-up, through the same
+    # pipeline, so that the copies and the shares settle before timing
+    if args.warmup > 0:
+        for st in (s_sm, s_ce, s_out):
+            st.wait_stream(compute)
+        run_steps(args.warmup)
+        torch.cuda.synchronize()
     clocks = ClockSampler(smi_index(torch.cuda.current_device()), "_e2e").__enter__()
     dist.barrier()
     torch.cuda.synchronize()
     t_wall = time.perf_counter()
-    host_ms = [0.0, 0.0, 0.0, 0.0]
     start.record(compute)
     for st in (s_sm, s_ce, s_out):
         st.wait_event(start)
-    for k in range(K):
-        hw = time.perf_counter()
-        if k >= 2:
-            # at most two steps in flight: step k-2's compute (and so its
-            # copies) has finished, and its copy rates set this step's shares
-            step_done[k - 2][G - 1].synchronize()
-            r_now = rates(k - 2)
-            if r_now[0] and r_now[1]:
-                for h, r in zip(hist, r_now):
-                    h.append(r)
-                t_budget = step_ms if step_ms else step_begin[k - 2].elapsed_time(step_done[k - 2][G - 1])
-                f_sm = h2d_sm_share(min(hist[0][-3:]), min(hist[1][-3:]), t_budget, need)
-        h0 = time.perf_counter()
-        host_ms[3] += (h0 - hw) * 1e3
-        shares.append(f_sm)
-        gd, bd = flats[k % 2]
-        for g, (_, a, b) in enumerate(groups):     # gradients of step k, group by group
-            m = a + int((b - a) * f_sm) // 64 * 64
-            cuts[k][g] = (a, m, b)
-            for st, b_ev, e_ev, lo, hi, copy in ((s_sm, sm_b, sm_e, a, m, sm_copy), (s_ce, ce_b, ce_e, m, b, ce_copy)):
-                with torch.cuda.stream(st):
-                    if k >= 2:
-                        st.wait_event(step_done[k - 2][g])   # step k-2 finished reading this segment
-                    b_ev[k][g].record(st)
-                    if hi > lo:
-                        copy(gd[lo:hi], g_host[lo:hi], st)
-                    e_ev[k][g].record(st)
-        h1 = time.perf_counter()
-        h_step = 0.0
-        for g, (call, a, b) in enumerate(groups):
-            compute.wait_event(sm_e[k][g])
-            compute.wait_event(ce_e[k][g])
-            if k >= 2:
-                compute.wait_event(d2h_done[k - 2][g])   # model copy of this segment of set k % 2 read back
-            if g == 0:
-                step_begin[k].record(compute)
-            c0 = time.perf_counter()
-            call(t, k % 2)
-            h_step += time.perf_counter() - c0
-            step_done[k][g].record(compute)
-            with torch.cuda.stream(s_out):             # model parameters of this group
-                s_out.wait_event(step_done[k][g])
-                d2h_begin[k][g].record(s_out)
-                b_host[a:b].copy_(bd[a:b], non_blocking=True)
-                d2h_done[k][g].record(s_out)
-        t += 1
-        h3 = time.perf_counter()
-        host_ms[0] += (h1 - h0) * 1e3
-        host_ms[1] += h_step * 1e3
-        host_ms[2] += ((h3 - h1) - h_step) * 1e3
+    run = run_steps(K)
+    sm_b, sm_e, ce_b, ce_e = run["sm_b"], run["sm_e"], run["ce_b"], run["ce_e"]
+    step_done, d2h_begin, d2h_done, step_begin = run["step_done"], run["d2h_begin"], run["d2h_done"], \
+        run["step_begin"]
+    host_ms, shares = run["host_ms"], run["shares"]
     torch.cuda.synchronize()
     wall_ms = (time.perf_counter() - t_wall) * 1e3
     clocks.__exit__(None, None, None)
@@ -1135,7 +1157,7 @@ def run_e2e(args, step_fn, prepare_set, params, flat, t, total, dist: Dist, grou
             min(min(at(sm_b[k][g]), at(ce_b[k][g])) for g in range(G)) for k in range(K)]
     seg_bytes = [(b - a) * g_host.element_size() for _, a, b in groups]
     step_gbs = sorted(sum(seg_bytes) / (span[k] * 1e6) for k in range(K))
-    path_gbs = [[r / 1e6 if r else None for r in rates(k)] for k in range(K)]
+    path_gbs = [[r / 1e6 if r else None for r in rates(run, k)] for k in range(K)]
     med = lambda xs: round(statistics.median(xs), 1) if xs else None
     # device time of each phase per step: the H2D span above, the D2H copies
     # summed over the groups, the step from its first group's start to its
@@ -1150,7 +1172,7 @@ def run_e2e(args, step_fn, prepare_set, params, flat, t, total, dist: Dist, grou
     per_step = total * (1 if getattr(args, "shard", False) else dist.world)
     return {"value": round(per_step * K / (ms * 1e-3), 1), "unit": UNIT,
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-            "steps": K, "ms_per_step": round(ms / K, 3),
+            "steps": K, "warmup_steps": max(args.warmup, 0), "ms_per_step": round(ms / K, 3),
             "calls_per_step": G,
             "pipelined": ("one library call per step group (each Muon shape class, the AdamW tensors), each "
                           "group's gradients one H2D copy and its bf16 model copies one D2H copy" if G > 1 else
